@@ -1,0 +1,146 @@
+/*
+ * gemm_oracle.c -- CPU oracle for the fp16 -> fp32 product Out = A @ B.T.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * execute this file; only the tests, the package smoke check and the timed
+ * CPU baseline of the benchmark use it.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * What it computes (the plain definition, written out):
+ *   "Warp Matrix Instructions", opening paragraph: the warp example computes
+ *   Out = A @ B.T with A (16,16) and B (8,16) float16 and float32 accumulation.
+ *   "Blackwell Tensor Cores", section "The Accumulator's Lifetime": the same
+ *   product for A (128,64), B (64,64), accumulated in TMEM as float32.
+ * The oracle accumulates in IEEE double instead of float32, so that it is
+ * closer to the exact sum than any fp32 implementation:
+ *   ref[b,i,j]    = sum_{k<K} dbl(A[b,i,k]) * dbl(B[b,j,k])   (sequential k)
+ *   absdot[b,i,j] = sum_{k<K} |dbl(A[b,i,k]) * dbl(B[b,j,k])|
+ * Each product of two fp16 values is exact in double (11+11 significant bits),
+ * so the only rounding is in the k-sequential double additions.
+ *
+ * The fp16 decoder below follows the IEEE 754 binary16 definition: 1 sign bit,
+ * 5 exponent bits with bias 15, 10 fraction bits; exponent 0 encodes zero and
+ * subnormals (fraction * 2^-24), exponent 31 encodes Inf (fraction 0) or NaN.
+ *
+ * Build (done by oracle/build.py):
+ *   gcc -O2 -fopenmp -shared -fPIC -o oracle/_build/liboracle.so oracle/gemm_oracle.c
+ * No -ffast-math: the summation order and IEEE semantics must be kept.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* 2^e as a double, built from its bit pattern (exact for -1022 <= e <= 1023). */
+static double pow2i(int e)
+{
+    uint64_t bits = (uint64_t)(e + 1023) << 52;
+    double d;
+    memcpy(&d, &bits, sizeof d);
+    return d;
+}
+
+/* IEEE 754 binary16 -> double, exact. */
+double oracle_half_to_double(uint16_t h)
+{
+    const unsigned sign = (h >> 15) & 1u;
+    const unsigned expo = (h >> 10) & 0x1fu;
+    const unsigned frac = h & 0x3ffu;
+    double v;
+    if (expo == 0) {
+        /* zero or subnormal: frac * 2^(1-15-10) */
+        v = (double)frac * pow2i(-24);
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        /* normal: (1 + frac/1024) * 2^(expo-15) = (1024 + frac) * 2^(expo-25) */
+        v = (double)(1024u + frac) * pow2i((int)expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* Decode n fp16 bit patterns to double (vectorised convenience for Python). */
+void oracle_half_to_double_array(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = oracle_half_to_double(src[t]);
+}
+
+/* One output element: dot product of row i of A with row j of B over K. */
+static void dot_nt(const uint16_t *a_row, const uint16_t *b_row, int64_t K,
+                   double *ref, double *absdot)
+{
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double p = oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k]);
+        acc += p;
+        aacc += fabs(p);
+    }
+    *ref = acc;
+    if (absdot)
+        *absdot = aacc;
+}
+
+/*
+ * Full batched product.  All sizes and strides are in elements.
+ *   A   : batch x M x K, row stride lda, batch stride sA
+ *   B   : batch x N x K, row stride ldb, batch stride sB
+ *   ref : batch x M x N, row stride ldr, batch stride sR   (double)
+ *   absdot (may be NULL): same layout as ref
+ * nthreads <= 0 means "all available".  Parallelised over output rows only;
+ * every element is still the sequential-k sum above.
+ */
+void oracle_gemm_nt(const uint16_t *A, const uint16_t *B, double *ref, double *absdot,
+                    int64_t batch, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldr,
+                    int64_t sA, int64_t sB, int64_t sR, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bi = 0; bi < batch * M; ++bi) {
+        const int64_t b = bi / M, i = bi % M;
+        const uint16_t *a_row = A + b * sA + i * lda;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint16_t *b_row = B + b * sB + j * ldb;
+            double *r = ref + b * sR + i * ldr + j;
+            double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
+            dot_nt(a_row, b_row, K, r, ab);
+        }
+    }
+}
+
+/*
+ * Selected elements only: for s < n, element (bidx[s], iidx[s], jidx[s]).
+ * Used where the full product is too large to recompute on the CPU.
+ */
+void oracle_gemm_nt_sampled(const uint16_t *A, const uint16_t *B,
+                            const int64_t *bidx, const int64_t *iidx, const int64_t *jidx,
+                            int64_t n, int64_t K, int64_t lda, int64_t ldb,
+                            int64_t sA, int64_t sB, double *ref, double *absdot, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t s = 0; s < n; ++s) {
+        const uint16_t *a_row = A + bidx[s] * sA + iidx[s] * lda;
+        const uint16_t *b_row = B + bidx[s] * sB + jidx[s] * ldb;
+        dot_nt(a_row, b_row, K, ref + s, absdot ? absdot + s : 0);
+    }
+}
+
+/* Number of threads the OpenMP runtime would use by default. */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,205 @@
+"""Pins of the CPU oracle: checks of ``oracle.Oracle`` against facts fixed by
+the pages and by mathematics, never against the oracle itself.
+
+Each ``pin_*`` raises AssertionError when the oracle is wrong.  They are run on
+the real oracle (tests/test_oracle.py, must pass) and on copies with a planted
+mistake (tests/test_oracle_mutants.py, some pin must fail).
+
+Sources:
+  * "Warp Matrix Instructions" (opening paragraph and the closing check of
+    "From Shared Memory to a Matrix Product"): Out = A @ B.T for A (16,16),
+    B (8,16) fp16 with fp32 accumulation, checked with rtol = atol = 2e-4
+    against the fp32 product of randn inputs.
+  * "Blackwell Tensor Cores", "The Accumulator's Lifetime": the same product
+    for A (128,64), B (64,64), same check.
+  * IEEE 754 binary16 (the fp16 format) and exact rational arithmetic.
+"""
+from fractions import Fraction
+
+import numpy as np
+
+U = 2.0 ** -53  # unit roundoff of IEEE double
+
+
+def gamma(n):
+    """Standard bound factor n*u/(1-n*u) for n sequential double additions."""
+    return n * U / (1.0 - n * U)
+
+
+def exact_product(A16, B16):
+    """Exact Out = A @ B.T as (Fraction matrix, exact sum |a*b| matrix).
+
+    Every finite fp16 value is an integer multiple of 2**-24, so scaling by
+    2**24 gives integers (computed through float64, which holds them exactly);
+    the products and their sums are then exact Python integers (object arrays),
+    with value S / 2**48.
+    """
+    a = (np.asarray(A16, dtype=np.float16).astype(np.float64) * 2.0 ** 24)
+    b = (np.asarray(B16, dtype=np.float16).astype(np.float64) * 2.0 ** 24)
+    ai = np.vectorize(int, otypes=[object])(a)
+    bi = np.vectorize(int, otypes=[object])(b)
+    s = ai.dot(bi.T)
+    sabs = np.abs(ai).dot(np.abs(bi).T)
+    scale = 2 ** 48
+    to_frac = np.vectorize(lambda v: Fraction(v, scale), otypes=[object])
+    return to_frac(s), to_frac(sabs)
+
+
+def check_against_exact(orc, A16, B16):
+    ref, absdot = orc.gemm_nt(A16, B16)
+    exact, exact_abs = exact_product(A16, B16)
+    K = np.shape(A16)[-1]
+    g = gamma(max(K - 1, 0))
+    ex = np.vectorize(float, otypes=[np.float64])(exact)
+    exa = np.vectorize(float, otypes=[np.float64])(exact_abs)
+    # ref within the summation bound of the exact value; absdot likewise.
+    err = np.abs(ref - ex)
+    assert np.all(err <= g * exa * (1 + 2 * U) + 2 * U * np.abs(ex) + 1e-300), \
+        "oracle differs from the exact sum by more than the double summation bound"
+    assert np.all(np.abs(absdot - exa) <= (g + 2 * U) * exa + 1e-300), \
+        "absdot differs from the exact sum of |a*b|"
+    return ref, absdot, ex
+
+
+def pin_decoder_exhaustive(orc):
+    """All 65536 fp16 bit patterns decode to numpy's float16 -> float64 value."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.half_to_double(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    nan_g, nan_w = np.isnan(got), np.isnan(want)
+    assert np.array_equal(nan_g, nan_w), "NaN patterns decode differently"
+    assert np.array_equal(got[~nan_g], want[~nan_w]), "fp16 decoder mismatch"
+    # signed zero keeps its sign
+    assert np.array_equal(np.signbit(got[~nan_g]), np.signbit(want[~nan_w]))
+
+
+def pin_bruteforce_tiny(orc, seed=11):
+    """Random tiny shapes, including subnormals and extreme fp16 values, equal
+    the exact rational sum within the double summation bound."""
+    rng = np.random.default_rng(seed)
+    specials = np.array([0.0, -0.0, 2.0 ** -24, -(2.0 ** -24), 2.0 ** -14, 65504.0,
+                         -65504.0, 1.0, -1.0, 0.5, 3.0], dtype=np.float16)
+    for trial in range(40):
+        M, N, K = (int(x) for x in rng.integers(1, 9, size=3))
+        A = (rng.standard_normal((M, K)) * 4).astype(np.float16)
+        B = (rng.standard_normal((N, K)) * 4).astype(np.float16)
+        if trial % 3 == 0:
+            A.flat[rng.integers(0, A.size, size=min(3, A.size))] = rng.choice(specials, size=min(3, A.size))
+            B.flat[rng.integers(0, B.size, size=min(3, B.size))] = rng.choice(specials[:5], size=min(3, B.size))
+        check_against_exact(orc, A, B)
+
+
+def pin_k1_exact(orc):
+    """K = 1: a single product of two fp16 values is exact in double."""
+    rng = np.random.default_rng(5)
+    A = (rng.standard_normal((7, 1)) * 100).astype(np.float16)
+    B = (rng.standard_normal((5, 1)) * 0.01).astype(np.float16)
+    ref, absdot = orc.gemm_nt(A, B)
+    want = A.astype(np.float64) @ B.astype(np.float64).T
+    assert np.array_equal(ref, want)
+    assert np.array_equal(absdot, np.abs(want))
+
+
+def pin_worked_examples(orc, seed=3):
+    """The two worked-example shapes: exact-sum bound, and the pages' own
+    assert_close(rtol=2e-4, atol=2e-4) against the fp32 product."""
+    rng = np.random.default_rng(seed)
+    for (M, N, K) in ((16, 8, 16), (128, 64, 64)):
+        A = rng.standard_normal((M, K)).astype(np.float16)
+        B = rng.standard_normal((N, K)).astype(np.float16)
+        ref, _, _ = check_against_exact(orc, A, B)
+        f32 = A.astype(np.float32) @ B.astype(np.float32).T
+        assert np.all(np.abs(ref - f32) <= 2e-4 + 2e-4 * np.abs(f32)), \
+            "oracle fails the pages' own fp32 check"
+
+
+def pin_closed_forms(orc):
+    """Products with a known closed form, exactly."""
+    # ones: every entry is K
+    for K in (1, 7, 64, 1000):
+        ref, absdot = orc.gemm_nt(np.ones((3, K), np.float16), np.ones((4, K), np.float16))
+        assert np.all(ref == K) and np.all(absdot == K)
+    rng = np.random.default_rng(7)
+    # identity: B = I_K gives Out = A (each entry is one exact product)
+    K = 24
+    A = rng.standard_normal((10, K)).astype(np.float16)
+    ref, _ = orc.gemm_nt(A, np.eye(K, dtype=np.float16))
+    assert np.array_equal(ref, A.astype(np.float64)), "identity product"
+    # permutation: B = P gives the columns of A permuted: Out[i,j] = A[i, p[j]]
+    p = rng.permutation(K)
+    P = np.zeros((K, K), np.float16)
+    P[np.arange(K), p] = 1
+    ref, _ = orc.gemm_nt(A, P)
+    assert np.array_equal(ref, A.astype(np.float64)[:, p]), "permutation product"
+    # identity on the left: A = I gives Out = B.T
+    B = rng.standard_normal((9, K)).astype(np.float16)
+    ref, _ = orc.gemm_nt(np.eye(K, dtype=np.float16), B)
+    assert np.array_equal(ref, B.astype(np.float64).T), "left identity"
+    # rank one: A[i,k] = x_i, B[j,k] = y_j gives K * x_i * y_j (small integers: exact)
+    x = rng.integers(-8, 9, size=6).astype(np.float16)
+    y = rng.integers(-8, 9, size=5).astype(np.float16)
+    K = 50
+    ref, absdot = orc.gemm_nt(np.repeat(x[:, None], K, 1), np.repeat(y[:, None], K, 1))
+    want = K * np.outer(x.astype(np.float64), y.astype(np.float64))
+    assert np.array_equal(ref, want) and np.array_equal(absdot, np.abs(want))
+    # a single nonzero column pair: only k = 3 contributes
+    A = np.zeros((4, 8), np.float16)
+    B = np.zeros((5, 8), np.float16)
+    A[:, 3] = np.arange(1, 5)
+    B[:, 3] = -np.arange(1, 6)
+    ref, _ = orc.gemm_nt(A, B)
+    assert np.array_equal(ref, -np.outer(np.arange(1, 5), np.arange(1, 6)).astype(np.float64))
+    # empty sum: K = 0 gives zeros
+    ref, absdot = orc.gemm_nt(np.zeros((3, 0), np.float16), np.zeros((2, 0), np.float16))
+    assert ref.shape == (3, 2) and np.all(ref == 0) and np.all(absdot == 0)
+
+
+def pin_integer_exact(orc, seed=4):
+    """Integer inputs in [-4,4]: every partial sum is an integer below 2**53,
+    so the oracle is exact; compare with integer arithmetic."""
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-4, 5, size=(2, 37, 300)).astype(np.float16)
+    B = rng.integers(-4, 5, size=(2, 29, 300)).astype(np.float16)
+    ref, absdot = orc.gemm_nt(A, B)
+    ai, bi = A.astype(np.int64), B.astype(np.int64)
+    want = np.einsum("bik,bjk->bij", ai, bi)
+    wabs = np.einsum("bik,bjk->bij", np.abs(ai), np.abs(bi))
+    assert np.array_equal(ref, want.astype(np.float64)), "integer product not exact"
+    assert np.array_equal(absdot, wabs.astype(np.float64))
+
+
+def pin_numpy_crosscheck(orc, seed=9):
+    """Mid-size shapes against numpy's float64 matmul (independent code, other
+    summation order): both are within gamma_K * absdot of the exact value."""
+    rng = np.random.default_rng(seed)
+    for (M, N, K) in ((96, 80, 200), (33, 130, 513)):
+        A = rng.standard_normal((M, K)).astype(np.float16)
+        B = rng.standard_normal((N, K)).astype(np.float16)
+        ref, absdot = orc.gemm_nt(A, B)
+        want = A.astype(np.float64) @ B.astype(np.float64).T
+        assert np.all(np.abs(ref - want) <= 2 * gamma(K) * absdot + 1e-300)
+        wabs = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64)).T
+        assert np.all(np.abs(absdot - wabs) <= 2 * gamma(K) * wabs + 1e-300)
+
+
+def pin_batched_and_sampled(orc, seed=13):
+    """Batched layout: batch b of the result is the product of batch b of the
+    inputs (checked with numpy); sampled elements equal the numpy values."""
+    rng = np.random.default_rng(seed)
+    batch, M, N, K = 3, 11, 6, 19
+    A = rng.integers(-4, 5, size=(batch, M, K)).astype(np.float16)
+    B = rng.integers(-4, 5, size=(batch, N, K)).astype(np.float16)
+    ref, _ = orc.gemm_nt(A, B)
+    want = np.einsum("bik,bjk->bij", A.astype(np.int64), B.astype(np.int64)).astype(np.float64)
+    assert np.array_equal(ref, want), "batched product"
+    bb = rng.integers(0, batch, size=50)
+    ii = rng.integers(0, M, size=50)
+    jj = rng.integers(0, N, size=50)
+    sref, sabs = orc.gemm_nt_sampled(A, B, bb, ii, jj)
+    assert np.array_equal(sref, want[bb, ii, jj]), "sampled product"
+    wabs = np.einsum("bik,bjk->bij", np.abs(A.astype(np.int64)), np.abs(B.astype(np.int64)))
+    assert np.array_equal(sabs, wabs[bb, ii, jj].astype(np.float64))
+
+
+ALL_PINS = [pin_decoder_exhaustive, pin_bruteforce_tiny, pin_k1_exact, pin_worked_examples,
+            pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled]

@@ -1,0 +1,42 @@
+"""Plant plausible mistakes in copies of the oracle and check that at least one
+pin rejects each (CPU only; the real oracle is untouched)."""
+import os
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+import oracle_pins
+
+SRC = open(obuild.SRC).read()
+
+# (name, original text, planted text)
+MUTANTS = [
+    ("exponent_bias", "(int)expo - 25", "(int)expo - 24"),
+    ("subnormal_scale", "pow2i(-24)", "pow2i(-25)"),
+    ("sign_dropped", "return sign ? -v : v;", "return v;"),
+    ("last_term_dropped", "for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
+    ("b_row_stride", "const uint16_t *b_row = B + b * sB + j * ldb;",
+     "const uint16_t *b_row = B + b * sB + j;"),
+    ("a_batch_stride", "const uint16_t *a_row = A + b * sA + i * lda;",
+     "const uint16_t *a_row = A + b * sB + i * lda;"),
+    ("abs_missing", "aacc += fabs(p);", "aacc += p;"),
+    ("float_accumulator", "double acc = 0.0, aacc = 0.0;", "float acc = 0.0f; double aacc = 0.0;"),
+    ("sampled_ij_swapped", "iidx[s] * lda", "jidx[s] * lda"),
+    ("product_sign", "oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k])",
+     "-oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k])"),
+]
+
+
+@pytest.mark.parametrize("name,orig,planted", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, orig, planted):
+    assert SRC.count(orig) >= 1, "mutation site vanished from the oracle source"
+    lib = obuild.build_variant(SRC.replace(orig, planted), str(tmp_path), "oracle_" + name)
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, IndexError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, "planted mistake %r passed every pin" % name

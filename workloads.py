@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs for the fp16 product Out = A @ B.T.
+
+This module holds the five workloads and their input recipe, and nothing of
+the product's arithmetic: it only draws random numbers and rounds them to fp16.
+Both sides of every parity check (the CPU oracle and the CUDA library) receive
+the arrays made here, so they see identical bits.
+
+Recipe (one ``numpy.random.default_rng(seed)`` stream per workload):
+  * A is drawn first (batch-major, then row-major), then B, from the same stream;
+  * uniform[-1,1]  -> ``rng.uniform(-1.0, 1.0)`` in float64;
+  * normal(0, s)   -> ``s * rng.standard_normal()`` in float64;
+  * integers [-4,4]-> ``rng.integers(-4, 5, dtype=int8)`` (inclusive bounds);
+  * every value is then rounded once to fp16 with round-to-nearest-even
+    (numpy's float64 -> float16 cast); values stay far inside fp16's range, and
+    normal(0, 0.02) yields some fp16 subnormals, which are kept.
+Float draws are made in chunks of 2**24 values; the stream is sequential, so
+the chunking does not change the values.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+
+_CHUNK = 1 << 24
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    M: int
+    N: int
+    K: int
+    dist: str          # "uniform", "normal" or "int4"
+    sigma: float       # for "normal"
+    seed: int
+    description: str
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.batch * self.M * self.N * self.K
+
+    @property
+    def bytes(self) -> float:
+        """Algorithmic bytes: read A and B once (fp16), write Out once (fp32)."""
+        return float(self.batch) * (2 * self.M * self.K + 2 * self.N * self.K + 4 * self.M * self.N)
+
+
+WORKLOADS = {
+    "tile_128x64x64": Workload(
+        "tile_128x64x64", 1, 128, 64, 64, "uniform", 0.0, 0,
+        "A (128,64), B (64,64), uniform[-1,1], seed 0: one CTA tile"),
+    "square_4096": Workload(
+        "square_4096", 1, 4096, 4096, 4096, "uniform", 0.0, 1,
+        "M=N=K=4096, uniform[-1,1], seed 1"),
+    "square_8192": Workload(
+        "square_8192", 1, 8192, 8192, 8192, "normal", 1.0, 2,
+        "M=N=K=8192, normal(0,1), seed 2 (compute-bound headline)"),
+    "skinny_64x16384x8192": Workload(
+        "skinny_64x16384x8192", 1, 64, 16384, 8192, "normal", 0.02, 3,
+        "M=64, N=16384, K=8192, normal(0,0.02), seed 3 (memory-bound)"),
+    "ragged_batch16_3001x2047x1000": Workload(
+        "ragged_batch16_3001x2047x1000", 16, 3001, 2047, 1000, "int4", 0.0, 4,
+        "batch 16 of M=3001, N=2047, K=1000, integers in [-4,4], seed 4 (exact)"),
+}
+
+
+def _draw(rng, n, dist, sigma):
+    out = np.empty(n, dtype=np.float16)
+    if dist == "int4":
+        out[:] = rng.integers(-4, 5, size=n, dtype=np.int8)
+        return out
+    for s in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s)
+        if dist == "uniform":
+            out[s:s + m] = rng.uniform(-1.0, 1.0, size=m)
+        elif dist == "normal":
+            out[s:s + m] = sigma * rng.standard_normal(size=m)
+        else:
+            raise ValueError("unknown distribution %r" % dist)
+    return out
+
+
+def make_inputs(batch, M, N, K, dist="uniform", sigma=1.0, seed=0):
+    """Return (A, B) as float16 arrays of shape (batch,M,K), (batch,N,K)
+    (or (M,K), (N,K) when batch == 0 is passed to mean "unbatched")."""
+    rng = np.random.default_rng(seed)
+    nb = max(batch, 1)
+    A = _draw(rng, nb * M * K, dist, sigma).reshape(nb, M, K)
+    B = _draw(rng, nb * N * K, dist, sigma).reshape(nb, N, K)
+    if batch == 0:
+        return A[0], B[0]
+    return A, B
+
+
+def workload_inputs(name):
+    """Inputs of a named workload: 2-D for batch 1, 3-D otherwise."""
+    w = WORKLOADS[name]
+    return make_inputs(0 if w.batch == 1 else w.batch, w.M, w.N, w.K, w.dist, w.sigma, w.seed)
