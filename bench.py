@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Benchmark of the fp16 -> fp32 product Out = A @ B.T on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one call of the library on one synthetic problem (the whole hot
+path: TMA staging, tcgen05 MMAs into TMEM, epilogue to HBM).  The default
+workload is the 8192^3 product (fp16 normal(0,1), seed 2).  Rank 0 prints one
+JSON line.
+
+  value      TFLOP/s with A, B resident in HBM, CUDA events on the launching
+             stream, max over ranks, whole-job aggregate (N replicas: weak scaling)
+  e2e        the same metric through gemm_nt_f16_f32_from_host: pinned host
+             A, B -> device, product, Out -> pinned host, every step
+  roofline   the dominant kernel against the measured peak (MEASURED_PEAKS.json)
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+  --impl reference  times that oracle alone (the reference arm of this bench)
+
+Inputs of the default workload (512 MiB touched per step) exceed the 129 MB L2,
+so no L2 flush is needed between steps; smaller workloads flush L2 by writing a
+256 MiB buffer between timed steps.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "TFLOP/s fp16→fp32 Out=A·Bᵀ at 8192³; % of dense fp16 peak / HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
+# sha256 of the kernel source it was taken on; reported as null once the kernel
+# source no longer matches.
+TRAFFIC = {}
+
+
+def kernel_source_sha():
+    path = os.path.join(ROOT, "dense_fp16_tensor_gemm_gb300", "csrc", "tc05_gemm.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "tflops": d["bf16_tflops"],
+                "tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.bus_id:
+            cmd += ["--id=" + self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 7:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, r[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        top = max(sm)
+        loaded = [s for s in sm if s >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_cpu_sample(w, A, B, target_s):
+    """Time the CPU oracle on whole rows of the workload (batch 0), sized to
+    about target_s seconds.  Returns (tflops, seconds, rows, threads)."""
+    import oracle
+    A0 = A if A.ndim == 2 else A[0]
+    B0 = B if B.ndim == 2 else B[0]
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A0[:1], B0)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(1, min(A0.shape[0], target_s / t1)))
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A0[:rows], B0)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * B0.shape[0] * A0.shape[1]
+    return flops / dt / 1e12, dt, rows, oracle.max_threads()
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    world, rank, _ = dist_init()
+    if rank != 0:
+        return 0
+    A, B = workloads.workload_inputs(w.name)
+    per_step = max(1.0, args.cpu_seconds / 2)
+    vals = []
+    rows_used = None
+    for i in range(args.warmup + args.steps):
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, per_step)
+        if i >= args.warmup:
+            vals.append((tf, dt))
+            rows_used = rows
+    tf = statistics.median(v[0] for v in vals)
+    ms = statistics.median(v[1] for v in vals) * 1e3
+    sample = ("%d full rows of batch 0 (%d x %d outputs, K=%d) per step"
+              % (rows_used, rows_used, w.N, w.K))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, None),
+        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, flush):
+    cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) fp16 row-major, "
+                       "fp32 accumulate, fp32 Out" % (
+                           w.name, w.description, "%d," % w.batch if w.batch > 1 else "", w.M, w.K,
+                           "%d," % w.batch if w.batch > 1 else "", w.N, w.K),
+           "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed}
+    if flush is not None:
+        cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (w.bytes / 2 ** 20)
+                     if not flush else "L2 flushed between timed steps (256 MiB write)")
+    return cfg
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_8192", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--path", default="AUTO")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import dense_fp16_tensor_gemm_gb300 as gnt
+
+    world, rank, local = dist_init()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    gnt.load()
+    path = gnt.Path[args.path]
+    A, B = workloads.workload_inputs(w.name)
+    a = torch.from_numpy(A).cuda()
+    b = torch.from_numpy(B).cuda()
+    batched = A.ndim == 3
+    out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=torch.float32,
+                      device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        if batched:
+            gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
+                                             w.K, w.K, w.N, w.batch, w.M * w.K, w.N * w.K, w.M * w.N,
+                                             path, sh)
+        else:
+            gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
+                                             w.K, w.K, w.N, 1, 0, 0, 0, path, sh)
+
+    flush = w.bytes <= 2 * L2_BYTES
+    scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
+
+    for _ in range(args.warmup):
+        step()
+    gnt.gemm_nt_check(sh)
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+    except AttributeError:
+        pass
+    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    gnt.gemm_nt_check(sh)
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(per_launch) if flush else starts[0].elapsed_time(ends[-1])
+    ms_step = total_ms / args.steps
+    t = torch.tensor([ms_step], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item())
+    value = w.flops * world / (ms_step * 1e-3) / 1e12
+    kernel_ms = statistics.mean(per_launch)
+
+    # ---- end to end through the host-buffer entry point
+    e2e_steps = args.e2e_steps or max(3, args.steps // 4)
+    ha = torch.from_numpy(A).pin_memory()
+    hb = torch.from_numpy(B).pin_memory()
+    ho = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
+                                      b.data_ptr(), out.data_ptr(), w.M, w.N, w.K, w.batch, sh)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    gnt.gemm_nt_check(sh)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t = torch.tensor([e2e_ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_ms = float(t.item())
+    e2e_val = w.flops * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    ai = w.flops / w.bytes
+    tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12
+    tr = TRAFFIC.get(w.name)
+    traffic = tr[0] if tr and tr[1] == kernel_source_sha() else None
+    if tensor_bound:
+        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["tflops"], "traffic": traffic,
+                "peak_source": "%s bf16 dense burst (kind::f16 runs fp16 at the bf16 rate)" % peaks["source"]}
+    else:
+        achieved = w.bytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": "%s HBM copy bandwidth" % peaks["source"]}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": "%d full rows of batch 0 (%d x %d outputs, K=%d), %.1f s" % (
+                   rows, rows, w.N, w.K, dt)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(w, flush),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+                "d2h_bytes_per_step": int(out.numel() * 4)},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "path": args.path,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

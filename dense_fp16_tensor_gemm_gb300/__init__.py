@@ -1,0 +1,185 @@
+"""Python binding of libgemm_nt: Out = A @ B.T, fp16 inputs, fp32 accumulate/output.
+
+The functions named like the C ABI (include/gemm_nt.h) take raw device
+pointers and sizes and only marshal arguments; ``gemm_nt`` and
+``gemm_nt_batched`` do the same for torch CUDA tensors (pointers, strides and
+the current stream).  Every step of the product runs in the library's CUDA
+kernels.  There is no fallback: if libgemm_nt.so has not been built, or a call
+fails, an exception is raised.
+"""
+import ctypes
+import enum
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgemm_nt.so")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_VALUE = 1
+    OVERLAP = 2
+    UNSUPPORTED_DEVICE = 3
+    CUDA = 4
+    DEVICE_TIMEOUT = 5
+    NOT_SUPPORTED = 6
+
+
+class Path(enum.IntEnum):
+    AUTO = 0
+    TC05 = 1
+    SKINNY = 2
+    MMASYNC = 3
+    TC05_PAIR = 4
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status):
+        self.status = Status(status)
+        super().__init__("libgemm_nt: %s (%s)" % (status_string(status), self.status.name))
+
+
+# name -> (restype, argtypes); mirrors include/gemm_nt.h
+_i64, _vp, _u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint64
+_SIGNATURES = {
+    "gemm_nt_f16_f32": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 6 + [_vp]),
+    "gemm_nt_f16_f32_batched": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [_vp]),
+    "gemm_nt_f16_f32_batched_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int, _vp]),
+    "gemm_nt_f16_f32_from_host": (ctypes.c_int, [_vp] * 6 + [_i64] * 4 + [_vp]),
+    "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
+    "gemm_nt_check": (ctypes.c_int, [_vp]),
+    "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_nt_probe_m16n8k16": (ctypes.c_int, [_vp] * 6),
+    "gemm_nt_debug_set_wait_limit": (None, [_u64]),
+    "gemm_nt_debug_set_fault": (None, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load libgemm_nt.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libgemm_nt.so is not built (%s); run `python -m dense_fp16_tensor_gemm_gb300._build`"
+                % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status):
+    if status != 0:
+        raise GemmError(status)
+
+
+def status_string(status):
+    return load().gemm_nt_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- C-ABI mirror
+def gemm_nt_f16_f32(A, B, Out, M, N, K, lda, ldb, ldo, stream=0):
+    _check(load().gemm_nt_f16_f32(A, B, Out, M, N, K, lda, ldb, ldo, stream))
+
+
+def gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO,
+                            stream=0):
+    _check(load().gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
+                                          strideB, strideO, stream))
+
+
+def gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
+                                 strideO, path, stream=0):
+    _check(load().gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
+                                               strideB, strideO, int(path), stream))
+
+
+def gemm_nt_f16_f32_from_host(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, batch, stream=0):
+    _check(load().gemm_nt_f16_f32_from_host(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, batch,
+                                            stream))
+
+
+def gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, batch=1, strideA=0, strideB=0, strideO=0):
+    return Path(load().gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
+                                           strideB, strideO))
+
+
+def gemm_nt_check(stream=0):
+    _check(load().gemm_nt_check(stream))
+
+
+def gemm_nt_probe_m16n8k16(A, B, ar, br, dr, stream=0):
+    _check(load().gemm_nt_probe_m16n8k16(A, B, ar, br, dr, stream))
+
+
+def gemm_nt_debug_set_wait_limit(cycles):
+    load().gemm_nt_debug_set_wait_limit(int(cycles))
+
+
+def gemm_nt_debug_set_fault(fault):
+    load().gemm_nt_debug_set_fault(int(fault))
+
+
+# ---------------------------------------------------------------- torch tensors
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _matrix_ld(t, name):
+    if t.stride(-1) != 1:
+        raise ValueError("%s must have unit stride along its last dimension" % name)
+    return t.stride(-2) if t.shape[-2] > 1 else max(t.shape[-1], 1)
+
+
+def gemm_nt(A, B, out=None, path=Path.AUTO, stream=None):
+    """Out = A @ B.T for torch CUDA tensors A (M,K) fp16, B (N,K) fp16.
+
+    Row strides may exceed the row length; the last dimension must be
+    contiguous.  ``out`` (M,N) fp32 is allocated if not given.  Runs on
+    ``stream`` (default: torch's current stream).
+    """
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("shapes: A (M,K), B (N,K)")
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, N):
+        raise ValueError("out must be float32 of shape (M,N)")
+    gemm_nt_f16_f32_batched_path(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                                 _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
+                                 1, 0, 0, 0, path, _stream_handle(stream))
+    return out
+
+
+def gemm_nt_batched(A, B, out=None, path=Path.AUTO, stream=None):
+    """Out[b] = A[b] @ B[b].T for torch CUDA tensors A (batch,M,K), B (batch,N,K)
+    fp16 (a batch stride of 0, e.g. from ``expand``, shares the operand)."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0] or A.shape[2] != B.shape[2]:
+        raise ValueError("shapes: A (batch,M,K), B (batch,N,K)")
+    batch, M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (batch, M, N):
+        raise ValueError("out must be float32 of shape (batch,M,N)")
+    gemm_nt_f16_f32_batched_path(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                                 _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
+                                 batch, A.stride(0), B.stride(0), out.stride(0), path,
+                                 _stream_handle(stream))
+    return out

@@ -1,0 +1,466 @@
+// gemm_nt_api.cu -- the C ABI of libgemm_nt (declared in include/gemm_nt.h):
+// argument validation, kernel selection, TMA tensor-map construction, per-device
+// state and the status word.
+//
+// The product is the one of the TIRx guides' worked examples ("Warp Matrix
+// Instructions" and "Blackwell Tensor Cores"): Out = A @ B.T, fp16 inputs, fp32
+// accumulation, Out overwritten.  The 128-byte swizzle of the tensor maps is the
+// guides' swizzle "mode 3" (1024-byte period), which the tcgen05 kernel's
+// shared-memory descriptors expect.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/gemm_nt.h"
+#include "internal.h"
+
+namespace gnt {
+
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimit = 4000000000ull;  // ~2 s of SM clock
+
+std::atomic<unsigned long long> g_wait_limit{0};
+std::atomic<int> g_fault{0};
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_err = cudaSuccess;
+    bool supported = false;
+    int num_sms = 0;
+    uint32_t* status = nullptr;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// Per-device one-time setup: capability check, SM count, kernel attributes and
+// the address of the status word.
+gemm_status_t device_state(DeviceState** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return GEMM_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    std::call_once(d.once, [&d, dev] {
+        int major = 0, minor = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            d.init_err = e;
+            return;
+        }
+        d.supported = (major == 10 && minor == 3);
+        if (!d.supported)
+            return;
+        void* sym = nullptr;
+        e = cudaGetSymbolAddress(&sym, g_status_word);
+        if (e == cudaSuccess) e = cudaMemset(sym, 0, sizeof(uint32_t));
+        if (e == cudaSuccess) e = tc05_configure(64, false);
+        if (e == cudaSuccess) e = tc05_configure(128, false);
+        if (e == cudaSuccess) e = tc05_configure(256, false);
+        if (e == cudaSuccess) e = tc05_configure(64, true);
+        d.status = static_cast<uint32_t*>(sym);
+        d.init_err = e;
+    });
+    if (d.init_err != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (!d.supported)
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+struct Problem {
+    const void* A;
+    const void* B;
+    float* Out;
+    int64_t M, N, K, lda, ldb, ldo, batch, sA, sB, sO;
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Byte span [lo, hi) touched by a strided batch of row-major matrices.
+void span(const void* base, int64_t esize, int64_t batch, int64_t stride, int64_t rows, int64_t ld,
+          int64_t cols, uintptr_t& lo, uintptr_t& hi)
+{
+    const int64_t last = (batch - 1) * stride + (rows - 1) * ld + cols;
+    lo = reinterpret_cast<uintptr_t>(base);
+    hi = lo + static_cast<uintptr_t>(last * esize);
+}
+
+gemm_status_t validate(const Problem& q)
+{
+    if (q.M < 0 || q.N < 0 || q.K < 0 || q.batch < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.M > INT32_MAX || q.N > INT32_MAX || q.K > INT32_MAX || q.batch > INT32_MAX)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.M == 0 || q.N == 0 || q.batch == 0)
+        return GEMM_OK;
+    if (!q.Out)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.K > 0 && (!q.A || !q.B))
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.ldo < q.N || (q.K > 0 && (q.lda < q.K || q.ldb < q.K)))
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.sA < 0 || q.sB < 0 || q.sO < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    // 64-bit extent limits (keep every byte offset below 2^62)
+    const double lim = 4.0e18;
+    if (static_cast<double>(q.batch) * static_cast<double>(std::max(q.sO, q.ldo * q.M)) * 4.0 > lim ||
+        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.M)) * 2.0 > lim ||
+        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.N)) * 2.0 > lim)
+        return GEMM_ERR_INVALID_VALUE;
+    if (!aligned(q.Out, 4) || (q.K > 0 && (!aligned(q.A, 2) || !aligned(q.B, 2))))
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.batch > 1 && q.sO < (q.M - 1) * q.ldo + q.N)
+        return GEMM_ERR_OVERLAP;
+    if (q.K > 0) {
+        uintptr_t olo, ohi, alo, ahi, blo, bhi;
+        span(q.Out, 4, q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
+        span(q.A, 2, q.batch, q.sA, q.M, q.lda, q.K, alo, ahi);
+        span(q.B, 2, q.batch, q.sB, q.N, q.ldb, q.K, blo, bhi);
+        if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
+            return GEMM_ERR_OVERLAP;
+    }
+    return GEMM_OK;
+}
+
+// Conditions for TMA tensor maps over A and B: 16-byte aligned bases and
+// row / batch strides that are multiples of 16 bytes and below 2^40 bytes.
+bool tma_ok(const Problem& q)
+{
+    if (!aligned(q.A, 16) || !aligned(q.B, 16))
+        return false;
+    if ((q.lda % 8) || (q.ldb % 8))
+        return false;
+    if (q.batch > 1 && ((q.sA % 8) || (q.sB % 8)))
+        return false;
+    // a batch dimension in a tensor map must step over whole matrices
+    if (q.batch > 1 && ((q.sA != 0 && q.sA < q.M * q.lda) || (q.sB != 0 && q.sB < q.N * q.ldb)))
+        return false;
+    const int64_t lim = int64_t(1) << 39;  // elements of 2 bytes
+    if (q.lda >= lim || q.ldb >= lim || q.sA >= lim || q.sB >= lim)
+        return false;
+    return true;
+}
+
+gemm_path_t select_path(const Problem& q)
+{
+    if (!tma_ok(q))
+        return GEMM_PATH_MMASYNC;
+    if (q.M <= 64 && q.N >= 1024)
+        return GEMM_PATH_SKINNY;
+    return GEMM_PATH_TC05;
+}
+
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
+              int64_t stride, int box_rows, int* bmul)
+{
+    auto enc = encode_fn();
+    if (!enc)
+        return false;
+    const bool batched = batch > 1 && stride > 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batched ? batch : 1)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
+                             static_cast<cuuint64_t>((batched ? stride : rows * ld) * 2)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    *bmul = batched ? 1 : 0;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+gemm_status_t zero_out(const Problem& q, cudaStream_t stream)
+{
+    if (q.sO == q.M * q.ldo || q.batch == 1) {
+        const int64_t rows = q.batch == 1 ? q.M : q.M * q.batch;
+        if (cudaMemset2DAsync(q.Out, q.ldo * 4, 0, q.N * 4, rows, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_OK;
+    }
+    for (int64_t b = 0; b < q.batch; ++b)
+        if (cudaMemset2DAsync(q.Out + b * q.sO, q.ldo * 4, 0, q.N * 4, q.M, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+unsigned long long wait_limit()
+{
+    const unsigned long long v = g_wait_limit.load();
+    return v ? v : kDefaultWaitLimit;
+}
+
+gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaStream_t stream)
+{
+    // X: the operand on the MMA's M side (128-row tiles); Y: the N side.
+    const void* xp = swap ? q.B : q.A;
+    const void* yp = swap ? q.A : q.B;
+    const int64_t xrows = swap ? q.N : q.M, yrows = swap ? q.M : q.N;
+    const int64_t xld = swap ? q.ldb : q.lda, yld = swap ? q.lda : q.ldb;
+    const int64_t xs = swap ? q.sB : q.sA, ys = swap ? q.sA : q.sB;
+    int bn;
+    if (swap) {
+        if (yrows > 64)
+            return GEMM_ERR_NOT_SUPPORTED;
+        bn = 64;
+    } else {
+        bn = yrows <= 64 ? 64 : (yrows <= 128 ? 128 : 256);
+    }
+    TcParams p{};
+    CUtensorMap tmx, tmy;
+    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, 128, &p.x_bmul) ||
+        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul))
+        return GEMM_ERR_CUDA;
+    p.out = q.Out;
+    p.ldo = q.ldo;
+    p.stride_o = q.sO;
+    p.rows_x = static_cast<int>(xrows);
+    p.rows_y = static_cast<int>(yrows);
+    p.batch = static_cast<int>(q.batch);
+    p.tiles_x = static_cast<int>((xrows + 127) / 128);
+    p.tiles_y = static_cast<int>((yrows + bn - 1) / bn);
+    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
+    const int64_t ntiles = tpb * q.batch;
+    if (ntiles > INT32_MAX)
+        return GEMM_ERR_NOT_SUPPORTED;
+    p.tiles_per_batch = static_cast<int>(tpb);
+    p.num_tiles = static_cast<int>(ntiles);
+    p.group_x = 16;
+    p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
+    p.vec4 = (!swap && aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.status = d.status;
+    p.wait_limit = wait_limit();
+    p.fault = g_fault.load();
+    int grid;
+    // Stream-K when there are too few tiles to fill the GPU: each CTA takes an
+    // even share of the (tile, k-block) iterations; tiles cut between CTAs are
+    // summed with atomics into a zeroed Out.
+    if (ntiles < d.num_sms && p.total_iters >= 2 * static_cast<long long>(d.num_sms) && swap) {
+        p.streamk = 1;
+        grid = d.num_sms;
+        gemm_status_t z = zero_out(q, stream);
+        if (z != GEMM_OK)
+            return z;
+    } else {
+        p.streamk = 0;
+        grid = static_cast<int>(std::min<int64_t>(ntiles, d.num_sms));
+    }
+    if (tc05_launch(tmx, tmy, p, bn, swap, grid, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
+{
+    if ((q.M + 63) / 64 > 65535)
+        return GEMM_ERR_NOT_SUPPORTED;
+    MmaParams p{};
+    p.A = static_cast<const uint16_t*>(q.A);
+    p.B = static_cast<const uint16_t*>(q.B);
+    p.out = q.Out;
+    p.M = static_cast<int>(q.M);
+    p.N = static_cast<int>(q.N);
+    p.K = static_cast<int>(q.K);
+    p.batch = static_cast<int>(q.batch);
+    p.lda = q.lda;
+    p.ldb = q.ldb;
+    p.ldo = q.ldo;
+    p.stride_a = q.sA;
+    p.stride_b = q.sB;
+    p.stride_o = q.sO;
+    p.vec_a = aligned(q.A, 16) && q.lda % 8 == 0 && (q.batch == 1 || q.sA % 8 == 0);
+    p.vec_b = aligned(q.B, 16) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
+    return mmasync_launch(p, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
+{
+    gemm_status_t st = validate(q);
+    if (st != GEMM_OK)
+        return st;
+    if (q.M == 0 || q.N == 0 || q.batch == 0)
+        return GEMM_OK;
+    if (path != GEMM_PATH_AUTO && path != GEMM_PATH_TC05 && path != GEMM_PATH_SKINNY &&
+        path != GEMM_PATH_MMASYNC && path != GEMM_PATH_TC05_PAIR)
+        return GEMM_ERR_INVALID_VALUE;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    if (q.K == 0)
+        return zero_out(q, stream);
+    if (path == GEMM_PATH_AUTO)
+        path = select_path(q);
+    switch (path) {
+    case GEMM_PATH_MMASYNC:
+        return run_mmasync(q, stream);
+    case GEMM_PATH_TC05:
+        if (!tma_ok(q))
+            return GEMM_ERR_NOT_SUPPORTED;
+        return run_tc05(q, *d, false, stream);
+    case GEMM_PATH_SKINNY:
+        if (!tma_ok(q))
+            return GEMM_ERR_NOT_SUPPORTED;
+        return run_tc05(q, *d, true, stream);
+    default:
+        return GEMM_ERR_NOT_SUPPORTED;
+    }
+}
+
+}  // namespace
+}  // namespace gnt
+
+using gnt::Problem;
+
+extern "C" {
+
+gemm_status_t gemm_nt_f16_f32(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldo, gemm_stream_t stream)
+{
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, 1, 0, 0, 0};
+    return gnt::run(q, GEMM_PATH_AUTO, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_f16_f32_batched(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
+                                      int64_t strideB, int64_t strideO, gemm_stream_t stream)
+{
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    return gnt::run(q, GEMM_PATH_AUTO, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_f16_f32_batched_path(const void* A, const void* B, float* Out, int64_t M, int64_t N,
+                                           int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch,
+                                           int64_t strideA, int64_t strideB, int64_t strideO, gemm_path_t path,
+                                           gemm_stream_t stream)
+{
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_f16_f32_from_host(const void* A_host, const void* B_host, float* Out_host, void* dA,
+                                        void* dB, float* dOut, int64_t M, int64_t N, int64_t K, int64_t batch,
+                                        gemm_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0 || batch < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0 || batch == 0)
+        return GEMM_OK;
+    if (!Out_host || !dOut || (K > 0 && (!A_host || !B_host || !dA || !dB)))
+        return GEMM_ERR_INVALID_VALUE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Problem q{dA, dB, dOut, M, N, K, K, K, N, batch, M * K, N * K, M * N};
+    gemm_status_t st = gnt::validate(q);
+    if (st != GEMM_OK)
+        return st;
+    if (K > 0) {
+        if (cudaMemcpyAsync(dA, A_host, static_cast<size_t>(batch * M * K * 2), cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(dB, B_host, static_cast<size_t>(batch * N * K * 2), cudaMemcpyHostToDevice, s) !=
+                cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    st = gnt::run(q, GEMM_PATH_AUTO, s);
+    if (st != GEMM_OK)
+        return st;
+    if (cudaMemcpyAsync(Out_host, dOut, static_cast<size_t>(batch * M * N * 4), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+gemm_path_t gemm_nt_select_path(const void* A, const void* B, const float* Out, int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
+                                int64_t strideB, int64_t strideO)
+{
+    Problem q{A, B, const_cast<float*>(Out), M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    return gnt::select_path(q);
+}
+
+gemm_status_t gemm_nt_check(gemm_stream_t stream)
+{
+    gnt::DeviceState* d = nullptr;
+    gemm_status_t st = gnt::device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (word) {
+        const uint32_t zero = 0;
+        if (cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+const char* gemm_nt_status_string(gemm_status_t status)
+{
+    switch (status) {
+    case GEMM_OK: return "success";
+    case GEMM_ERR_INVALID_VALUE: return "invalid argument";
+    case GEMM_ERR_OVERLAP: return "output overlaps an input or itself";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case GEMM_ERR_NOT_SUPPORTED: return "the requested kernel cannot take these arguments";
+    }
+    return "unknown status";
+}
+
+gemm_status_t gemm_nt_probe_m16n8k16(const void* A, const void* B, uint32_t* ar, uint32_t* br, float* dr,
+                                     gemm_stream_t stream)
+{
+    if (!A || !B || !ar || !br || !dr)
+        return GEMM_ERR_INVALID_VALUE;
+    if (!gnt::aligned(A, 2) || !gnt::aligned(B, 2) || !gnt::aligned(ar, 4) || !gnt::aligned(br, 4) ||
+        !gnt::aligned(dr, 4))
+        return GEMM_ERR_INVALID_VALUE;
+    gnt::DeviceState* d = nullptr;
+    gemm_status_t st = gnt::device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    return gnt::probe_launch(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), ar, br, dr,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
+}
+
+void gemm_nt_debug_set_wait_limit(uint64_t cycles) { gnt::g_wait_limit.store(cycles); }
+
+void gemm_nt_debug_set_fault(int fault) { gnt::g_fault.store(fault); }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the host API and the kernel translation
+// units of libgemm_nt.  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gnt {
+
+// Device status word bits (OR-ed by kernels, read and cleared by gemm_nt_check).
+constexpr uint32_t kStatusTimeout = 1u;
+
+// Parameters of the tcgen05 kernel.  "X" is the operand on the MMA's M side
+// (128 rows per tile), "Y" the operand on its N side (BN rows per tile).
+// Without swapping X = A and Y = B and Out[x][y]; with swapping (small M)
+// X = B, Y = A and the tile is written transposed, Out[y][x].
+struct TcParams {
+    float* out;
+    int64_t ldo;
+    int64_t stride_o;
+    int rows_x;
+    int rows_y;
+    int batch;
+    int tiles_x;
+    int tiles_y;
+    int num_kb;           // k-blocks of 64 per tile (K tail zero-filled by TMA)
+    int tiles_per_batch;  // tiles_x * tiles_y
+    int num_tiles;        // batch * tiles_per_batch
+    int group_x;          // grouped raster: x-tiles per group
+    int streamk;          // 0: whole tiles round-robin; 1: even k-block ranges per CTA
+    long long total_iters;  // num_tiles * num_kb
+    int x_bmul;           // 1 if X's tensor map has a batch dimension, 0 if shared
+    int y_bmul;
+    int vec4;             // Out base and ldo allow 16-byte stores
+    uint32_t* status;     // device status word
+    unsigned long long wait_limit;  // bounded-wait limit, SM clock cycles
+    int fault;            // test hook: 0 none, 1 drop a producer stage, 2 skip a release
+};
+
+struct MmaParams {
+    const uint16_t* A;
+    const uint16_t* B;
+    float* out;
+    int M, N, K, batch;
+    int64_t lda, ldb, ldo;
+    int64_t stride_a, stride_b, stride_o;
+    int vec_a;  // A rows and base 16-byte aligned
+    int vec_b;
+};
+
+// tcgen05 kernel family.  bn in {64, 128, 256}; swap selects the transposed
+// epilogue.  Returns the launch status.
+cudaError_t tc05_configure(int bn, bool swap);  // one-time per device
+cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn,
+                        bool swap, int grid, cudaStream_t stream);
+
+cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream);
+cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
+                         cudaStream_t stream);
+
+}  // namespace gnt

@@ -1,0 +1,195 @@
+// mmasync_gemm.cu -- ldmatrix + mma.sync m16n8k16 kernel for Out = A @ B.T on
+// any layout (unaligned bases, odd leading dimensions, tiny or ragged shapes),
+// and the one-warp fragment probe.
+//
+// "Warp Matrix Instructions" ("From Shared Memory to a Matrix Product") computes
+// one 16x8 output tile with a single warp: the operands are staged in shared
+// memory, ldmatrix.x4 loads A (16x16) as four 8x8 matrices in the order
+// (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15),
+// ldmatrix.x2 loads B (8x16) as (k 0-7), (k 8-15), and one mma.sync m16n8k16
+// (row.col, f32 accumulators, C = 0) leaves dr[r] for lane l at
+// Out[l/4 + 8*(r/2), 2*(l%4) + r%2].  "Other Fragment Shapes and Transfers" adds
+// that a longer K is several issues accumulating into the previous D.
+// "copy -> ldstmatrix" ("Algorithm" steps 3-4) gives the shared-memory rule:
+// each lane supplies the address of one 16-byte row, so row strides are
+// multiples of 8 fp16.
+//
+// This kernel tiles that warp product: a CTA of 4 warps owns a 64x64 output
+// tile, each warp a 32x32 sub-tile (2 x 4 m16n8 tiles), and K advances 32 at a
+// time through shared memory with 80-byte row pitch (16-byte aligned rows,
+// conflict-free ldmatrix).  Out-of-range rows and the K tail are zero-filled
+// while staging, and stores are masked.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gnt {
+
+namespace {
+
+constexpr int MBM = 64, MBN = 64, MBK = 32, MPAD = 8;
+constexpr int MPITCH = MBK + MPAD;  // 40 fp16 = 80 bytes
+constexpr int MThreads = 128;
+
+// Stage one (rows x 32) operand tile into shared memory, zero-filling
+// everything outside rows < nrows and k < K.
+__device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, int64_t ld, int row0, int nrows,
+                                           int k0, int K, bool vec)
+{
+    const int tid = threadIdx.x;
+    if (vec) {
+        // 64 rows x 4 chunks of 8 fp16 = 256 chunks, two per thread.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = tid + i * MThreads;
+            const int r = c >> 2;
+            const int kc = (c & 3) * 8;
+            const int row = row0 + r;
+            const int k = k0 + kc;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (row < nrows) {
+                const uint16_t* g = src + static_cast<int64_t>(row) * ld + k;
+                if (k + 8 <= K) {
+                    v = *reinterpret_cast<const uint4*>(g);
+                } else if (k < K) {
+                    uint16_t tmp[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        tmp[e] = (k + e < K) ? g[e] : uint16_t(0);
+                    v = make_uint4(tmp[0] | (uint32_t(tmp[1]) << 16), tmp[2] | (uint32_t(tmp[3]) << 16),
+                                   tmp[4] | (uint32_t(tmp[5]) << 16), tmp[6] | (uint32_t(tmp[7]) << 16));
+                }
+            }
+            *reinterpret_cast<uint4*>(sdst + r * MPITCH + kc) = v;
+        }
+    } else {
+        // Element-wise, consecutive threads on consecutive k.
+#pragma unroll 4
+        for (int i = 0; i < (64 * MBK) / MThreads; ++i) {
+            const int e = tid + i * MThreads;
+            const int r = e / MBK;
+            const int kk = e % MBK;
+            const int row = row0 + r;
+            const int k = k0 + kk;
+            uint16_t v = 0;
+            if (row < nrows && k < K)
+                v = src[static_cast<int64_t>(row) * ld + k];
+            sdst[r * MPITCH + kk] = v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams p)
+{
+    __shared__ __align__(16) uint16_t As[MBM * MPITCH];
+    __shared__ __align__(16) uint16_t Bs[MBN * MPITCH];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wm = warp >> 1, wn = warp & 1;
+    const int m0 = blockIdx.y * MBM, n0 = blockIdx.x * MBN;
+
+    for (int b = blockIdx.z; b < p.batch; b += gridDim.z) {
+        const uint16_t* Ab = p.A + static_cast<int64_t>(b) * p.stride_a;
+        const uint16_t* Bb = p.B + static_cast<int64_t>(b) * p.stride_b;
+        float acc[2][4][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    acc[i][j][r] = 0.f;
+
+        for (int k0 = 0; k0 < p.K; k0 += MBK) {
+            __syncthreads();  // previous tile fully consumed
+            stage_tile(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
+            stage_tile(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
+            __syncthreads();
+#pragma unroll
+            for (int ks = 0; ks < MBK; ks += 16) {
+                uint32_t af[2][4];
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi) {
+                    const int row = wm * 32 + mi * 16 + (lane & 15);
+                    const int col = ks + (lane >> 4) * 8;
+                    ldmatrix_x4(smem_u32(As + row * MPITCH + col), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+                }
+                uint32_t bfr[4][2];
+#pragma unroll
+                for (int nj = 0; nj < 2; ++nj) {
+                    // lanes 0-7: n 0-7 @k, 8-15: n 0-7 @k+8, 16-23: n 8-15 @k, 24-31: n 8-15 @k+8
+                    const int row = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    const int col = ks + ((lane >> 3) & 1) * 8;
+                    ldmatrix_x4(smem_u32(Bs + row * MPITCH + col), bfr[2 * nj][0], bfr[2 * nj][1],
+                                bfr[2 * nj + 1][0], bfr[2 * nj + 1][1]);
+                }
+#pragma unroll
+                for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                    for (int nb = 0; nb < 4; ++nb)
+                        mma_m16n8k16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
+            }
+        }
+
+        float* Ob = p.out + static_cast<int64_t>(b) * p.stride_o;
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int row = m0 + wm * 32 + mi * 16 + (lane >> 2) + 8 * (r >> 1);
+                    const int col = n0 + wn * 32 + nb * 8 + 2 * (lane & 3) + (r & 1);
+                    if (row < p.M && col < p.N)
+                        Ob[static_cast<int64_t>(row) * p.ldo + col] = acc[mi][nb][r];
+                }
+    }
+}
+
+// One warp, the warp example verbatim in structure: lanes copy elements
+// lane + 32q of A and B into shared memory, ldmatrix.x4 / .x2, one MMA with
+// C = 0, and the raw registers are written out lane-major.
+__global__ void __launch_bounds__(32) probe_kernel(const uint16_t* A, const uint16_t* B, uint32_t* ar_out,
+                                                    uint32_t* br_out, float* dr_out)
+{
+    __shared__ __align__(16) uint16_t a[16 * 16];
+    __shared__ __align__(16) uint16_t b[8 * 16];
+    const int lane = threadIdx.x;
+    for (int q = 0; q < 8; ++q)
+        a[lane + 32 * q] = A[lane + 32 * q];
+    for (int q = 0; q < 4; ++q)
+        b[lane + 32 * q] = B[lane + 32 * q];
+    __syncthreads();
+    uint32_t ar[4], br[2];
+    ldmatrix_x4(smem_u32(a + (lane & 15) * 16 + (lane >> 4) * 8), ar[0], ar[1], ar[2], ar[3]);
+    ldmatrix_x2(smem_u32(b + (lane & 7) * 16 + ((lane >> 3) & 1) * 8), br[0], br[1]);
+    float dr[4];
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_m16n8k16(dr, ar, br[0], br[1], zero);
+    for (int r = 0; r < 4; ++r) {
+        ar_out[lane * 4 + r] = ar[r];
+        dr_out[lane * 4 + r] = dr[r];
+    }
+    for (int r = 0; r < 2; ++r)
+        br_out[lane * 2 + r] = br[r];
+}
+
+}  // namespace
+
+cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream)
+{
+    dim3 grid((p.N + MBN - 1) / MBN, (p.M + MBM - 1) / MBM, p.batch < 65535 ? p.batch : 65535);
+    if (grid.y > 65535)
+        return cudaErrorInvalidConfiguration;
+    mmasync_gemm_kernel<<<grid, MThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
+                         cudaStream_t stream)
+{
+    probe_kernel<<<1, 32, 0, stream>>>(A, B, ar, br, dr);
+    return cudaGetLastError();
+}
+
+}  // namespace gnt

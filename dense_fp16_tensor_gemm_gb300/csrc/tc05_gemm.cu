@@ -1,0 +1,443 @@
+// tc05_gemm.cu -- persistent, warp-specialised tcgen05 kernel for Out = A @ B.T
+// (fp16 inputs, fp32 accumulation in Tensor Memory, fp32 output).
+//
+// The single-CTA example of "Blackwell Tensor Cores" ("The Accumulator's
+// Lifetime") allocates TMEM with warp 0, stages A/B in 128-byte-swizzled shared
+// memory (swizzle mode 3, 1024-byte period), lets one thread issue four
+// tcgen05.mma kind::f16 of shape 128x64x16 (accumulate off for the first K
+// slice), commits them to an mbarrier, waits for phase 0, fences, reads the
+// accumulator with tcgen05.ld 32x32b (warp w <-> TMEM lanes 32w..32w+31, one row
+// per thread) and releases TMEM after a final barrier.  This kernel keeps those
+// steps and turns them into a pipeline that streams K and loops over tiles:
+//
+//   warp 0      TMA producer: one thread waits for a free stage, posts the
+//               expected byte count and issues two 3-D tensor loads (X and Y
+//               tiles, 64 fp16 of K each, 128-byte swizzle) into the stage ring.
+//   warp 1      allocates 2*BN TMEM columns (two accumulators) and one thread
+//               issues 4 MMAs 128xBNx16 per stage, committing each stage back to
+//               the producer and each finished tile to the epilogue.
+//   warps 2-5   epilogue warpgroup: TMEM -> registers (32x32b.x32) -> global,
+//               overlapped with the next tile's MMAs through the second
+//               accumulator.
+//
+// Every mbarrier wait is bounded (wait_limit cycles); on expiry the kernel sets
+// the device status word and an abort flag, all roles leave their loops, loads
+// still in flight are waited for, TMEM is freed and the kernel returns.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gnt {
+
+namespace {
+
+constexpr int BM = 128;  // MMA M: rows of X per tile (TMEM lanes)
+constexpr int BK = 64;   // K per stage: 64 fp16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+
+template <int BN, bool SWAP>
+struct Cfg {
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr int X_BYTES = BM * BK * 2;
+    static constexpr int Y_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
+    static constexpr int EPI_BYTES = SWAP ? 0 : 4 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
+    static constexpr int TMEM_COLS = 2 * BN;                      // power of two, >= 32
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+struct Seg {
+    int tile;
+    int kb0;
+    int kb1;
+};
+
+// Walks this CTA's share of the work.  Tile mode: whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Stream-K mode: the contiguous range of
+// (tile, k-block) iterations [total*c/G, total*(c+1)/G), cut at tile borders.
+struct WorkIter {
+    long long it, end;
+    int tile, step, ntiles, nkb, streamk;
+
+    __device__ explicit WorkIter(const TcParams& p)
+    {
+        streamk = p.streamk;
+        nkb = p.num_kb;
+        ntiles = p.num_tiles;
+        if (streamk) {
+            it = p.total_iters * blockIdx.x / gridDim.x;
+            end = p.total_iters * (blockIdx.x + 1) / gridDim.x;
+        } else {
+            tile = blockIdx.x;
+            step = gridDim.x;
+        }
+    }
+
+    __device__ bool next(Seg& s)
+    {
+        if (streamk) {
+            if (it >= end)
+                return false;
+            s.tile = static_cast<int>(it / nkb);
+            s.kb0 = static_cast<int>(it - static_cast<long long>(s.tile) * nkb);
+            long long k1 = s.kb0 + (end - it);
+            s.kb1 = k1 < nkb ? static_cast<int>(k1) : nkb;
+            it += s.kb1 - s.kb0;
+            return true;
+        }
+        if (tile >= ntiles)
+            return false;
+        s.tile = tile;
+        s.kb0 = 0;
+        s.kb1 = nkb;
+        tile += step;
+        return true;
+    }
+};
+
+// Tile index -> (batch, x tile, y tile).  Within a batch, tiles are taken in
+// groups of group_x x-tiles, column by column, so CTAs running at the same time
+// share X rows and Y rows in L2.
+__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int& b, int& tx, int& ty)
+{
+    b = tile / p.tiles_per_batch;
+    const int t = tile - b * p.tiles_per_batch;
+    const int span = p.group_x * p.tiles_y;
+    const int g = t / span;
+    const int first_x = g * p.group_x;
+    const int rem_x = p.tiles_x - first_x;
+    const int gx = rem_x < p.group_x ? rem_x : p.group_x;
+    const int r = t - g * span;
+    tx = first_x + r % gx;
+    ty = r / gx;
+}
+
+// Bounded wait.  Returns false if the limit passed or another role aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                             unsigned long long limit)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (static_cast<unsigned long long>(clock64() - t0) > limit)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(p.status, kStatusTimeout);
+}
+
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc05_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
+                     const TcParams p)
+{
+    using C = Cfg<BN, SWAP>;
+    constexpr int STAGES = C::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* xs = smem;
+    uint8_t* ys = smem + STAGES * C::X_BYTES;
+    float* epi = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 128);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&tmx);
+        tma_prefetch_map(&tmy);
+    }
+    if (warp == 1) {
+        tmem_alloc<C::TMEM_COLS>(smem_u32(tmem_slot));
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0;       // bit s: stage s has a load this thread issued
+            uint32_t fill_parity = 0;  // bit s: parity of that fill
+            bool first = true, ok = true;
+            WorkIter w(p);
+            Seg s;
+            while (ok && w.next(s)) {
+                int b, tx, ty;
+                decode_tile(p, s.tile, b, tx, ty);
+                const int x0 = tx * BM, y0 = ty * BN;
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const bool drop = p.fault == 1 && blockIdx.x == 0 && first;
+                    first = false;
+                    if (!drop) {
+                        const uint32_t fb = smem_u32(&full[stage]);
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        tma_load_3d(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * BK, x0, b * p.x_bmul);
+                        tma_load_3d(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * BK, y0, b * p.y_bmul);
+                        filled |= 1u << stage;
+                        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // Let every load this thread issued land before the CTA can exit.
+            for (int st = 0; st < STAGES; ++st) {
+                if (filled & (1u << st)) {
+                    const uint32_t par = (fill_parity >> st) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(smem_u32(&full[st]), par) &&
+                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool first = true, ok = true;
+            WorkIter w(p);
+            Seg s;
+            while (ok && w.next(s)) {
+                const int buf = local & 1;
+                const uint32_t use = static_cast<uint32_t>(local >> 1);
+                if (!wait_bounded(smem_u32(&tempty[buf]), (use & 1) ^ 1, abort_flag, p.wait_limit)) {
+                    raise_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = smem_u32(xs + stage * C::X_BYTES);
+                    const uint32_t ya = smem_u32(ys + stage * C::Y_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        tc_mma_f16(d_tmem, sw128_kmajor_desc(xa + k * 32), sw128_kmajor_desc(ya + k * 32),
+                                   C::IDESC, (kb > s.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
+                    first = false;
+                    if (!skip)
+                        tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(smem_u32(&tfull[buf]));
+                ++local;
+            }
+            // No MMA may still be running when TMEM is released.
+            tc_commit(smem_u32(drain));
+            const long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(drain), 0) &&
+                   static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        float* stage_buf = epi + q * 32 * 32;
+        int local = 0;
+        WorkIter w(p);
+        Seg s;
+        while (w.next(s)) {
+            const int buf = local & 1;
+            const uint32_t use = static_cast<uint32_t>(local >> 1);
+            if (!wait_bounded(smem_u32(&tfull[buf]), use & 1, abort_flag, p.wait_limit)) {
+                raise_timeout(p, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            int b, tx, ty;
+            decode_tile(p, s.tile, b, tx, ty);
+            const bool partial = s.kb0 != 0 || s.kb1 != p.num_kb;
+            const uint32_t tbase = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            float* obase = p.out + static_cast<int64_t>(b) * p.stride_o;
+            const int x_row0 = tx * BM + q * 32;
+            const int y0 = ty * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
+                if (SWAP) {
+                    // Thread <-> x (consecutive Out columns): each j is one
+                    // coalesced 128-byte row segment across the warp.
+                    const int x = x_row0 + lane;
+                    if (x < p.rows_x) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int y = y0 + c + j;
+                            if (y < p.rows_y) {
+                                float* dst = obase + static_cast<int64_t>(y) * p.ldo + x;
+                                if (partial)
+                                    atomicAdd(dst, __uint_as_float(r[j]));
+                                else
+                                    *dst = __uint_as_float(r[j]);
+                            }
+                        }
+                    }
+                } else {
+                    // Thread <-> row: transpose the 32x32 chunk through shared
+                    // memory (16-byte slots XOR-swizzled by row) so the global
+                    // stores are row-contiguous across the warp.
+                    float4* sb4 = reinterpret_cast<float4*>(stage_buf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        sb4[lane * 8 + (j ^ (lane & 7))] =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    }
+                    __syncwarp();
+                    const int col0 = y0 + c;
+                    if (p.vec4 && !partial) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = i * 4 + (lane >> 3);
+                            const int ch = lane & 7;
+                            const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
+                            const int row = x_row0 + rr;
+                            const int col = col0 + ch * 4;
+                            if (row < p.rows_x) {
+                                float* dst = obase + static_cast<int64_t>(row) * p.ldo + col;
+                                if (col + 3 < p.rows_y) {
+                                    *reinterpret_cast<float4*>(dst) = v;
+                                } else {
+                                    if (col < p.rows_y) dst[0] = v.x;
+                                    if (col + 1 < p.rows_y) dst[1] = v.y;
+                                    if (col + 2 < p.rows_y) dst[2] = v.z;
+                                }
+                            }
+                        }
+                    } else {
+                        const int col = col0 + lane;
+#pragma unroll 4
+                        for (int rr = 0; rr < 32; ++rr) {
+                            const float v = stage_buf[rr * 32 + (((lane >> 2) ^ (rr & 7)) << 2) + (lane & 3)];
+                            const int row = x_row0 + rr;
+                            if (row < p.rows_x && col < p.rows_y) {
+                                float* dst = obase + static_cast<int64_t>(row) * p.ldo + col;
+                                if (partial)
+                                    atomicAdd(dst, v);
+                                else
+                                    *dst = v;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[buf]));
+            ++local;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<C::TMEM_COLS>(tmem_base);
+    }
+}
+
+template <int BN, bool SWAP>
+cudaError_t configure_one()
+{
+    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<BN, SWAP>::SMEM);
+}
+
+template <int BN, bool SWAP>
+cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid,
+                       cudaStream_t stream)
+{
+    tc05_gemm_kernel<BN, SWAP><<<grid, kThreads, Cfg<BN, SWAP>::SMEM, stream>>>(tmx, tmy, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc05_configure(int bn, bool swap)
+{
+    if (swap) {
+        if (bn == 64) return configure_one<64, true>();
+        return cudaErrorInvalidValue;
+    }
+    switch (bn) {
+    case 64: return configure_one<64, false>();
+    case 128: return configure_one<128, false>();
+    case 256: return configure_one<256, false>();
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn, bool swap,
+                        int grid, cudaStream_t stream)
+{
+    if (swap) {
+        if (bn == 64) return launch_one<64, true>(tmx, tmy, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    switch (bn) {
+    case 64: return launch_one<64, false>(tmx, tmy, p, grid, stream);
+    case 128: return launch_one<128, false>(tmx, tmy, p, grid, stream);
+    case 256: return launch_one<256, false>(tmx, tmy, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gnt

@@ -1,0 +1,165 @@
+/*
+ * gemm_nt.h -- C ABI of the GB300 (sm_103a) fp16 -> fp32 matrix product
+ *
+ *     Out = A @ B.T
+ *
+ * with A (M,K) and B (N,K) row-major IEEE binary16, Out (M,N) row-major float32,
+ * float32 accumulation.  This is the product computed by the two worked examples
+ * of the Apache TVM TIRx programming guides: "Warp Matrix Instructions" (opening
+ * paragraph and "From Shared Memory to a Matrix Product": A (16,16), B (8,16),
+ * ldmatrix + mma.sync m16n8k16, fp32 accumulators) and "Blackwell Tensor Cores"
+ * ("The Accumulator's Lifetime": A (128,64), B (64,64), tcgen05.mma kind::f16
+ * with the fp32 accumulator in Tensor Memory).  Both examples start a fresh
+ * accumulator (C = 0, accum=False), so Out is overwritten: there is no alpha,
+ * beta or C input.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers A, B, Out are DEVICE pointers owned by the caller.  A and B hold
+ *     fp16 bit patterns (__half / uint16_t).  The library keeps no reference to
+ *     them after the call's work has run.
+ *   - Sizes and leading dimensions are in ELEMENTS; rows are contiguous:
+ *       A[i,k] = A[i*lda + k],  B[j,k] = B[j*ldb + k],  Out[i,j] = Out[i*ldo + j].
+ *     Batched forms add b*strideA, b*strideB, b*strideO elements for batch b.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t / CUstream;
+ *     NULL = the legacy default stream).  Argument errors are detected on the
+ *     host, return immediately and launch nothing.
+ *   - Empty cases: M == 0, N == 0 or batch == 0 -> GEMM_OK, nothing launched.
+ *     K == 0 -> Out is filled with zeros (the empty sum).
+ *   - Any alignment is accepted.  The tensor-core kernels need 16-byte aligned
+ *     A/B bases and lda, ldb (and strideA, strideB) multiples of 8 elements;
+ *     other inputs run on the warp-MMA kernel, which accepts any layout.
+ *   - Device-side failures (a bounded wait inside a kernel that ran out) are
+ *     recorded in a per-device status word and reported by gemm_nt_check().
+ *   - Thread safety: all entry points may be called concurrently from several
+ *     host threads.  Calls whose Out ranges overlap must not run concurrently.
+ *   - Only devices of compute capability 10.3 (GB300, sm_103a) are supported.
+ */
+#ifndef GEMM_NT_H
+#define GEMM_NT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t and CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* null pointer, negative size, ld < row length, ... */
+    GEMM_ERR_OVERLAP = 2,            /* Out overlaps A or B, or batches of Out overlap */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (launch, tensor map) */
+    GEMM_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait ran out; Out is undefined */
+    GEMM_ERR_NOT_SUPPORTED = 6       /* the requested kernel cannot take these arguments */
+} gemm_status_t;
+
+/* Kernel choice.  GEMM_PATH_AUTO lets the library pick (see gemm_nt_select_path). */
+typedef enum gemm_path {
+    GEMM_PATH_AUTO = 0,
+    GEMM_PATH_TC05 = 1,     /* persistent tcgen05 kernel, TMEM accumulator, one CTA per tile */
+    GEMM_PATH_SKINNY = 2,   /* tcgen05 with swapped operands and split K, for small M */
+    GEMM_PATH_MMASYNC = 3,  /* ldmatrix + mma.sync m16n8k16 warp kernel, any layout */
+    GEMM_PATH_TC05_PAIR = 4 /* tcgen05 on a CTA pair (cta_group::2), 256-row tiles */
+} gemm_path_t;
+
+/*
+ * Out = A @ B.T for one problem.
+ *   A   : M x K, leading dimension lda >= K
+ *   B   : N x K, leading dimension ldb >= K
+ *   Out : M x N float32, leading dimension ldo >= N; must not overlap A or B.
+ * Returns GEMM_OK once the work is enqueued on `stream`.
+ */
+gemm_status_t gemm_nt_f16_f32(const void *A, const void *B, float *Out,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldo,
+                              gemm_stream_t stream);
+
+/*
+ * Strided batch of independent products: for b < batch,
+ *   Out_b = A_b @ B_b.T,  A_b = A + b*strideA,  B_b = B + b*strideB,  Out_b = Out + b*strideO.
+ * strideA or strideB may be 0 (the operand is shared by every batch); strideO
+ * must separate the batches of Out (strideO >= (M-1)*ldo + N when batch > 1).
+ */
+gemm_status_t gemm_nt_f16_f32_batched(const void *A, const void *B, float *Out,
+                                      int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldo,
+                                      int64_t batch, int64_t strideA, int64_t strideB,
+                                      int64_t strideO, gemm_stream_t stream);
+
+/*
+ * As gemm_nt_f16_f32_batched, on an explicitly chosen kernel.  Returns
+ * GEMM_ERR_NOT_SUPPORTED (and launches nothing) if that kernel cannot take the
+ * arguments, e.g. a tensor-core path with unaligned A.
+ */
+gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *Out,
+                                           int64_t M, int64_t N, int64_t K,
+                                           int64_t lda, int64_t ldb, int64_t ldo,
+                                           int64_t batch, int64_t strideA, int64_t strideB,
+                                           int64_t strideO, gemm_path_t path,
+                                           gemm_stream_t stream);
+
+/*
+ * Host-side pipeline for callers whose data lives in host memory: copies A and
+ * B (packed: lda = ldb = K, strideA = M*K, strideB = N*K) from host to the
+ * caller's device buffers dA, dB, runs the batched product into dOut (packed,
+ * ldo = N, strideO = M*N) and copies dOut back to host Out, all on `stream`.
+ * For the copies to be asynchronous the host buffers must be pinned.  The
+ * caller synchronises `stream` before reading Out.  Allocates nothing.
+ */
+gemm_status_t gemm_nt_f16_f32_from_host(const void *A_host, const void *B_host, float *Out_host,
+                                        void *dA, void *dB, float *dOut,
+                                        int64_t M, int64_t N, int64_t K, int64_t batch,
+                                        gemm_stream_t stream);
+
+/*
+ * The kernel GEMM_PATH_AUTO would choose for these arguments (host-only: reads
+ * no device state and makes no CUDA call).  Pointers are used only for their
+ * alignment.
+ */
+gemm_path_t gemm_nt_select_path(const void *A, const void *B, const float *Out,
+                                int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldo,
+                                int64_t batch, int64_t strideA, int64_t strideB,
+                                int64_t strideO);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: GEMM_ERR_DEVICE_TIMEOUT if any kernel launched since the last check hit
+ * its bounded-wait limit, GEMM_ERR_CUDA if the synchronisation failed, else GEMM_OK.
+ */
+gemm_status_t gemm_nt_check(gemm_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char *gemm_nt_status_string(gemm_status_t status);
+
+/*
+ * Diagnostic: one warp executes the warp example of "Warp Matrix Instructions"
+ * ("From Shared Memory to a Matrix Product") on device inputs A (16x16, row-
+ * major fp16) and B (8x16): stage to shared memory, ldmatrix.x4 / .x2, one
+ * mma.sync m16n8k16 with C = 0.  It writes the raw per-lane registers to device
+ * buffers ar (32x4 uint32), br (32x2 uint32), dr (32x4 float), lane-major, so
+ * the fragment maps can be checked.
+ */
+gemm_status_t gemm_nt_probe_m16n8k16(const void *A, const void *B, uint32_t *ar, uint32_t *br,
+                                     float *dr, gemm_stream_t stream);
+
+/*
+ * Test hooks for the bounded waits (not for production use).  Sets, for the
+ * calling process, the wait limit in SM clock cycles of the tcgen05 kernels
+ * (0 restores the default of about two seconds) and a fault to inject into the
+ * next launches on CTA 0: 0 none, 1 the producer drops its first stage, 2 the
+ * MMA thread skips its first stage release.  With a fault injected the kernel
+ * gives up after the limit and gemm_nt_check() returns GEMM_ERR_DEVICE_TIMEOUT.
+ */
+void gemm_nt_debug_set_wait_limit(uint64_t cycles);
+void gemm_nt_debug_set_fault(int fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_NT_H */

@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/gemm_nt.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp16_tensor_gemm_gb300 as gnt
+from dense_fp16_tensor_gemm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_nt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gnt.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gemm_nt_f16_f32", "gemm_nt_f16_f32_batched", "gemm_nt_check",
+              "gemm_nt_status_string", "gemm_nt_select_path"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(gnt._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for s in gnt.Status:
+        assert gnt.status_string(s)
+    assert gnt.status_string(99) == "unknown status"
+
+
+FAKE_A, FAKE_B, FAKE_O = 0x10000000, 0x20000000, 0x30000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE_A, FAKE_B, FAKE_O, -1, 8, 8, 8, 8, 8), gnt.Status.INVALID_VALUE),
+    ((FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 7, 8, 8), gnt.Status.INVALID_VALUE),   # lda < K
+    ((FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 7, 8), gnt.Status.INVALID_VALUE),   # ldb < K
+    ((FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 7), gnt.Status.INVALID_VALUE),   # ldo < N
+    ((0, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8), gnt.Status.INVALID_VALUE),        # null A
+    ((FAKE_A, FAKE_B, 0, 8, 8, 8, 8, 8, 8), gnt.Status.INVALID_VALUE),        # null Out
+    ((FAKE_A, FAKE_B, FAKE_O + 2, 8, 8, 8, 8, 8, 8), gnt.Status.INVALID_VALUE),  # Out not 4-aligned
+    ((FAKE_A, FAKE_B, FAKE_A + 64, 8, 8, 8, 8, 8, 8), gnt.Status.OVERLAP),    # Out inside A
+    ((FAKE_A, FAKE_B, FAKE_B - 16, 8, 8, 8, 8, 8, 8), gnt.Status.OVERLAP),    # Out runs into B
+    ((FAKE_A, FAKE_B, FAKE_O, 2 ** 31, 8, 8, 8, 8, 8), gnt.Status.INVALID_VALUE),
+])
+def test_host_validation(lib, args, status):
+    assert lib.gemm_nt_f16_f32(*args, None) == status
+
+
+def test_empty_problems_launch_nothing(lib):
+    # M, N or batch zero: success without touching the (absent) device
+    assert lib.gemm_nt_f16_f32(FAKE_A, FAKE_B, FAKE_O, 0, 8, 8, 8, 8, 8, None) == 0
+    assert lib.gemm_nt_f16_f32(0, 0, 0, 8, 0, 8, 8, 8, 8, None) == 0
+    assert lib.gemm_nt_f16_f32_batched(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 0, 64, 64, 64,
+                                       None) == 0
+
+
+def test_batched_validation(lib):
+    f = lib.gemm_nt_f16_f32_batched
+    # batches of Out overlap (strideO too small)
+    assert f(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 2, 64, 64, 63, None) == gnt.Status.OVERLAP
+    # negative stride
+    assert f(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 2, -64, 64, 64, None) == gnt.Status.INVALID_VALUE
+    # bad explicit path
+    assert lib.gemm_nt_f16_f32_batched_path(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 1, 0, 0, 0, 99,
+                                            None) == gnt.Status.INVALID_VALUE
+
+
+def test_from_host_validation(lib):
+    f = lib.gemm_nt_f16_f32_from_host
+    assert f(FAKE_A, FAKE_B, FAKE_O, FAKE_A, FAKE_B, 0, 8, 8, 8, 1, None) == gnt.Status.INVALID_VALUE
+    assert f(0, 0, 0, 0, 0, 0, 0, 8, 8, 1, None) == 0
+
+
+def test_path_selection():
+    sel = gnt.gemm_nt_select_path
+    al = 0x10000000
+    # aligned, large -> tcgen05
+    assert sel(al, al + 2 ** 26, al + 2 ** 27, 8192, 8192, 8192, 8192, 8192, 8192) == gnt.Path.TC05
+    assert sel(al, al, al, 128, 64, 64, 64, 64, 64) == gnt.Path.TC05
+    # small M, long N -> swapped tcgen05 (skinny)
+    assert sel(al, al, al, 64, 16384, 8192, 8192, 8192, 16384) == gnt.Path.SKINNY
+    # ragged batched (K=1000: 2000-byte rows are 16-byte multiples) -> tcgen05
+    assert sel(al, al, al, 3001, 2047, 1000, 1000, 1000, 2047, 16, 3001000, 2047000,
+               3001 * 2047) == gnt.Path.TC05
+    # misaligned base, odd leading dimension or batch stride -> warp MMA kernel
+    assert sel(al + 2, al, al, 256, 256, 256, 256, 256, 256) == gnt.Path.MMASYNC
+    assert sel(al, al, al, 256, 256, 250, 250, 256, 256) == gnt.Path.MMASYNC
+    assert sel(al, al, al, 256, 256, 256, 256, 256, 256, 2, 65540, 65536, 65536) == gnt.Path.MMASYNC
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(gnt, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        gnt.load(str(tmp_path / "nope.so"))
+
+
+def test_no_multicast_anywhere():
+    """No TMA multicast form appears in the kernel sources."""
+    csrc = os.path.join(ROOT, "dense_fp16_tensor_gemm_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert ".multicast::cluster" not in open(os.path.join(csrc, f)).read(), f
