@@ -37,6 +37,7 @@ struct DeviceState {
     cudaError_t init_err = cudaSuccess;
     bool supported = false;
     int num_sms = 0;
+    int max_pairs = 0;  // CTA pairs of the pair kernel resident at once
     uint32_t* status = nullptr;
 };
 
@@ -85,6 +86,7 @@ gemm_status_t device_state(DeviceState** out)
         if (e == cudaSuccess) e = tc05_configure(128, false);
         if (e == cudaSuccess) e = tc05_configure(256, false);
         if (e == cudaSuccess) e = tc05_configure(64, true);
+        if (e == cudaSuccess) e = tc05_pair_configure(&d.max_pairs);
         d.status = static_cast<uint32_t*>(sym);
         d.init_err = e;
     });
@@ -176,6 +178,8 @@ gemm_path_t select_path(const Problem& q)
         return GEMM_PATH_MMASYNC;
     if (q.M <= 64 && q.N >= 1024)
         return GEMM_PATH_SKINNY;
+    if (q.M > 128 && q.N > 128)
+        return GEMM_PATH_TC05_PAIR;
     return GEMM_PATH_TC05;
 }
 
@@ -262,20 +266,65 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
     int grid;
-    // Stream-K when there are too few tiles to fill the GPU: each CTA takes an
-    // even share of the (tile, k-block) iterations; tiles cut between CTAs are
-    // summed with atomics into a zeroed Out.
-    if (ntiles < d.num_sms && p.total_iters >= 2 * static_cast<long long>(d.num_sms) && swap) {
-        p.streamk = 1;
+    if (swap && q.batch == 1 && p.tiles_y == 1 && xrows >= 64 * static_cast<int64_t>(d.num_sms) &&
+        xrows <= 128 * static_cast<int64_t>(d.num_sms)) {
+        // Row split: every CTA takes an even share of the rows (at most 128)
+        // over all of K; no partial sums, nothing to zero.
+        p.mode = kModeRowSplit;
+        grid = d.num_sms;
+    } else if (swap && ntiles < d.num_sms && p.total_iters >= 2 * static_cast<long long>(d.num_sms)) {
+        // Stream-K when there are too few tiles to fill the GPU: each CTA takes
+        // an even share of the (tile, k-block) iterations; tiles cut between
+        // CTAs are summed with atomics into a zeroed Out.
+        p.mode = kModeStreamK;
         grid = d.num_sms;
         gemm_status_t z = zero_out(q, stream);
         if (z != GEMM_OK)
             return z;
     } else {
-        p.streamk = 0;
+        p.mode = kModeTiles;
         grid = static_cast<int>(std::min<int64_t>(ntiles, d.num_sms));
     }
     if (tc05_launch(tmx, tmy, p, bn, swap, grid, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+// CTA pairs: 256 x 256 tiles; each CTA loads its 128 rows of A and 128 of the
+// tile's 256 rows of B.
+gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t stream)
+{
+    if (d.max_pairs < 1)
+        return GEMM_ERR_NOT_SUPPORTED;
+    TcParams p{};
+    CUtensorMap tma, tmb;
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, 128, &p.y_bmul))
+        return GEMM_ERR_CUDA;
+    p.out = q.Out;
+    p.ldo = q.ldo;
+    p.stride_o = q.sO;
+    p.rows_x = static_cast<int>(q.M);
+    p.rows_y = static_cast<int>(q.N);
+    p.batch = static_cast<int>(q.batch);
+    p.tiles_x = static_cast<int>((q.M + 255) / 256);
+    p.tiles_y = static_cast<int>((q.N + 255) / 256);
+    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
+    const int64_t ntiles = tpb * q.batch;
+    if (ntiles > INT32_MAX)
+        return GEMM_ERR_NOT_SUPPORTED;
+    p.tiles_per_batch = static_cast<int>(tpb);
+    p.num_tiles = static_cast<int>(ntiles);
+    p.group_x = 8;
+    p.mode = kModeTiles;
+    p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
+    p.vec4 = (aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.status = d.status;
+    p.wait_limit = wait_limit();
+    p.fault = g_fault.load();
+    const int pairs = static_cast<int>(std::min<int64_t>(ntiles, d.max_pairs));
+    if (tc05_pair_launch(tma, tmb, p, pairs, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -332,6 +381,10 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         if (!tma_ok(q))
             return GEMM_ERR_NOT_SUPPORTED;
         return run_tc05(q, *d, true, stream);
+    case GEMM_PATH_TC05_PAIR:
+        if (!tma_ok(q))
+            return GEMM_ERR_NOT_SUPPORTED;
+        return run_tc05_pair(q, *d, stream);
     default:
         return GEMM_ERR_NOT_SUPPORTED;
     }

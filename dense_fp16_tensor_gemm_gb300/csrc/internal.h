@@ -7,6 +7,11 @@
 
 namespace gnt {
 
+// Work distribution of the tcgen05 kernel.
+constexpr int kModeTiles = 0;     // whole tiles, round-robin over CTAs
+constexpr int kModeStreamK = 1;   // even share of (tile, k-block) iterations per CTA
+constexpr int kModeRowSplit = 2;  // even share of rows per CTA (<= 128 each), all of K
+
 // Device status word bits (OR-ed by kernels, read and cleared by gemm_nt_check).
 constexpr uint32_t kStatusTimeout = 1u;
 
@@ -27,7 +32,7 @@ struct TcParams {
     int tiles_per_batch;  // tiles_x * tiles_y
     int num_tiles;        // batch * tiles_per_batch
     int group_x;          // grouped raster: x-tiles per group
-    int streamk;          // 0: whole tiles round-robin; 1: even k-block ranges per CTA
+    int mode;             // kModeTiles, kModeStreamK or kModeRowSplit
     long long total_iters;  // num_tiles * num_kb
     int x_bmul;           // 1 if X's tensor map has a batch dimension, 0 if shared
     int y_bmul;
@@ -53,6 +58,12 @@ struct MmaParams {
 cudaError_t tc05_configure(int bn, bool swap);  // one-time per device
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn,
                         bool swap, int grid, cudaStream_t stream);
+
+// CTA-pair tcgen05 kernel: 256 x 256 tiles on clusters of two CTAs.
+// tc05_pair_configure reports how many pairs can be resident at once.
+cudaError_t tc05_pair_configure(int* max_pairs);  // one-time per device
+cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
+                             cudaStream_t stream);
 
 cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream);
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,

@@ -1,0 +1,232 @@
+// tc05_common.cuh -- pieces shared by the tcgen05 kernels (one CTA per tile,
+// and CTA pairs): work decomposition, bounded mbarrier waits and the epilogue
+// that moves one finished TMEM accumulator to Out.
+#pragma once
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gnt {
+namespace tc {
+
+constexpr int BM = 128;  // MMA rows per CTA (TMEM lanes)
+constexpr int BK = 64;   // K per stage: 64 fp16 = one 128-byte swizzle row
+
+// Tile index -> (batch, x tile, y tile).  Within a batch, tiles are taken in
+// groups of group_x x-tiles, column by column, so CTAs running at the same time
+// share X rows and Y rows in L2.
+__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int& b, int& tx, int& ty)
+{
+    b = tile / p.tiles_per_batch;
+    const int t = tile - b * p.tiles_per_batch;
+    const int span = p.group_x * p.tiles_y;
+    const int g = t / span;
+    const int first_x = g * p.group_x;
+    const int rem_x = p.tiles_x - first_x;
+    const int gx = rem_x < p.group_x ? rem_x : p.group_x;
+    const int r = t - g * span;
+    tx = first_x + r % gx;
+    ty = r / gx;
+}
+
+// One piece of work: output rows [x0, xend) x columns [y0, y0 + BN) of batch b,
+// k-blocks [kb0, kb1).  `partial` when the k range is not the whole of K.
+struct Seg {
+    int b, x0, xend, y0, kb0, kb1;
+    bool partial;
+};
+
+// Walks this CTA's share of the work.
+//   kModeTiles     whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//   kModeStreamK   the contiguous range of (tile, k-block) iterations
+//                  [total*c/G, total*(c+1)/G), cut at tile borders
+//   kModeRowSplit  one piece per CTA: rows [rows_x*c/G, rows_x*(c+1)/G) (at
+//                  most 128) over all of K; the 128-row operand box starts at
+//                  the first row, so neighbouring boxes overlap and only the
+//                  CTA's own rows are stored
+template <int BN>
+struct WorkIter {
+    long long it, end;
+    int tile, step, mode;
+    const TcParams& p;
+
+    __device__ explicit WorkIter(const TcParams& prm) : p(prm)
+    {
+        mode = p.mode;
+        if (mode == kModeStreamK) {
+            it = p.total_iters * blockIdx.x / gridDim.x;
+            end = p.total_iters * (blockIdx.x + 1) / gridDim.x;
+        } else {
+            tile = blockIdx.x;
+            step = gridDim.x;
+        }
+    }
+
+    __device__ bool next(Seg& s)
+    {
+        int t, tx, ty;
+        if (mode == kModeRowSplit) {
+            if (tile >= static_cast<int>(gridDim.x))
+                return false;
+            const long long rx = p.rows_x;
+            s.b = 0;
+            s.x0 = static_cast<int>(rx * tile / gridDim.x);
+            s.xend = static_cast<int>(rx * (tile + 1) / gridDim.x);
+            s.y0 = 0;
+            s.kb0 = 0;
+            s.kb1 = p.num_kb;
+            s.partial = false;
+            tile += step;
+            return true;
+        }
+        if (mode == kModeStreamK) {
+            if (it >= end)
+                return false;
+            t = static_cast<int>(it / p.num_kb);
+            s.kb0 = static_cast<int>(it - static_cast<long long>(t) * p.num_kb);
+            const long long k1 = s.kb0 + (end - it);
+            s.kb1 = k1 < p.num_kb ? static_cast<int>(k1) : p.num_kb;
+            it += s.kb1 - s.kb0;
+        } else {
+            if (tile >= p.num_tiles)
+                return false;
+            t = tile;
+            s.kb0 = 0;
+            s.kb1 = p.num_kb;
+            tile += step;
+        }
+        decode_tile(p, t, s.b, tx, ty);
+        s.x0 = tx * BM;
+        s.xend = s.x0 + BM < p.rows_x ? s.x0 + BM : p.rows_x;
+        s.y0 = ty * BN;
+        s.partial = s.kb0 != 0 || s.kb1 != p.num_kb;
+        return true;
+    }
+};
+
+// Bounded wait.  Returns false if the limit passed or another role aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                             unsigned long long limit)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (static_cast<unsigned long long>(clock64() - t0) > limit)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* abort_flag)
+{
+    *abort_flag = 1;
+    atomicOr(p.status, kStatusTimeout);
+}
+
+
+// One epilogue warp's share of a finished accumulator: TMEM lane quadrant q
+// (tile rows s.x0 + 32q .. +31) and accumulator columns [c_begin, c_end),
+// where `tacc` is the TMEM address of the accumulator's first column.
+// Rows >= s.xend and columns >= rows_y are not stored; `stage_buf` is this
+// warp's 32x32 fp32 staging area (unused when SWAP).
+template <bool SWAP>
+__device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, uint32_t tacc, int q,
+                                               int c_begin, int c_end, int lane, float* stage_buf)
+{
+    const bool partial = s.partial;
+    const uint32_t tbase = tacc + (static_cast<uint32_t>(q * 32) << 16);
+    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    const int x_row0 = s.x0 + q * 32;
+    const int nx = s.xend - x_row0;  // valid rows of this quadrant (may exceed 32)
+    const int y0 = s.y0;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        if (nx <= 0 || y0 + c >= p.rows_y)
+            break;  // warp-uniform: nothing of this chunk is inside Out
+        uint32_t r[32];
+        tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
+        if (SWAP) {
+            // Thread <-> x (consecutive Out columns): each j is one
+            // coalesced 128-byte row segment across the warp.
+            const int ny = p.rows_y - (y0 + c);
+            if (lane < nx) {
+                float* dst = obase + static_cast<int64_t>(y0 + c) * p.ldo + (x_row0 + lane);
+                if (partial) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j < ny) atomicAdd(dst, __uint_as_float(r[j]));
+                        dst += p.ldo;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j < ny) __stcs(dst, __uint_as_float(r[j]));
+                        dst += p.ldo;
+                    }
+                }
+            }
+        } else {
+            // Thread <-> row: transpose the 32x32 chunk through shared
+            // memory (16-byte slots XOR-swizzled by row) so the global
+            // stores are row-contiguous across the warp.
+            float4* sb4 = reinterpret_cast<float4*>(stage_buf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                sb4[lane * 8 + (j ^ (lane & 7))] =
+                    make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            }
+            __syncwarp();
+            const int col0 = y0 + c;
+            if (p.vec4 && !partial) {
+                // 8 lanes per 128-byte row segment, 4 rows per instruction
+                const int ch = lane & 7, rsub = lane >> 3;
+                const int ncol = p.rows_y - (col0 + ch * 4);
+                float* dst = obase + static_cast<int64_t>(x_row0 + rsub) * p.ldo + col0 + ch * 4;
+                const int64_t step = 4 * p.ldo;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = i * 4 + rsub;
+                    const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
+                    if (rr < nx) {
+                        if (ncol >= 4) {
+                            __stcs(reinterpret_cast<float4*>(dst), v);
+                        } else {
+                            if (ncol > 0) __stcs(dst, v.x);
+                            if (ncol > 1) __stcs(dst + 1, v.y);
+                            if (ncol > 2) __stcs(dst + 2, v.z);
+                        }
+                    }
+                    dst += step;
+                }
+            } else if (col0 + lane < p.rows_y) {
+                // one 4-byte column per lane, 32 rows
+                float* dst = obase + static_cast<int64_t>(x_row0) * p.ldo + col0 + lane;
+                const float* src = stage_buf + (lane & 3);
+                const int g = lane >> 2;
+                if (partial) {
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                        if (rr < nx) atomicAdd(dst, v);
+                        dst += p.ldo;
+                    }
+                } else {
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                        if (rr < nx) __stcs(dst, v);
+                        dst += p.ldo;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
+}  // namespace tc
+}  // namespace gnt

@@ -16,23 +16,23 @@
 //   warp 1      allocates 2*BN TMEM columns (two accumulators) and one thread
 //               issues 4 MMAs 128xBNx16 per stage, committing each stage back to
 //               the producer and each finished tile to the epilogue.
-//   warps 2-5   epilogue warpgroup: TMEM -> registers (32x32b.x32) -> global,
-//               overlapped with the next tile's MMAs through the second
-//               accumulator.
+//   warps 2-9   epilogue, two warpgroups: TMEM -> registers (32x32b.x32) ->
+//               global, overlapped with the next tile's MMAs through the
+//               second accumulator.  Each warp owns one TMEM lane quadrant
+//               (32 rows) and half of the tile's columns.
 //
 // Every mbarrier wait is bounded (wait_limit cycles); on expiry the kernel sets
 // the device status word and an abort flag, all roles leave their loops, loads
 // still in flight are waited for, TMEM is freed and the kernel returns.
-#include "internal.h"
-#include "ptx.cuh"
+#include "tc05_common.cuh"
 
 namespace gnt {
 
 namespace {
 
-constexpr int BM = 128;  // MMA M: rows of X per tile (TMEM lanes)
-constexpr int BK = 64;   // K per stage: 64 fp16 = one 128-byte swizzle row
-constexpr int kThreads = 192;
+using namespace tc;
+
+constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 
 template <int BN, bool SWAP>
 struct Cfg {
@@ -40,7 +40,7 @@ struct Cfg {
     static constexpr int X_BYTES = BM * BK * 2;
     static constexpr int Y_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
-    static constexpr int EPI_BYTES = SWAP ? 0 : 4 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
+    static constexpr int EPI_BYTES = SWAP ? 0 : 8 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
     static constexpr int TMEM_COLS = 2 * BN;                      // power of two, >= 32
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -48,95 +48,6 @@ struct Cfg {
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
-
-struct Seg {
-    int tile;
-    int kb0;
-    int kb1;
-};
-
-// Walks this CTA's share of the work.  Tile mode: whole tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ...  Stream-K mode: the contiguous range of
-// (tile, k-block) iterations [total*c/G, total*(c+1)/G), cut at tile borders.
-struct WorkIter {
-    long long it, end;
-    int tile, step, ntiles, nkb, streamk;
-
-    __device__ explicit WorkIter(const TcParams& p)
-    {
-        streamk = p.streamk;
-        nkb = p.num_kb;
-        ntiles = p.num_tiles;
-        if (streamk) {
-            it = p.total_iters * blockIdx.x / gridDim.x;
-            end = p.total_iters * (blockIdx.x + 1) / gridDim.x;
-        } else {
-            tile = blockIdx.x;
-            step = gridDim.x;
-        }
-    }
-
-    __device__ bool next(Seg& s)
-    {
-        if (streamk) {
-            if (it >= end)
-                return false;
-            s.tile = static_cast<int>(it / nkb);
-            s.kb0 = static_cast<int>(it - static_cast<long long>(s.tile) * nkb);
-            long long k1 = s.kb0 + (end - it);
-            s.kb1 = k1 < nkb ? static_cast<int>(k1) : nkb;
-            it += s.kb1 - s.kb0;
-            return true;
-        }
-        if (tile >= ntiles)
-            return false;
-        s.tile = tile;
-        s.kb0 = 0;
-        s.kb1 = nkb;
-        tile += step;
-        return true;
-    }
-};
-
-// Tile index -> (batch, x tile, y tile).  Within a batch, tiles are taken in
-// groups of group_x x-tiles, column by column, so CTAs running at the same time
-// share X rows and Y rows in L2.
-__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int& b, int& tx, int& ty)
-{
-    b = tile / p.tiles_per_batch;
-    const int t = tile - b * p.tiles_per_batch;
-    const int span = p.group_x * p.tiles_y;
-    const int g = t / span;
-    const int first_x = g * p.group_x;
-    const int rem_x = p.tiles_x - first_x;
-    const int gx = rem_x < p.group_x ? rem_x : p.group_x;
-    const int r = t - g * span;
-    tx = first_x + r % gx;
-    ty = r / gx;
-}
-
-// Bounded wait.  Returns false if the limit passed or another role aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
-                                             unsigned long long limit)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*abort_flag)
-            return false;
-        if (static_cast<unsigned long long>(clock64() - t0) > limit)
-            return false;
-    }
-}
-
-__device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* abort_flag)
-{
-    *abort_flag = 1;
-    atomicOr(p.status, kStatusTimeout);
-}
 
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -170,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 128);
+            mbar_init(smem_u32(&tempty[b]), 256);
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
@@ -195,12 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t filled = 0;       // bit s: stage s has a load this thread issued
             uint32_t fill_parity = 0;  // bit s: parity of that fill
             bool first = true, ok = true;
-            WorkIter w(p);
+            WorkIter<BN> w(p);
             Seg s;
             while (ok && w.next(s)) {
-                int b, tx, ty;
-                decode_tile(p, s.tile, b, tx, ty);
-                const int x0 = tx * BM, y0 = ty * BN;
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
@@ -212,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
                         mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                        tma_load_3d(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * BK, x0, b * p.x_bmul);
-                        tma_load_3d(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * BK, y0, b * p.y_bmul);
+                        tma_load_3d(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * BK, s.x0, s.b * p.x_bmul);
+                        tma_load_3d(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * BK, s.y0, s.b * p.y_bmul);
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -241,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int local = 0;
             bool first = true, ok = true;
-            WorkIter w(p);
+            WorkIter<BN> w(p);
             Seg s;
             while (ok && w.next(s)) {
                 const int buf = local & 1;
@@ -289,10 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        float* stage_buf = epi + q * 32 * 32;
+        // Eight warps: warp w reads TMEM lanes 32*(w%4).. (the only quadrant it
+        // may access) and half of the tile's columns.
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const int c_begin = (ew >> 2) * (BN / 2);
+        float* stage_buf = epi + ew * 32 * 32;
         int local = 0;
-        WorkIter w(p);
+        WorkIter<BN> w(p);
         Seg s;
         while (w.next(s)) {
             const int buf = local & 1;
@@ -302,84 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            int b, tx, ty;
-            decode_tile(p, s.tile, b, tx, ty);
-            const bool partial = s.kb0 != 0 || s.kb1 != p.num_kb;
-            const uint32_t tbase = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            float* obase = p.out + static_cast<int64_t>(b) * p.stride_o;
-            const int x_row0 = tx * BM + q * 32;
-            const int y0 = ty * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
-                if (SWAP) {
-                    // Thread <-> x (consecutive Out columns): each j is one
-                    // coalesced 128-byte row segment across the warp.
-                    const int x = x_row0 + lane;
-                    if (x < p.rows_x) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int y = y0 + c + j;
-                            if (y < p.rows_y) {
-                                float* dst = obase + static_cast<int64_t>(y) * p.ldo + x;
-                                if (partial)
-                                    atomicAdd(dst, __uint_as_float(r[j]));
-                                else
-                                    *dst = __uint_as_float(r[j]);
-                            }
-                        }
-                    }
-                } else {
-                    // Thread <-> row: transpose the 32x32 chunk through shared
-                    // memory (16-byte slots XOR-swizzled by row) so the global
-                    // stores are row-contiguous across the warp.
-                    float4* sb4 = reinterpret_cast<float4*>(stage_buf);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        sb4[lane * 8 + (j ^ (lane & 7))] =
-                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    }
-                    __syncwarp();
-                    const int col0 = y0 + c;
-                    if (p.vec4 && !partial) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int rr = i * 4 + (lane >> 3);
-                            const int ch = lane & 7;
-                            const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
-                            const int row = x_row0 + rr;
-                            const int col = col0 + ch * 4;
-                            if (row < p.rows_x) {
-                                float* dst = obase + static_cast<int64_t>(row) * p.ldo + col;
-                                if (col + 3 < p.rows_y) {
-                                    *reinterpret_cast<float4*>(dst) = v;
-                                } else {
-                                    if (col < p.rows_y) dst[0] = v.x;
-                                    if (col + 1 < p.rows_y) dst[1] = v.y;
-                                    if (col + 2 < p.rows_y) dst[2] = v.z;
-                                }
-                            }
-                        }
-                    } else {
-                        const int col = col0 + lane;
-#pragma unroll 4
-                        for (int rr = 0; rr < 32; ++rr) {
-                            const float v = stage_buf[rr * 32 + (((lane >> 2) ^ (rr & 7)) << 2) + (lane & 3)];
-                            const int row = x_row0 + rr;
-                            if (row < p.rows_x && col < p.rows_y) {
-                                float* dst = obase + static_cast<int64_t>(row) * p.ldo + col;
-                                if (partial)
-                                    atomicAdd(dst, v);
-                                else
-                                    *dst = v;
-                            }
-                        }
-                    }
-                    __syncwarp();
-                }
-            }
+            epilogue_store<SWAP>(p, s, tmem_base + static_cast<uint32_t>(buf * BN), q, c_begin, c_begin + BN / 2,
+                                 lane, stage_buf);
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[buf]));
             ++local;

@@ -1,0 +1,298 @@
+// tc05_pair.cu -- tcgen05 kernel on CTA pairs (cta_group::2) for Out = A @ B.T.
+//
+// "Blackwell Tensor Cores" names CTA-pair operation among the MMA forms beyond
+// its single-CTA example.  Here a cluster of two CTAs on two SMs owns a
+// 256 x 256 output tile: CTA r stages rows [128r, 128r+128) of the tile's A
+// panel and rows [128r, 128r+128) of its B panel (half of B) in its own shared
+// memory; the leader CTA (rank 0) issues tcgen05.mma.cta_group::2 with shape
+// 256x256x16, which reads both CTAs' operands and leaves rows [128r, 128r+128)
+// of the fp32 accumulator in CTA r's TMEM.  Compared with one CTA per 128x256
+// tile, each SM moves 32 KB per k-block from L2 instead of 48 KB for the same
+// MMA work.
+//
+// Roles per CTA (320 threads): warp 0 producer, warp 1 TMEM allocation (both
+// CTAs) and MMA issue (leader only), warps 2-9 epilogue.  Synchronisation:
+//   full[s]    in the leader: its producer posts the byte count of both CTAs'
+//              loads; both CTAs' TMA loads complete on it
+//   empty[s]   in each CTA: the leader's MMA commit arrives on both (multicast)
+//   tfull[b]   in each CTA: the leader's commit after a tile's last MMA
+//   tempty[b]  in the leader: one arrival per epilogue warp of both CTAs
+// Every wait is bounded as in the single-CTA kernel.
+#include "tc05_common.cuh"
+
+namespace gnt {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kPairThreads = 320;
+constexpr int PBN = 256;                       // tile columns (B rows) per pair
+constexpr int kStages = 6;
+constexpr int A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A
+constexpr int B_BYTES = (PBN / 2) * BK * 2;    // this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_BYTES = 8 * 32 * 32 * 4;
+constexpr int TMEM_COLS = 2 * PBN;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM = 1024 + kStages * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+constexpr uint32_t IDESC = idesc_f16_f32(2 * BM, PBN);
+constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CTAs
+static_assert(SMEM <= 232448, "shared memory budget");
+static_assert((2 * kStages + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+
+// Pair tiles (256 rows x 256 columns), whole tiles round-robin over pairs.
+struct PairIter {
+    int tile, step, rank;
+    const TcParams& p;
+
+    __device__ PairIter(const TcParams& prm, int r) : rank(r), p(prm)
+    {
+        tile = blockIdx.x >> 1;
+        step = gridDim.x >> 1;
+    }
+
+    __device__ bool next(Seg& s)
+    {
+        if (tile >= p.num_tiles)
+            return false;
+        int tx, ty;
+        decode_tile(p, tile, s.b, tx, ty);
+        s.x0 = tx * 2 * BM + rank * BM;
+        s.xend = s.x0 + BM < p.rows_x ? s.x0 + BM : p.rows_x;
+        s.y0 = ty * PBN;
+        s.kb0 = 0;
+        s.kb1 = p.num_kb;
+        s.partial = false;
+        tile += step;
+        return true;
+    }
+};
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                     const TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* as = smem;
+    uint8_t* bs = smem + kStages * A_BYTES;
+    float* epi = reinterpret_cast<float*>(smem + kStages * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES + EPI_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* tfull = bars + 2 * kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), kTemptyArrivals);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&tma);
+        tma_prefetch_map(&tmb);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;
+            bool first = true, ok = true;
+            PairIter w(p, static_cast<int>(rank));
+            Seg s;
+            while (ok && w.next(s)) {
+                const int yb = s.y0 + static_cast<int>(rank) * (PBN / 2);
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const bool drop = p.fault == 1 && blockIdx.x == 0 && first;
+                    first = false;
+                    if (!drop) {
+                        const uint32_t fb_local = smem_u32(&full[stage]);
+                        const uint32_t fb_leader = mapa_shared(fb_local, 0);
+                        if (leader) {
+                            mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+                            filled |= 1u << stage;
+                            fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        tma_load_3d_pair(smem_u32(as + stage * A_BYTES), &tma, fb_leader, kb * BK, s.x0,
+                                         s.b * p.x_bmul);
+                        tma_load_3d_pair(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, kb * BK, yb,
+                                         s.b * p.y_bmul);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // The leader's full barriers count both CTAs' bytes: waiting for the
+            // last fills lets every load of the pair land before either exits.
+            for (int st = 0; st < kStages; ++st) {
+                if (filled & (1u << st)) {
+                    const uint32_t par = (fill_parity >> st) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(smem_u32(&full[st]), par) &&
+                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool first = true, ok = true;
+            PairIter w(p, 0);
+            Seg s;
+            while (ok && w.next(s)) {
+                const int buf = local & 1;
+                const uint32_t use = static_cast<uint32_t>(local >> 1);
+                if (!wait_bounded(smem_u32(&tempty[buf]), (use & 1) ^ 1, abort_flag, p.wait_limit)) {
+                    raise_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * PBN);
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t aa = smem_u32(as + stage * A_BYTES);
+                    const uint32_t ba = smem_u32(bs + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), IDESC,
+                                        (kb > s.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
+                    first = false;
+                    if (!skip)
+                        tc_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit_pair_mc(smem_u32(&tfull[buf]), 0x3);
+                ++local;
+            }
+            tc_commit_pair(smem_u32(drain));
+            const long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(drain), 0) &&
+                   static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const int c_begin = (ew >> 2) * (PBN / 2);
+        float* stage_buf = epi + ew * 32 * 32;
+        int local = 0;
+        PairIter w(p, static_cast<int>(rank));
+        Seg s;
+        while (w.next(s)) {
+            const int buf = local & 1;
+            const uint32_t use = static_cast<uint32_t>(local >> 1);
+            if (!wait_bounded(smem_u32(&tfull[buf]), use & 1, abort_flag, p.wait_limit)) {
+                raise_timeout(p, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, c_begin,
+                                  c_begin + PBN / 2, lane, stage_buf);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+            ++local;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair<TMEM_COLS>(tmem_base);
+    }
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+}  // namespace
+
+cudaError_t tc05_pair_configure(int* max_pairs)
+{
+    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel, &cfg);
+    if (e != cudaSuccess)
+        return e;
+    *max_pairs = n;
+    return cudaSuccess;
+}
+
+cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
+                             cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(2 * pairs, stream, attr);
+    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel, tma, tmb, p);
+}
+
+}  // namespace gnt

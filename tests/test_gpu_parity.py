@@ -33,7 +33,7 @@ def built():
     gnt.load()
 
 
-@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.MMASYNC])
+@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR, P.MMASYNC])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_small_shapes(path, M, N, K):
     A, B = workloads.make_inputs(0, M, N, K, "uniform", seed=M * 7 + N * 3 + K)
@@ -42,8 +42,12 @@ def test_small_shapes(path, M, N, K):
     assert_parity(out, ref, absdot, what="%s %dx%dx%d" % (path.name, M, N, K))
 
 
+# Swapped-operand shapes covering its three work distributions on a 152-SM
+# GB300: whole tiles (few k-blocks), stream-K (few tiles, long K) and the row
+# split (64..128 rows of N per CTA).
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 64), (7, 2000, 136), (64, 4096, 520), (33, 1500, 1000),
-                                   (64, 16384, 256)])
+                                   (16, 4096, 8192), (64, 16384, 256), (50, 12001, 200),
+                                   (3, 19456, 72)])
 def test_skinny_shapes(M, N, K):
     A, B = workloads.make_inputs(0, M, N, K, "normal", 0.02, seed=M + N + K)
     ref, absdot = oracle.gemm_nt(A, B)
@@ -51,7 +55,7 @@ def test_skinny_shapes(M, N, K):
     assert_parity(out, ref, absdot, what="SKINNY %dx%dx%d" % (M, N, K))
 
 
-@pytest.mark.parametrize("path", [P.TC05, P.SKINNY, P.MMASYNC])
+@pytest.mark.parametrize("path", [P.TC05, P.TC05_PAIR, P.SKINNY, P.MMASYNC])
 def test_integer_inputs_bit_exact(path):
     M = 48 if path == P.SKINNY else 300
     A, B = workloads.make_inputs(0, M, 1100, 1000, "int4", seed=4)
@@ -59,7 +63,7 @@ def test_integer_inputs_bit_exact(path):
     assert_parity(run_path(A, B, path), ref, absdot, exact=True, what=path.name)
 
 
-@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.MMASYNC])
+@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR, P.MMASYNC])
 def test_padded_leading_dimensions(path):
     A, B = workloads.make_inputs(0, 190, 270, 200, "uniform", seed=5)
     ref, absdot = oracle.gemm_nt(A, B)
@@ -78,7 +82,7 @@ def test_misaligned_inputs_use_warp_kernel():
     assert e.value.status == gnt.Status.NOT_SUPPORTED
 
 
-@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.MMASYNC])
+@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR, P.MMASYNC])
 def test_batched_ragged(path):
     A, B = workloads.make_inputs(3, 301, 207, 104, "int4", seed=4)
     ref, absdot = oracle.gemm_nt(A, B)
@@ -93,7 +97,7 @@ def test_batched_shared_operand():
     ref, absdot = oracle.gemm_nt(A, np.broadcast_to(B0, B.shape).copy())
     a = torch.from_numpy(A).cuda()
     b = torch.from_numpy(B0).cuda().unsqueeze(0).expand(4, -1, -1)
-    for path in (P.AUTO, P.MMASYNC):
+    for path in (P.AUTO, P.TC05_PAIR, P.MMASYNC):
         out = gnt.gemm_nt_batched(a, b, path=path)
         gnt.gemm_nt_check()
         assert_parity(out.cpu().numpy(), ref, absdot, what="shared B " + path.name)
@@ -146,14 +150,14 @@ def test_coded_inputs_show_row_per_thread_map():
     accumulator row t.  With A[i,0] = i (else 0) and B[j,0] = 1, Out[i,j] = i;
     with A[i,0] = 1 and B[j,0] = j, Out[i,j] = j.  Any lane or column mix-up in
     the TMEM read-out shows as a wrong row or column value."""
-    M, N, K = 128, 64, 64
-    A = np.zeros((M, K), np.float16); B = np.zeros((N, K), np.float16)
-    A[:, 0] = np.arange(M); B[:, 0] = 1
-    out = run_path(A, B, P.TC05)
-    assert np.array_equal(out, np.repeat(np.arange(M, dtype=np.float32)[:, None], N, 1))
-    A[:, 0] = 1; B[:, 0] = np.arange(N)
-    out = run_path(A, B, P.TC05)
-    assert np.array_equal(out, np.repeat(np.arange(N, dtype=np.float32)[None, :], M, 0))
+    for path, (M, N, K) in ((P.TC05, (128, 64, 64)), (P.TC05_PAIR, (256, 256, 64))):
+        A = np.zeros((M, K), np.float16); B = np.zeros((N, K), np.float16)
+        A[:, 0] = np.arange(M); B[:, 0] = 1
+        out = run_path(A, B, path)
+        assert np.array_equal(out, np.repeat(np.arange(M, dtype=np.float32)[:, None], N, 1)), path.name
+        A[:, 0] = 1; B[:, 0] = np.arange(N)
+        out = run_path(A, B, path)
+        assert np.array_equal(out, np.repeat(np.arange(N, dtype=np.float32)[None, :], M, 0)), path.name
 
 
 def test_identity_and_permutation():
@@ -163,6 +167,6 @@ def test_identity_and_permutation():
     I = np.eye(K, dtype=np.float16)
     p = rng.permutation(K)
     Pm = np.zeros((K, K), np.float16); Pm[np.arange(K), p] = 1
-    for path in (P.TC05, P.MMASYNC):
+    for path in (P.TC05, P.TC05_PAIR, P.MMASYNC):
         assert np.array_equal(run_path(A, I, path), A.astype(np.float32))
         assert np.array_equal(run_path(A, Pm, path), A.astype(np.float32)[:, p])
