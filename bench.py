@@ -121,6 +121,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """Largest value of x over all ranks (the job is as slow as its slowest rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, world, ms_per_step):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -273,12 +289,8 @@ def main():
     gnt.gemm_nt_check(sh)
     per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(per_launch) if flush else starts[0].elapsed_time(ends[-1])
-    ms_step = total_ms / args.steps
-    t = torch.tensor([ms_step], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item())
-    value = w.flops * world / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(total_ms / args.steps, world, "cuda")
+    value = job_tflops(w.flops, world, ms_step)
     kernel_ms = statistics.mean(per_launch)
 
     # ---- end to end through the host-buffer entry point
@@ -303,12 +315,8 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     gnt.gemm_nt_check(sh)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    t = torch.tensor([e2e_ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_ms = float(t.item())
-    e2e_val = w.flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, "cuda")
+    e2e_val = job_tflops(w.flops, world, e2e_ms)
 
     if rank != 0:
         if world > 1:

@@ -17,7 +17,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include "../../include/gemm_nt.h"
+#include "gemm_nt.h"
 #include "internal.h"
 
 namespace gnt {
@@ -240,8 +240,19 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         bn = yrows <= 64 ? 64 : (yrows <= 128 ? 128 : 256);
     }
     TcParams p{};
+    // Row split (swapped operands, one batch, one column tile, 64..128 rows of
+    // X per CTA): every CTA takes an even share of the rows over all of K, with
+    // an X box just tall enough for that share (a multiple of 8 rows).
+    const bool rowsplit = swap && q.batch == 1 && yrows <= bn && xrows >= 64 * static_cast<int64_t>(d.num_sms) &&
+                          xrows <= 128 * static_cast<int64_t>(d.num_sms);
+    int xbox = 128;
+    if (rowsplit) {
+        const int64_t share = (xrows + d.num_sms - 1) / d.num_sms;
+        xbox = static_cast<int>(std::min<int64_t>(128, (share + 7) / 8 * 8));
+    }
+    p.x_box_bytes = xbox * 128;
     CUtensorMap tmx, tmy;
-    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, 128, &p.x_bmul) ||
+    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul) ||
         !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
@@ -266,10 +277,8 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
     int grid;
-    if (swap && q.batch == 1 && p.tiles_y == 1 && xrows >= 64 * static_cast<int64_t>(d.num_sms) &&
-        xrows <= 128 * static_cast<int64_t>(d.num_sms)) {
-        // Row split: every CTA takes an even share of the rows (at most 128)
-        // over all of K; no partial sums, nothing to zero.
+    if (rowsplit) {
+        // no partial sums, nothing to zero
         p.mode = kModeRowSplit;
         grid = d.num_sms;
     } else if (swap && ntiles < d.num_sms && p.total_iters >= 2 * static_cast<long long>(d.num_sms)) {

@@ -37,6 +37,7 @@ struct TcParams {
     int x_bmul;           // 1 if X's tensor map has a batch dimension, 0 if shared
     int y_bmul;
     int vec4;             // Out base and ldo allow 16-byte stores
+    int x_box_bytes;      // bytes of one X box (its height x 128 B; at most 16 KB)
     uint32_t* status;     // device status word
     unsigned long long wait_limit;  // bounded-wait limit, SM clock cycles
     int fault;            // test hook: 0 none, 1 drop a producer stage, 2 skip a release

@@ -187,10 +187,12 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), with the default CTA-scope release: it does not wait for this
+// thread's earlier global stores, which no consumer of this barrier reads.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // 3-D tiled load into this CTA's shared memory whose byte count completes on an

@@ -36,7 +36,7 @@ constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 
 template <int BN, bool SWAP>
 struct Cfg {
-    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? 9 : 8));
     static constexpr int X_BYTES = BM * BK * 2;
     static constexpr int Y_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
-                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES);
                         tma_load_3d(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * BK, s.x0, s.b * p.x_bmul);
                         tma_load_3d(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * BK, s.y0, s.b * p.y_bmul);
                         filled |= 1u << stage;
