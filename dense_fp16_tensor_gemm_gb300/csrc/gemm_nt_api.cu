@@ -39,6 +39,12 @@ struct DeviceState {
     int num_sms = 0;
     int max_pairs = 0;  // CTA pairs of the pair kernel resident at once
     uint32_t* status = nullptr;
+    // host-buffer pipeline: copy streams and events, created on first use
+    std::once_flag pipe_once;
+    cudaError_t pipe_err = cudaSuccess;
+    std::mutex pipe_mu;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev[2 + 2 * 4];
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -183,8 +189,32 @@ gemm_path_t select_path(const Problem& q)
     return GEMM_PATH_TC05;
 }
 
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-              int64_t stride, int box_rows, int* bmul)
+// Tensor maps depend only on the address and geometry, so each host thread
+// keeps the last few it encoded (no lock needed) and repeat calls skip the
+// driver's encoder.
+struct MapKey {
+    const void* base;
+    int64_t rows, K, ld, batch, stride;
+    int box_rows;
+    bool operator==(const MapKey& o) const
+    {
+        return base == o.base && rows == o.rows && K == o.K && ld == o.ld && batch == o.batch &&
+               stride == o.stride && box_rows == o.box_rows;
+    }
+};
+
+struct MapCache {
+    static constexpr int kEntries = 16;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    int bmul[kEntries];
+    int count = 0, next = 0;
+};
+
+thread_local MapCache t_maps;
+
+bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
+                int64_t stride, int box_rows, int* bmul)
 {
     auto enc = encode_fn();
     if (!enc)
@@ -201,6 +231,30 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
+              int64_t stride, int box_rows, int* bmul)
+{
+    const MapKey k{base, rows, K, ld, batch, stride, box_rows};
+    MapCache& c = t_maps;
+    for (int i = 0; i < c.count; ++i) {
+        if (c.key[i] == k) {
+            *map = c.map[i];
+            *bmul = c.bmul[i];
+            return true;
+        }
+    }
+    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul))
+        return false;
+    const int slot = c.next;
+    c.key[slot] = k;
+    c.map[slot] = *map;
+    c.bmul[slot] = *bmul;
+    c.next = (slot + 1) % MapCache::kEntries;
+    if (c.count < MapCache::kEntries)
+        ++c.count;
+    return true;
 }
 
 gemm_status_t zero_out(const Problem& q, cudaStream_t stream)
@@ -361,6 +415,18 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     return mmasync_launch(p, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+constexpr int kPipeChunks = 4;
+
+// Host buffers in, host buffer out, with the copies overlapped with the
+// products: the problem is cut into up to four chunks (rows of A and Out for a
+// single product, whole batches otherwise).  One library stream copies inputs
+// to the device, the caller's stream runs each chunk's product once its inputs
+// have arrived, a second library stream copies each chunk's Out back as soon as
+// it is done, and the caller's stream finally waits for that last copy.
+gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float* Out_host, uint16_t* dA,
+                                  uint16_t* dB, float* dOut, int64_t M, int64_t N, int64_t K, int64_t batch,
+                                  cudaStream_t stream);
+
 gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
 {
     gemm_status_t st = validate(q);
@@ -397,6 +463,81 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
     default:
         return GEMM_ERR_NOT_SUPPORTED;
     }
+}
+
+gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float* Out_host, uint16_t* dA,
+                                  uint16_t* dB, float* dOut, int64_t M, int64_t N, int64_t K, int64_t batch,
+                                  cudaStream_t stream)
+{
+    DeviceState* d = nullptr;
+    gemm_status_t st = device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    std::call_once(d->pipe_once, [d] {
+        cudaError_t e = cudaStreamCreateWithFlags(&d->h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d->d2h, cudaStreamNonBlocking);
+        for (auto& ev : d->ev)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        d->pipe_err = e;
+    });
+    if (d->pipe_err != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    // chunks: [first, first + count) of batches, or of rows when batch == 1
+    const bool by_rows = batch == 1;
+    const int64_t units = by_rows ? M : batch;
+    int64_t per = units;
+    if (by_rows && M >= 1024)
+        per = ((M + kPipeChunks - 1) / kPipeChunks + 255) / 256 * 256;
+    else if (!by_rows)
+        per = (batch + kPipeChunks - 1) / kPipeChunks;
+    const int nchunks = static_cast<int>((units + per - 1) / per);
+    const uint8_t* ha = static_cast<const uint8_t*>(A_host);
+    const uint8_t* hb = static_cast<const uint8_t*>(B_host);
+    uint8_t* ho = reinterpret_cast<uint8_t*>(Out_host);
+
+    std::lock_guard<std::mutex> lock(d->pipe_mu);  // the events are shared by calls on this device
+    cudaEvent_t ev_start = d->ev[0], ev_done = d->ev[1];
+    cudaEvent_t* ev_in = d->ev + 2;
+    cudaEvent_t* ev_out = d->ev + 2 + kPipeChunks;
+    if (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(d->h2d, ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(d->d2h, ev_start, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const size_t a_unit = static_cast<size_t>(by_rows ? K : M * K) * 2;  // bytes per row / per batch of A
+    const size_t b_unit = static_cast<size_t>(N * K) * 2;                // bytes per batch of B
+    const size_t o_unit = static_cast<size_t>(by_rows ? N : M * N) * 4;
+    if (by_rows && K > 0 && cudaMemcpyAsync(dB, hb, b_unit, cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t first = c * per, count = std::min(per, units - first);
+        if (K > 0) {
+            if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dA) + first * a_unit, ha + first * a_unit, count * a_unit,
+                                cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            if (!by_rows && cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dB) + first * b_unit, hb + first * b_unit,
+                                            count * b_unit, cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+        if (cudaEventRecord(ev_in[c], d->h2d) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t first = c * per, count = std::min(per, units - first);
+        if (cudaStreamWaitEvent(stream, ev_in[c], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        Problem q = by_rows ? Problem{dA + first * K, dB, dOut + first * N, count, N, K, K, K, N, 1, 0, 0, 0}
+                            : Problem{dA + first * M * K, dB + first * N * K, dOut + first * M * N, M, N, K, K, K, N,
+                                      count, M * K, N * K, M * N};
+        st = run(q, GEMM_PATH_AUTO, stream);
+        if (st != GEMM_OK)
+            return st;
+        if (cudaEventRecord(ev_out[c], stream) != cudaSuccess || cudaStreamWaitEvent(d->d2h, ev_out[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(ho + first * o_unit, reinterpret_cast<uint8_t*>(dOut) + first * o_unit, count * o_unit,
+                            cudaMemcpyDeviceToHost, d->d2h) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    if (cudaEventRecord(ev_done, d->d2h) != cudaSuccess || cudaStreamWaitEvent(stream, ev_done, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
 }
 
 }  // namespace
@@ -440,25 +581,12 @@ gemm_status_t gemm_nt_f16_f32_from_host(const void* A_host, const void* B_host, 
         return GEMM_OK;
     if (!Out_host || !dOut || (K > 0 && (!A_host || !B_host || !dA || !dB)))
         return GEMM_ERR_INVALID_VALUE;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     Problem q{dA, dB, dOut, M, N, K, K, K, N, batch, M * K, N * K, M * N};
     gemm_status_t st = gnt::validate(q);
     if (st != GEMM_OK)
         return st;
-    if (K > 0) {
-        if (cudaMemcpyAsync(dA, A_host, static_cast<size_t>(batch * M * K * 2), cudaMemcpyHostToDevice, s) !=
-                cudaSuccess ||
-            cudaMemcpyAsync(dB, B_host, static_cast<size_t>(batch * N * K * 2), cudaMemcpyHostToDevice, s) !=
-                cudaSuccess)
-            return GEMM_ERR_CUDA;
-    }
-    st = gnt::run(q, GEMM_PATH_AUTO, s);
-    if (st != GEMM_OK)
-        return st;
-    if (cudaMemcpyAsync(Out_host, dOut, static_cast<size_t>(batch * M * N * 4), cudaMemcpyDeviceToHost, s) !=
-        cudaSuccess)
-        return GEMM_ERR_CUDA;
-    return GEMM_OK;
+    return gnt::from_host_pipelined(A_host, B_host, Out_host, static_cast<uint16_t*>(dA), static_cast<uint16_t*>(dB),
+                                    dOut, M, N, K, batch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_path_t gemm_nt_select_path(const void* A, const void* B, const float* Out, int64_t M, int64_t N, int64_t K,

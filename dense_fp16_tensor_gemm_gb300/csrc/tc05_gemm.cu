@@ -34,10 +34,14 @@ using namespace tc;
 
 constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 
-template <int BN, bool SWAP>
+// XR: rows of X staged per stage.  128 normally; 112 for the row split of the
+// swapped path (shares of at most 112 rows), which packs 10 stages instead of
+// 9.  The MMA still reads 128 rows: rows XR..127 come from the next slot and
+// only feed accumulator rows that are never stored.
+template <int BN, bool SWAP, int XR = 128>
 struct Cfg {
-    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? 9 : 8));
-    static constexpr int X_BYTES = BM * BK * 2;
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? (XR <= 112 ? 10 : 9) : 8));
+    static constexpr int X_BYTES = XR * BK * 2;
     static constexpr int Y_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
     static constexpr int EPI_BYTES = SWAP ? 0 : 8 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
@@ -47,14 +51,15 @@ struct Cfg {
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(X_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
 };
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int XR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const TcParams p)
 {
-    using C = Cfg<BN, SWAP>;
+    using C = Cfg<BN, SWAP, XR>;
     constexpr int STAGES = C::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -230,18 +235,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int XR = 128>
 cudaError_t configure_one()
 {
-    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<BN, SWAP>::SMEM);
+    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<BN, SWAP, XR>::SMEM);
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int XR = 128>
 cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid,
                        cudaStream_t stream)
 {
-    tc05_gemm_kernel<BN, SWAP><<<grid, kThreads, Cfg<BN, SWAP>::SMEM, stream>>>(tmx, tmy, p);
+    tc05_gemm_kernel<BN, SWAP, XR><<<grid, kThreads, Cfg<BN, SWAP, XR>::SMEM, stream>>>(tmx, tmy, p);
     return cudaGetLastError();
 }
 
@@ -250,8 +255,10 @@ cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcP
 cudaError_t tc05_configure(int bn, bool swap)
 {
     if (swap) {
-        if (bn == 64) return configure_one<64, true>();
-        return cudaErrorInvalidValue;
+        if (bn != 64)
+            return cudaErrorInvalidValue;
+        cudaError_t e = configure_one<64, true>();
+        return e == cudaSuccess ? configure_one<64, true, 112>() : e;
     }
     switch (bn) {
     case 64: return configure_one<64, false>();
@@ -265,8 +272,11 @@ cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const Tc
                         int grid, cudaStream_t stream)
 {
     if (swap) {
-        if (bn == 64) return launch_one<64, true>(tmx, tmy, p, grid, stream);
-        return cudaErrorInvalidValue;
+        if (bn != 64)
+            return cudaErrorInvalidValue;
+        if (p.x_box_bytes <= 112 * 128)
+            return launch_one<64, true, 112>(tmx, tmy, p, grid, stream);
+        return launch_one<64, true>(tmx, tmy, p, grid, stream);
     }
     switch (bn) {
     case 64: return launch_one<64, false>(tmx, tmy, p, grid, stream);

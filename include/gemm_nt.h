@@ -106,9 +106,17 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *
  * Host-side pipeline for callers whose data lives in host memory: copies A and
  * B (packed: lda = ldb = K, strideA = M*K, strideB = N*K) from host to the
  * caller's device buffers dA, dB, runs the batched product into dOut (packed,
- * ldo = N, strideO = M*N) and copies dOut back to host Out, all on `stream`.
- * For the copies to be asynchronous the host buffers must be pinned.  The
- * caller synchronises `stream` before reading Out.  Allocates nothing.
+ * ldo = N, strideO = M*N) and copies dOut back to host Out.  The work is cut
+ * into up to four chunks (row blocks of A and Out when batch == 1, groups of
+ * batches otherwise) so that copies in both directions overlap the products:
+ * inputs travel on a library-owned copy stream, each chunk's product runs on
+ * `stream` once its inputs have arrived, and its Out travels back on a second
+ * library-owned stream; `stream` finally waits for the last copy, so
+ * synchronising `stream` is enough before reading Out.  For the copies to be
+ * asynchronous the host buffers must be pinned.  No device memory is
+ * allocated; the two copy streams and ten events are created once per device,
+ * on the first call (make that first call outside any stream capture).  Calls
+ * on one device are enqueued one at a time (an internal lock).
  */
 gemm_status_t gemm_nt_f16_f32_from_host(const void *A_host, const void *B_host, float *Out_host,
                                         void *dA, void *dB, float *dOut,

@@ -128,21 +128,26 @@ def test_torch_wrapper_and_streams():
     assert_parity(out.cpu().numpy(), ref, absdot, what="torch wrapper")
 
 
-def test_from_host_pipeline():
+@pytest.mark.parametrize("batch,M,N,K", [(2, 130, 260, 192), (5, 70, 90, 64), (1, 2000, 300, 136),
+                                         (1, 100, 50, 40)])
+def test_from_host_pipeline(batch, M, N, K):
+    """Host buffers in and out; chunks of batches or of rows overlap the copies."""
     import torch
-    A, B = workloads.make_inputs(2, 130, 260, 192, "uniform", seed=10)
+    A, B = workloads.make_inputs(batch, M, N, K, "uniform", seed=10)
     ref, absdot = oracle.gemm_nt(A, B)
     ha = torch.from_numpy(A).pin_memory()
     hb = torch.from_numpy(B).pin_memory()
-    ho = torch.empty((2, 130, 260), dtype=torch.float32).pin_memory()
+    ho = torch.full((batch, M, N), float("nan"), dtype=torch.float32).pin_memory()
     da = torch.empty_like(ha, device="cuda")
     db = torch.empty_like(hb, device="cuda")
     do = torch.empty_like(ho, device="cuda")
     st = torch.cuda.current_stream()
-    gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), da.data_ptr(),
-                                  db.data_ptr(), do.data_ptr(), 130, 260, 192, 2, st.cuda_stream)
-    gnt.gemm_nt_check(st.cuda_stream)
-    assert_parity(ho.numpy(), ref, absdot, what="from_host")
+    for _ in range(2):  # twice: the second call reuses the streams and events
+        gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), da.data_ptr(),
+                                      db.data_ptr(), do.data_ptr(), M, N, K, batch, st.cuda_stream)
+        gnt.gemm_nt_check(st.cuda_stream)
+        assert_parity(ho.numpy(), ref, absdot, what="from_host")
+        ho.fill_(float("nan"))
 
 
 def test_coded_inputs_show_row_per_thread_map():
