@@ -256,6 +256,22 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel in the stream be scheduled before this one finishes
+// (it still waits in pdl_wait before touching memory).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every grid this one depends on has completed and its memory
+// operations are visible; returns at once when launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                             uint32_t& r3)

@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only this CTA's shared memory and TMEM; global
+    // memory is read and written only after the preceding grids are done.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -246,8 +250,17 @@ template <int BN, bool SWAP, int XR = 128>
 cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid,
                        cudaStream_t stream)
 {
-    tc05_gemm_kernel<BN, SWAP, XR><<<grid, kThreads, Cfg<BN, SWAP, XR>::SMEM, stream>>>(tmx, tmy, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<BN, SWAP, XR>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR>, tmx, tmy, p);
 }
 
 }  // namespace

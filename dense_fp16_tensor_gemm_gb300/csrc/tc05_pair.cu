@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait();  // global memory only after the preceding grids are done
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -265,8 +267,10 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
@@ -277,7 +281,7 @@ cudaError_t tc05_pair_configure(int* max_pairs)
     cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess)
         return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel, &cfg);
@@ -290,7 +294,7 @@ cudaError_t tc05_pair_configure(int* max_pairs)
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
                              cudaStream_t stream)
 {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2 * pairs, stream, attr);
     return cudaLaunchKernelEx(&cfg, tc05_pair_kernel, tma, tmb, p);
 }
