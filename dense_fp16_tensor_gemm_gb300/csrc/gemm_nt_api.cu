@@ -11,7 +11,9 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -102,6 +104,53 @@ gemm_status_t device_state(DeviceState** out)
         return GEMM_ERR_UNSUPPORTED_DEVICE;
     *out = &d;
     return GEMM_OK;
+}
+
+// Stream-K workspace of the pair kernel, one per (device, stream) so that calls
+// on different streams never share one; allocated and zeroed on first use and
+// kept until the process exits (about 38 MB with 76 pairs).
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+gemm_status_t stream_workspace(cudaStream_t stream, size_t bytes, void** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace& w = g_ws[std::make_pair(dev, stream)];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(w.ptr) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        if (cudaMalloc(&w.ptr, bytes) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMemset(w.ptr, 0, bytes) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return GEMM_OK;
+}
+
+// After a kernel gave up (bounded wait), its stream-K counters may be left
+// non-zero: clear every workspace of the current device.
+void reset_workspaces()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    for (auto& kv : g_ws)
+        if (kv.first.first == dev && kv.second.ptr)
+            cudaMemset(kv.second.ptr, 0, kv.second.bytes);
 }
 
 struct Problem {
@@ -386,7 +435,33 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     p.status = d.status;
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
-    const int pairs = static_cast<int>(std::min<int64_t>(ntiles, d.max_pairs));
+    // Stream-K when there are far fewer tiles than pairs and K is long (e.g.
+    // 512 x 512 x 8192: 4 tiles for 76 pairs): every tile is cut into at most
+    // kMaxPieces k ranges spread over the pairs; the warp that finishes a
+    // portion last sums its slices.  That sum sits on the critical path (a few
+    // microseconds), so the last partial round of a large problem is left to
+    // whole tiles.
+    constexpr int64_t kMaxPieces = 4;
+    constexpr int64_t kMinKBlocks = 96;
+    const int P = d.max_pairs;
+    const int64_t rem = ntiles < P / 2 ? ntiles : 0;
+    const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
+    int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
+    p.sk_first = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_pairs = 0;
+    if (rem != 0 && p.num_kb >= kMinKBlocks) {
+        void* ws = nullptr;
+        gemm_status_t st = stream_workspace(stream, pair_workspace_bytes(P), &ws);
+        if (st != GEMM_OK)
+            return st;
+        p.sk_first = static_cast<int>(ntiles - rem);
+        p.sk_iters = rem * p.num_kb;
+        p.sk_pairs = static_cast<int>(sk_pairs);
+        p.ws = static_cast<float*>(ws);
+        p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(P) * 4 * kPairSliceBytes);
+        pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
+    }
     if (tc05_pair_launch(tma, tmb, p, pairs, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
@@ -612,6 +687,7 @@ gemm_status_t gemm_nt_check(gemm_stream_t stream)
         const uint32_t zero = 0;
         if (cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return GEMM_ERR_CUDA;
+        gnt::reset_workspaces();
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
     return GEMM_OK;

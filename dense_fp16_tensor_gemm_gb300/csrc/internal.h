@@ -38,6 +38,15 @@ struct TcParams {
     int y_bmul;
     int vec4;             // Out base and ldo allow 16-byte stores
     int x_box_bytes;      // bytes of one X box (its height x 128 B; at most 16 KB)
+    // Stream-K on the pair kernel: tiles [sk_first, num_tiles) are cut into
+    // even k-block ranges, one per pair.  Each partial piece leaves its slice in
+    // ws; per-(tile, CTA, epilogue warp) counters in ws_flags pick the warp that
+    // arrives last, which sums the slices in k order and stores Out.
+    int sk_first;           // = num_tiles when stream-K is off
+    long long sk_iters;     // (num_tiles - sk_first) * num_kb
+    int sk_pairs;           // pairs [0, sk_pairs) share the stream-K iterations
+    float* ws;              // [pairs][2 slots][2 CTAs][8 warps][4 chunks][32 cols][32 rows] fp32
+    uint32_t* ws_flags;     // [stream-K tiles][2 CTAs][8 warps], zero between launches
     uint32_t* status;     // device status word
     unsigned long long wait_limit;  // bounded-wait limit, SM clock cycles
     int fault;            // test hook: 0 none, 1 drop a producer stage, 2 skip a release
@@ -63,6 +72,12 @@ cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const Tc
 // CTA-pair tcgen05 kernel: 256 x 256 tiles on clusters of two CTAs.
 // tc05_pair_configure reports how many pairs can be resident at once.
 cudaError_t tc05_pair_configure(int* max_pairs);  // one-time per device
+// Workspace bytes the pair kernel's stream-K pieces need for `pairs` pairs.
+constexpr size_t kPairSliceBytes = 128 * 256 * 4;
+inline size_t pair_workspace_bytes(int pairs)
+{
+    return static_cast<size_t>(pairs) * 4 * kPairSliceBytes + static_cast<size_t>(pairs) * 2 * 8 * 4;
+}
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
                              cudaStream_t stream);
 

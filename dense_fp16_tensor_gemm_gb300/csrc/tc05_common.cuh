@@ -33,6 +33,8 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int& b,
 struct Seg {
     int b, x0, xend, y0, kb0, kb1;
     bool partial;
+    int sk_t;  // stream-K tile index (from sk_first), -1 outside stream-K
+    int slot;  // workspace slot of a stream-K piece: 0 first of the CTA's range, 1 last
 };
 
 // Walks this CTA's share of the work.
@@ -64,6 +66,8 @@ struct WorkIter {
     __device__ bool next(Seg& s)
     {
         int t, tx, ty;
+        s.sk_t = -1;
+        s.slot = 0;
         if (mode == kModeRowSplit) {
             if (tile >= static_cast<int>(gridDim.x))
                 return false;
@@ -127,11 +131,70 @@ __device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* a
 }
 
 
+// Stores one 32x32 chunk of the accumulator held row-per-thread (lane i has
+// row x_row0 + i, columns col0..col0+31 in r[]): transpose through shared
+// memory (16-byte slots XOR-swizzled by row) so the global stores are
+// row-contiguous across the warp.  Rows beyond nx and columns beyond rows_y
+// are not stored; `atomic` adds into Out instead of storing.
+__device__ __forceinline__ void store_rows_chunk(const TcParams& p, float* obase, int x_row0, int nx, int col0,
+                                                 const float (&v)[32], int lane, float* stage_buf, bool atomic)
+{
+    float4* sb4 = reinterpret_cast<float4*>(stage_buf);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        sb4[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    if (p.vec4 && !atomic) {
+        // 8 lanes per 128-byte row segment, 4 rows per instruction
+        const int ch = lane & 7, rsub = lane >> 3;
+        const int ncol = p.rows_y - (col0 + ch * 4);
+        float* dst = obase + static_cast<int64_t>(x_row0 + rsub) * p.ldo + col0 + ch * 4;
+        const int64_t step = 4 * p.ldo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + rsub;
+            const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
+            if (rr < nx) {
+                if (ncol >= 4) {
+                    __stcs(reinterpret_cast<float4*>(dst), v);
+                } else {
+                    if (ncol > 0) __stcs(dst, v.x);
+                    if (ncol > 1) __stcs(dst + 1, v.y);
+                    if (ncol > 2) __stcs(dst + 2, v.z);
+                }
+            }
+            dst += step;
+        }
+    } else if (col0 + lane < p.rows_y) {
+        // one 4-byte column per lane, 32 rows
+        float* dst = obase + static_cast<int64_t>(x_row0) * p.ldo + col0 + lane;
+        const float* src = stage_buf + (lane & 3);
+        const int g = lane >> 2;
+        if (atomic) {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                if (rr < nx) atomicAdd(dst, v);
+                dst += p.ldo;
+            }
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                if (rr < nx) __stcs(dst, v);
+                dst += p.ldo;
+            }
+        }
+    }
+    __syncwarp();
+}
+
 // One epilogue warp's share of a finished accumulator: TMEM lane quadrant q
 // (tile rows s.x0 + 32q .. +31) and accumulator columns [c_begin, c_end),
 // where `tacc` is the TMEM address of the accumulator's first column.
 // Rows >= s.xend and columns >= rows_y are not stored; `stage_buf` is this
-// warp's 32x32 fp32 staging area (unused when SWAP).
+// warp's 32x32 fp32 staging area (unused when SWAP).  Partial segments (a
+// k range short of all of K) add into Out with atomics.
 template <bool SWAP>
 __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, uint32_t tacc, int q,
                                                int c_begin, int c_end, int lane, float* stage_buf)
@@ -169,61 +232,11 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, 
                 }
             }
         } else {
-            // Thread <-> row: transpose the 32x32 chunk through shared
-            // memory (16-byte slots XOR-swizzled by row) so the global
-            // stores are row-contiguous across the warp.
-            float4* sb4 = reinterpret_cast<float4*>(stage_buf);
+            float v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                sb4[lane * 8 + (j ^ (lane & 7))] =
-                    make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            }
-            __syncwarp();
-            const int col0 = y0 + c;
-            if (p.vec4 && !partial) {
-                // 8 lanes per 128-byte row segment, 4 rows per instruction
-                const int ch = lane & 7, rsub = lane >> 3;
-                const int ncol = p.rows_y - (col0 + ch * 4);
-                float* dst = obase + static_cast<int64_t>(x_row0 + rsub) * p.ldo + col0 + ch * 4;
-                const int64_t step = 4 * p.ldo;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = i * 4 + rsub;
-                    const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
-                    if (rr < nx) {
-                        if (ncol >= 4) {
-                            __stcs(reinterpret_cast<float4*>(dst), v);
-                        } else {
-                            if (ncol > 0) __stcs(dst, v.x);
-                            if (ncol > 1) __stcs(dst + 1, v.y);
-                            if (ncol > 2) __stcs(dst + 2, v.z);
-                        }
-                    }
-                    dst += step;
-                }
-            } else if (col0 + lane < p.rows_y) {
-                // one 4-byte column per lane, 32 rows
-                float* dst = obase + static_cast<int64_t>(x_row0) * p.ldo + col0 + lane;
-                const float* src = stage_buf + (lane & 3);
-                const int g = lane >> 2;
-                if (partial) {
-#pragma unroll
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
-                        if (rr < nx) atomicAdd(dst, v);
-                        dst += p.ldo;
-                    }
-                } else {
-#pragma unroll
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
-                        if (rr < nx) __stcs(dst, v);
-                        dst += p.ldo;
-                    }
-                }
-            }
-            __syncwarp();
+            for (int k = 0; k < 32; ++k)
+                v[k] = __uint_as_float(r[k]);
+            store_rows_chunk(p, obase, x_row0, nx, y0 + c, v, lane, stage_buf, partial);
         }
     }
 }

@@ -41,33 +41,160 @@ constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CT
 static_assert(SMEM <= 232448, "shared memory budget");
 static_assert((2 * kStages + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 
-// Pair tiles (256 rows x 256 columns), whole tiles round-robin over pairs.
+// Pair tiles (256 rows x 256 columns): tiles [0, sk_first) whole and round-robin
+// over the pairs; then, for stream-K, pair q < S takes the k-block iterations
+// [I*q/S, I*(q+1)/S) of the remaining tiles (I = sk_iters, S = sk_pairs), cut
+// at tile borders.
 struct PairIter {
-    int tile, step, rank;
+    int tile, step, rank, pair;
+    long long it, it0, end;
+    bool in_sk;
     const TcParams& p;
 
     __device__ PairIter(const TcParams& prm, int r) : rank(r), p(prm)
     {
-        tile = blockIdx.x >> 1;
+        pair = blockIdx.x >> 1;
         step = gridDim.x >> 1;
+        tile = pair;
+        in_sk = false;
+        if (pair < p.sk_pairs) {
+            it0 = it = p.sk_iters * pair / p.sk_pairs;
+            end = p.sk_iters * (pair + 1) / p.sk_pairs;
+        } else {
+            it0 = it = end = 0;
+        }
     }
 
     __device__ bool next(Seg& s)
     {
-        if (tile >= p.num_tiles)
-            return false;
+        int t;
+        if (!in_sk && tile < p.sk_first) {
+            t = tile;
+            tile += step;
+            s.kb0 = 0;
+            s.kb1 = p.num_kb;
+            s.partial = false;
+            s.sk_t = -1;
+            s.slot = 0;
+        } else {
+            in_sk = true;
+            if (it >= end)
+                return false;
+            const int tl = static_cast<int>(it / p.num_kb);
+            s.kb0 = static_cast<int>(it - static_cast<long long>(tl) * p.num_kb);
+            const long long k1 = s.kb0 + (end - it);
+            s.kb1 = k1 < p.num_kb ? static_cast<int>(k1) : p.num_kb;
+            s.slot = it == it0 ? 0 : 1;
+            it += s.kb1 - s.kb0;
+            t = p.sk_first + tl;
+            s.partial = s.kb0 != 0 || s.kb1 != p.num_kb;
+            s.sk_t = tl;
+        }
         int tx, ty;
-        decode_tile(p, tile, s.b, tx, ty);
+        decode_tile(p, t, s.b, tx, ty);
         s.x0 = tx * 2 * BM + rank * BM;
         s.xend = s.x0 + BM < p.rows_x ? s.x0 + BM : p.rows_x;
         s.y0 = ty * PBN;
-        s.kb0 = 0;
-        s.kb1 = p.num_kb;
-        s.partial = false;
-        tile += step;
         return true;
     }
 };
+
+// Workspace slice of one epilogue warp's portion of a stream-K piece (pair q,
+// slot, CTA rank, warp ew): 4 chunks of 32 columns x 32 rows, column-major in
+// each chunk, so that lane l's value of column k sits at k*32 + l and every
+// store or load of one column is a single 128-byte line.
+__device__ __forceinline__ float* sk_portion(const TcParams& p, int q, int slot, int rank, int ew)
+{
+    return p.ws + ((((static_cast<size_t>(q) * 2 + slot) * 2 + rank) * 8 + ew) * 4) * (32 * 32);
+}
+
+// Workspace slot of pair q's piece of stream-K tile t: 0 if t is the first tile
+// of q's k range, else 1 (only the first and the last piece of a range can be
+// partial).
+__device__ __forceinline__ int sk_slot(const TcParams& p, int t, int q)
+{
+    const int first_tile = static_cast<int>((p.sk_iters * q / p.sk_pairs) / p.num_kb);
+    return t == first_tile ? 0 : 1;
+}
+
+// Stream-K piece of one epilogue warp (its TMEM quadrant q, columns
+// [c_begin, c_end)): store the slice to the workspace, release TMEM, count the
+// arrival, and if this warp's portion of the tile is now complete in every
+// piece, sum the pieces in k order and store Out.  Nothing here waits on other
+// CTAs, so no co-residency is assumed; the sum order, and with it every bit of
+// Out, does not depend on which piece arrives last.
+__device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uint32_t tacc, int q, int ew,
+                                            int c_begin, int c_end, int lane, int rank, float* stage_buf,
+                                            uint32_t tempty_leader)
+{
+    const int S = p.sk_pairs;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const uint32_t tbase = tacc + (static_cast<uint32_t>(q * 32) << 16);
+    float* mine = sk_portion(p, pair, s.slot, rank, ew) + lane;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        uint32_t r[32];
+        tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
+        float* dst = mine + ((c - c_begin) >> 5) * (32 * 32);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            __stcg(dst + k * 32, __uint_as_float(r[k]));
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive_cluster(tempty_leader);  // TMEM is free for the next tile
+    __threadfence();
+    __syncwarp();
+    uint32_t* counter = p.ws_flags + (static_cast<size_t>(s.sk_t) * 2 + rank) * 8 + ew;
+    uint32_t old = 0;
+    if (lane == 0)
+        old = atomicAdd(counter, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    // the pairs whose ranges cover this tile: p_first .. p_last
+    const long long I = p.sk_iters;
+    const long long a = static_cast<long long>(s.sk_t) * p.num_kb, b = a + p.num_kb;
+    const int p_first = static_cast<int>(((a + 1) * S - 1) / I);
+    const int p_last = static_cast<int>((b * S - 1) / I);
+    const int n = p_last - p_first + 1;
+    if (static_cast<int>(old) != n - 1)
+        return;
+    __threadfence();
+    if (lane == 0)
+        *counter = 0;  // ready for the next launch
+    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    const int x_row0 = s.x0 + q * 32;
+    const int nx = s.xend - x_row0;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        if (nx <= 0 || s.y0 + c >= p.rows_y)
+            break;
+        const int chunk = (c - c_begin) >> 5;
+        // acc = ((slice_0 + slice_1) + slice_2) + ...: two slices per round trip
+        float acc[32];
+#pragma unroll 1
+        for (int j = 0; j < n; j += 2) {
+            const float* src0 = sk_portion(p, p_first + j, sk_slot(p, s.sk_t, p_first + j), rank, ew) +
+                                chunk * (32 * 32) + lane;
+            const bool two = j + 1 < n;
+            const float* src1 = two ? sk_portion(p, p_first + j + 1, sk_slot(p, s.sk_t, p_first + j + 1), rank, ew) +
+                                          chunk * (32 * 32) + lane
+                                    : src0;
+            float v0[32], v1[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                v0[k] = __ldcg(src0 + k * 32);
+                v1[k] = __ldcg(src1 + k * 32);
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float t = j == 0 ? v0[k] : acc[k] + v0[k];
+                acc[k] = two ? t + v1[k] : t;
+            }
+        }
+        store_rows_chunk(p, obase, x_row0, nx, s.y0 + c, acc, lane, stage_buf, false);
+    }
+}
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
@@ -237,12 +364,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc_fence_after();
-            epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, c_begin,
-                                  c_begin + PBN / 2, lane, stage_buf);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+            const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[buf]), 0);
+            if (s.partial) {
+                sk_epilogue(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, ew, c_begin, c_begin + PBN / 2,
+                            lane, static_cast<int>(rank), stage_buf, tempty_leader);
+            } else {
+                epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, c_begin,
+                                      c_begin + PBN / 2, lane, stage_buf);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(tempty_leader);
+            }
             ++local;
         }
     }

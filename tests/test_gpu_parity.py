@@ -175,3 +175,27 @@ def test_identity_and_permutation():
     for path in (P.TC05, P.TC05_PAIR, P.MMASYNC):
         assert np.array_equal(run_path(A, I, path), A.astype(np.float32))
         assert np.array_equal(run_path(A, Pm, path), A.astype(np.float32)[:, p])
+
+
+# Shapes that put the CTA-pair kernel in stream-K mode on a 152-SM GB300 (76
+# pairs): far fewer tiles than pairs and at least 96 k-blocks, with ragged M/N
+# and K tails and batches; (1024, 1024, 4096) stays on whole tiles.
+SK_SHAPES = [(512, 512, 8192, 0), (700, 900, 7000, 0), (300, 500, 6504, 3), (1024, 1024, 6144, 0),
+             (1024, 1024, 4096, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,batch", SK_SHAPES)
+def test_pair_stream_k(M, N, K, batch):
+    A, B = workloads.make_inputs(batch, M, N, K, "uniform", seed=M + N + K)
+    ref, absdot = oracle.gemm_nt(A, B)
+    assert_parity(run_path(A, B, P.TC05_PAIR), ref, absdot, what="pair stream-K %s" % ((M, N, K, batch),))
+
+
+def test_pair_stream_k_integer_exact_and_deterministic():
+    A, B = workloads.make_inputs(0, 512, 512, 8192, "int4", seed=4)
+    ref, absdot = oracle.gemm_nt(A, B)
+    out1 = run_path(A, B, P.TC05_PAIR)
+    assert_parity(out1, ref, absdot, exact=True, what="pair stream-K integers")
+    A, B = workloads.make_inputs(0, 512, 512, 8192, "normal", 1.0, seed=5)
+    o1, o2 = run_path(A, B, P.TC05_PAIR), run_path(A, B, P.TC05_PAIR)
+    assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32)), "stream-K sum order is not fixed"
