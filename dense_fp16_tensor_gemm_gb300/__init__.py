@@ -23,6 +23,7 @@ class Status(enum.IntEnum):
     CUDA = 4
     DEVICE_TIMEOUT = 5
     NOT_SUPPORTED = 6
+    SCRATCH_TOO_SMALL = 7
 
 
 class Path(enum.IntEnum):
@@ -46,6 +47,7 @@ _SIGNATURES = {
     "gemm_nt_f16_f32_batched": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [_vp]),
     "gemm_nt_f16_f32_batched_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int, _vp]),
     "gemm_nt_f16_f32_from_host": (ctypes.c_int, [_vp] * 6 + [_i64] * 4 + [_vp]),
+    "gemm_nt_f16_f32_batched_no_alloc": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [_vp]),
     "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
     "gemm_nt_check": (ctypes.c_int, [_vp]),
     "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -98,6 +100,14 @@ def gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strid
                                  strideO, path, stream=0):
     _check(load().gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
                                                strideB, strideO, int(path), stream))
+
+
+def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
+                                     strideO, stream=0):
+    """The batched product without any device allocation (fixed scratch array
+    inside the library; see include/gemm_nt.h)."""
+    _check(load().gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
+                                                   strideB, strideO, stream))
 
 
 def gemm_nt_f16_f32_from_host(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, batch, stream=0):

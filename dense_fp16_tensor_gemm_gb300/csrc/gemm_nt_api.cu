@@ -616,6 +616,83 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
 }
 
 }  // namespace
+
+// The CTA-pair kernel with the split planned as in run_tc05_pair, but its
+// scratch taken from memory the caller of this function owns (no allocation).
+int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
+                      float* slices, int slice_pairs, uint32_t* counters, int counter_tiles, cudaStream_t stream)
+{
+    const Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    gemm_status_t st = validate(q);
+    if (st != GEMM_OK)
+        return st;
+    if (q.M == 0 || q.N == 0 || q.batch == 0)
+        return GEMM_OK;
+    DeviceState* d = nullptr;
+    st = device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    if (q.K == 0)
+        return zero_out(q, stream);
+    if (!tma_ok(q) || d->max_pairs < 1)
+        return GEMM_ERR_NOT_SUPPORTED;
+    TcParams p{};
+    CUtensorMap tma, tmb;
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, 128, &p.y_bmul))
+        return GEMM_ERR_CUDA;
+    p.out = q.Out;
+    p.ldo = q.ldo;
+    p.stride_o = q.sO;
+    p.rows_x = static_cast<int>(q.M);
+    p.rows_y = static_cast<int>(q.N);
+    p.batch = static_cast<int>(q.batch);
+    p.tiles_x = static_cast<int>((q.M + 255) / 256);
+    p.tiles_y = static_cast<int>((q.N + 255) / 256);
+    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
+    const int64_t ntiles = tpb * q.batch;
+    if (ntiles > INT32_MAX)
+        return GEMM_ERR_NOT_SUPPORTED;
+    p.tiles_per_batch = static_cast<int>(tpb);
+    p.num_tiles = static_cast<int>(ntiles);
+    p.group_x = 8;
+    p.mode = kModeTiles;
+    p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
+    p.vec4 = (aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.status = d->status;
+    p.wait_limit = wait_limit();
+    p.fault = g_fault.load();
+    // same split rule as run_tc05_pair
+    constexpr int64_t kMaxPieces = 4;
+    constexpr int64_t kMinKBlocks = 96;
+    const int P = d->max_pairs;
+    const int64_t rem = ntiles < P / 2 ? ntiles : 0;
+    const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
+    int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
+    p.sk_first = p.num_tiles;
+    p.sk_iters = 0;
+    p.sk_pairs = 0;
+    if (rem != 0 && p.num_kb >= kMinKBlocks) {
+        if (sk_pairs > slice_pairs || rem > counter_tiles)
+            return GEMM_ERR_SCRATCH_TOO_SMALL;
+        // the counters must start at zero; the slices are fully rewritten
+        if (cudaMemsetAsync(counters, 0, static_cast<size_t>(rem) * 2 * 8 * sizeof(uint32_t), stream) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        p.sk_first = static_cast<int>(ntiles - rem);
+        p.sk_iters = rem * p.num_kb;
+        p.sk_pairs = static_cast<int>(sk_pairs);
+        p.ws = slices;
+        p.ws_flags = counters;
+        pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
+    }
+    if (tc05_pair_launch(tma, tmb, p, pairs, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
 }  // namespace gnt
 
 using gnt::Problem;
@@ -703,6 +780,8 @@ const char* gemm_nt_status_string(gemm_status_t status)
     case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
     case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
     case GEMM_ERR_NOT_SUPPORTED: return "the requested kernel cannot take these arguments";
+    case GEMM_ERR_SCRATCH_TOO_SMALL:
+        return "the call needs more scratch than the no-allocation entry point's fixed array holds";
     }
     return "unknown status";
 }

@@ -74,7 +74,7 @@ cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const Tc
 cudaError_t tc05_pair_configure(int* max_pairs);  // one-time per device
 // Workspace bytes the pair kernel's stream-K pieces need for `pairs` pairs.
 constexpr size_t kPairSliceBytes = 128 * 256 * 4;
-inline size_t pair_workspace_bytes(int pairs)
+constexpr size_t pair_workspace_bytes(int pairs)
 {
     return static_cast<size_t>(pairs) * 4 * kPairSliceBytes + static_cast<size_t>(pairs) * 2 * 8 * 4;
 }
@@ -84,5 +84,14 @@ cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, con
 cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream);
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
                          cudaStream_t stream);
+
+// The CTA-pair kernel on caller-independent scratch (no allocation): `slices`
+// holds the stream-K slices of up to `slice_pairs` pairs, `counters` the
+// counters of up to `counter_tiles` split tiles.  Plans the call exactly like
+// the automatic path would for the CTA-pair kernel; returns
+// GEMM_ERR_SCRATCH_TOO_SMALL if that plan needs more.
+int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
+                      float* slices, int slice_pairs, uint32_t* counters, int counter_tiles, cudaStream_t stream);
 
 }  // namespace gnt

@@ -54,7 +54,9 @@ typedef enum gemm_status {
     GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
     GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (launch, tensor map) */
     GEMM_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait ran out; Out is undefined */
-    GEMM_ERR_NOT_SUPPORTED = 6       /* the requested kernel cannot take these arguments */
+    GEMM_ERR_NOT_SUPPORTED = 6,      /* the requested kernel cannot take these arguments */
+    GEMM_ERR_SCRATCH_TOO_SMALL = 7   /* gemm_nt_f16_f32_batched_no_alloc: the call needs more
+                                        scratch than the library's fixed array holds */
 } gemm_status_t;
 
 /* Kernel choice.  GEMM_PATH_AUTO lets the library pick (see gemm_nt_select_path). */
@@ -122,6 +124,40 @@ gemm_status_t gemm_nt_f16_f32_from_host(const void *A_host, const void *B_host, 
                                         void *dA, void *dB, float *dOut,
                                         int64_t M, int64_t N, int64_t K, int64_t batch,
                                         gemm_stream_t stream);
+
+/*
+ * Same product as gemm_nt_f16_f32_batched, for callers that must not allocate
+ * device memory.  (The source pages have no counterpart to this entry point;
+ * it exists for users of this library.)  Code running inside CUDA stream
+ * capture may not call cudaMalloc, applications whose device memory is owned by
+ * their own pool allocator may forbid any other allocation, and latency-
+ * critical code cannot afford an allocation on its first call - yet the
+ * automatic path allocates a workspace (about 38 MB per stream, once) when it
+ * splits a problem with few output tiles and a long K across the GPU.
+ *
+ * This entry point always runs the CTA-pair tensor-core kernel (so A and B
+ * must meet the tensor-core alignment rule, else GEMM_ERR_NOT_SUPPORTED) and
+ * plans the split exactly as the automatic path does, but takes its scratch
+ * from one fixed array inside the library: 8 MiB for the partial results of
+ * up to 16 CTA pairs plus 4 KiB of counters for up to 64 split tiles.  Every
+ * GPU that loads the library holds that array until the process exits.  A call
+ * whose split would need more (a problem of 5 to about 37 tiles of 256 x 256
+ * with K >= 6144 on a 152-SM GB300) returns GEMM_ERR_SCRATCH_TOO_SMALL and
+ * launches nothing; problems that are not split use no scratch at all.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Before each split launch the counters are cleared on `stream`.  All calls
+ * share the one array: calls that may overlap on the GPU (different streams,
+ * or several host threads without ordering) race on it and give wrong results,
+ * so order them on one stream.
+ */
+gemm_status_t gemm_nt_f16_f32_batched_no_alloc(const void *A, const void *B, float *Out,
+                                               int64_t M, int64_t N, int64_t K,
+                                               int64_t lda, int64_t ldb, int64_t ldo,
+                                               int64_t batch, int64_t strideA, int64_t strideB,
+                                               int64_t strideO, gemm_stream_t stream);
 
 /*
  * The kernel GEMM_PATH_AUTO would choose for these arguments (host-only: reads

@@ -1,0 +1,73 @@
+"""gemm_nt_f16_f32_batched_no_alloc: the batched product with no device
+allocation, for callers that must not allocate (code being captured into a
+CUDA graph cannot call cudaMalloc; an application whose pool allocator owns the
+device memory may not allow a library to take more; a latency-critical first
+call cannot pay for one).  The entry point keeps its scratch in one fixed
+array inside the library, so its answers must match the ordinary entry point's
+call after call, and a split too large for that array must be refused, not
+attempted.
+
+Collected last on purpose (file name), so a failure here stops a -x run only
+after every other test has run.  It needs nothing from earlier tests and also
+passes alone in a fresh process.
+"""
+import numpy as np
+import pytest
+
+import dense_fp16_tensor_gemm_gb300 as gnt
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_fp16_tensor_gemm_gb300 import _build
+    _build.build()
+    return gnt.load()
+
+
+def _call(fn, a, b, out, batch, M, N, K):
+    import torch
+    return fn(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, K, K, N, batch, M * K, N * K, M * N,
+              torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("batch,M,N,K", [
+    (1, 512, 512, 8192),   # 4 tiles, long K: split across pairs, scratch in use
+    (1, 300, 500, 6144),   # ragged, 4 tiles, split
+    (2, 300, 500, 640),    # short K: whole tiles, no scratch needed
+])
+def test_matches_existing_entry_point_on_consecutive_calls(lib, batch, M, N, K):
+    import torch
+    A, B = workloads.make_inputs(batch, M, N, K, "normal", 1.0, seed=M + N + K)
+    _, absdot = oracle.gemm_nt(A, B)
+    a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    ref = torch.full((batch, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    assert _call(lib.gemm_nt_f16_f32_batched, a, b, ref, batch, M, N, K) == 0
+    gnt.gemm_nt_check()
+    ref = ref.cpu().numpy().astype(np.float64)
+    for call in range(2):  # the array keeps the previous call's contents
+        out = torch.full((batch, M, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call(lib.gemm_nt_f16_f32_batched_no_alloc, a, b, out, batch, M, N, K) == 0
+        gnt.gemm_nt_check()
+        got = out.cpu().numpy().astype(np.float64)
+        assert not np.isnan(got).any(), "call %d left elements unwritten" % call
+        bad = np.abs(got - ref) > 1e-3 * absdot + 1e-6
+        assert not bad.any(), "call %d: %d elements differ from the existing entry point" % (call, int(bad.sum()))
+
+
+def test_split_beyond_the_array_is_refused(lib):
+    """16 tiles with K = 8192 would split over 64 CTA pairs, more than the 16
+    the fixed array holds: the call returns SCRATCH_TOO_SMALL and writes nothing."""
+    import torch
+    M = N = 1024
+    K = 8192
+    a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    b = torch.zeros((N, K), dtype=torch.float16, device="cuda")
+    out = torch.full((1, M, N), 7.0, dtype=torch.float32, device="cuda")
+    assert _call(lib.gemm_nt_f16_f32_batched_no_alloc, a, b, out, 1, M, N, K) == gnt.Status.SCRATCH_TOO_SMALL
+    gnt.gemm_nt_check()
+    assert bool(torch.all(out == 7.0))
+    assert "scratch" in gnt.status_string(gnt.Status.SCRATCH_TOO_SMALL)
