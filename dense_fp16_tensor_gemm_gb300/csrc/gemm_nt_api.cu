@@ -402,16 +402,55 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     return GEMM_OK;
 }
 
-// CTA pairs: 256 x 256 tiles; each CTA loads its 128 rows of A and 128 of the
-// tile's 256 rows of B.
+// Tile width of the CTA-pair kernel: 256 columns, or 224 / 192 when that fits
+// the number of tiles better to a whole number of rounds over the pairs.  The
+// cost of a width is (rounds) x (width), the MMA work on the critical path,
+// with a mild surcharge for narrower tiles, which move more bytes per MMA cycle
+// (32 KB per 512 cycles at 256, 30 KB per 448 at 224, 28 KB per 384 at 192).
+int pair_tile_width(int64_t M, int64_t N, int64_t batch, int pairs)
+{
+    static const int widths[3] = {256, 224, 192};
+    static const double surcharge[3] = {1.0, 1.036, 1.084};
+    int best = 256;
+    double best_cost = 0;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = batch * ((M + 255) / 256) * ((N + widths[i] - 1) / widths[i]);
+        const int64_t rounds = (tiles + pairs - 1) / pairs;
+        const double cost = static_cast<double>(rounds) * widths[i] * surcharge[i];
+        if (i == 0 || cost < best_cost) {
+            best = widths[i];
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// The split (stream-K) rule of the pair kernel, shared by both of its hosts:
+// far fewer tiles than pairs and K long enough.
+bool pair_split(int64_t ntiles, int num_kb, int pairs)
+{
+    return ntiles < pairs / 2 && num_kb >= 96;
+}
+
+int pair_plan_width(const Problem& q, const DeviceState& d)
+{
+    const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
+    if (pair_split(tiles256, static_cast<int>((q.K + 63) / 64), d.max_pairs))
+        return 256;
+    return pair_tile_width(q.M, q.N, q.batch, d.max_pairs);
+}
+
+// CTA pairs: 256 x PBN tiles; each CTA loads its 128 rows of A and PBN/2 of
+// the tile's PBN rows of B.
 gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t stream)
 {
     if (d.max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
     TcParams p{};
+    const int pbn = pair_plan_width(q, d);
     CUtensorMap tma, tmb;
     if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, 128, &p.y_bmul))
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.ldo = q.ldo;
@@ -420,7 +459,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     p.rows_y = static_cast<int>(q.N);
     p.batch = static_cast<int>(q.batch);
     p.tiles_x = static_cast<int>((q.M + 255) / 256);
-    p.tiles_y = static_cast<int>((q.N + 255) / 256);
+    p.tiles_y = static_cast<int>((q.N + pbn - 1) / pbn);
     p.num_kb = static_cast<int>((q.K + 63) / 64);
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
     const int64_t ntiles = tpb * q.batch;
@@ -442,15 +481,14 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     // microseconds), so the last partial round of a large problem is left to
     // whole tiles.
     constexpr int64_t kMaxPieces = 4;
-    constexpr int64_t kMinKBlocks = 96;
     const int P = d.max_pairs;
-    const int64_t rem = ntiles < P / 2 ? ntiles : 0;
+    const int64_t rem = pair_split(ntiles, p.num_kb, P) ? ntiles : 0;
     const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
     int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
     p.sk_first = p.num_tiles;
     p.sk_iters = 0;
     p.sk_pairs = 0;
-    if (rem != 0 && p.num_kb >= kMinKBlocks) {
+    if (rem != 0) {
         void* ws = nullptr;
         gemm_status_t st = stream_workspace(stream, pair_workspace_bytes(P), &ws);
         if (st != GEMM_OK)
@@ -462,7 +500,9 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
         p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(P) * 4 * kPairSliceBytes);
         pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
     }
-    if (tc05_pair_launch(tma, tmb, p, pairs, stream) != cudaSuccess)
+    // Out rows 32-byte aligned: the epilogue stores without staging
+    const bool direct = p.sk_pairs == 0 && aligned(q.Out, 32) && q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -638,9 +678,10 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     if (!tma_ok(q) || d->max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
     TcParams p{};
+    const int pbn = pair_plan_width(q, *d);
     CUtensorMap tma, tmb;
     if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, 128, &p.y_bmul))
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.ldo = q.ldo;
@@ -649,7 +690,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     p.rows_y = static_cast<int>(q.N);
     p.batch = static_cast<int>(q.batch);
     p.tiles_x = static_cast<int>((q.M + 255) / 256);
-    p.tiles_y = static_cast<int>((q.N + 255) / 256);
+    p.tiles_y = static_cast<int>((q.N + pbn - 1) / pbn);
     p.num_kb = static_cast<int>((q.K + 63) / 64);
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
     const int64_t ntiles = tpb * q.batch;
@@ -666,15 +707,14 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     p.fault = g_fault.load();
     // same split rule as run_tc05_pair
     constexpr int64_t kMaxPieces = 4;
-    constexpr int64_t kMinKBlocks = 96;
     const int P = d->max_pairs;
-    const int64_t rem = ntiles < P / 2 ? ntiles : 0;
+    const int64_t rem = pair_split(ntiles, p.num_kb, P) ? ntiles : 0;
     const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
     int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
     p.sk_first = p.num_tiles;
     p.sk_iters = 0;
     p.sk_pairs = 0;
-    if (rem != 0 && p.num_kb >= kMinKBlocks) {
+    if (rem != 0) {
         if (sk_pairs > slice_pairs || rem > counter_tiles)
             return GEMM_ERR_SCRATCH_TOO_SMALL;
         // the counters must start at zero; the slices are fully rewritten
@@ -688,7 +728,9 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
         p.ws_flags = counters;
         pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
     }
-    if (tc05_pair_launch(tma, tmb, p, pairs, stream) != cudaSuccess)
+    // Out rows 32-byte aligned: the epilogue stores without staging
+    const bool direct = p.sk_pairs == 0 && aligned(q.Out, 32) && q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }

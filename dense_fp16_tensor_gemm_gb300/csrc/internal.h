@@ -78,8 +78,11 @@ constexpr size_t pair_workspace_bytes(int pairs)
 {
     return static_cast<size_t>(pairs) * 4 * kPairSliceBytes + static_cast<size_t>(pairs) * 2 * 8 * 4;
 }
-cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
-                             cudaStream_t stream);
+// pbn: tile columns per pair, 256, 224 or 192 (B tensor maps use boxes of pbn/2
+// rows).  direct: epilogue without shared-memory staging and a 7-stage ring;
+// needs Out rows 32-byte aligned and no split (p.sk_pairs == 0).
+cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
+                             bool direct, cudaStream_t stream);
 
 cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream);
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,

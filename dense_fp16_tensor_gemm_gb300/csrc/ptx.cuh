@@ -139,6 +139,25 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
+// 16 lanes x 256 bits, repeated 4 times along the columns: with the lane field
+// of taddr selecting the first of 16 TMEM lanes and col the first of 32
+// columns, thread t of the warp receives, for j = 0..3,
+//   r[4j+0], r[4j+1] = lane t/4,     columns col + 8j + 2(t%4) + {0, 1}
+//   r[4j+2], r[4j+3] = lane t/4 + 8, columns col + 8j + 2(t%4) + {0, 1}
+// so the four threads of a quad hold 8 consecutive columns (32 bytes) of a row.
+__device__ __forceinline__ void tmem_ld16x256_x4_wait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
 // 128-byte swizzle: rows of 128 B (64 fp16 of K), 8-row groups 1024 B apart.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused

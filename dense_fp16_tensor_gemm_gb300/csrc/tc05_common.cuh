@@ -241,5 +241,49 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, 
     }
 }
 
+// Direct epilogue for Out rows whose starts are 32-byte aligned (ldo a
+// multiple of 8, base 32-byte aligned): no shared-memory staging.  TMEM is
+// read with the 16x256b shape, which hands each quad of lanes 8 consecutive
+// columns of one row, and each float2 store of a warp writes 8 whole 32-byte
+// sectors.  Same coverage and masking as epilogue_store.
+__device__ __forceinline__ void epilogue_store_direct(const TcParams& p, const Seg& s, uint32_t tacc, int q,
+                                                      int c_begin, int c_end, int lane)
+{
+    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    const int x_row0 = s.x0 + q * 32;
+    const int nx = s.xend - x_row0;
+    const int rsub = lane >> 2;
+    const int csub = 2 * (lane & 3);
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        if (nx <= 0 || s.y0 + c >= p.rows_y)
+            break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h * 16 >= nx)
+                break;
+            uint32_t r[16];
+            tmem_ld16x256_x4_wait(tacc + (static_cast<uint32_t>(q * 32 + h * 16) << 16) + static_cast<uint32_t>(c), r);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int row = h * 16 + half * 8 + rsub;  // within the quadrant
+                if (row < nx) {
+                    float* dst = obase + static_cast<int64_t>(x_row0 + row) * p.ldo + s.y0 + c + csub;
+                    const int ncol = p.rows_y - (s.y0 + c + csub);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float v0 = __uint_as_float(r[4 * j + 2 * half]);
+                        const float v1 = __uint_as_float(r[4 * j + 2 * half + 1]);
+                        if (ncol - 8 * j >= 2)
+                            __stcs(reinterpret_cast<float2*>(dst + 8 * j), make_float2(v0, v1));
+                        else if (ncol - 8 * j == 1)
+                            __stcs(dst + 8 * j, v0);
+                    }
+                }
+            }
+        }
+    }
+}
+
 }  // namespace tc
 }  // namespace gnt

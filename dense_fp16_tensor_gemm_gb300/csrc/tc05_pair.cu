@@ -18,6 +18,8 @@
 //   tfull[b]   in each CTA: the leader's commit after a tile's last MMA
 //   tempty[b]  in the leader: one arrival per epilogue warp of both CTAs
 // Every wait is bounded as in the single-CTA kernel.
+#include <algorithm>
+
 #include "tc05_common.cuh"
 
 namespace gnt {
@@ -27,24 +29,38 @@ namespace {
 using namespace tc;
 
 constexpr int kPairThreads = 320;
-constexpr int PBN = 256;                       // tile columns (B rows) per pair
-constexpr int kStages = 6;
 constexpr int A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A
-constexpr int B_BYTES = (PBN / 2) * BK * 2;    // this CTA's half of B
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_BYTES = 8 * 32 * 32 * 4;
-constexpr int TMEM_COLS = 2 * PBN;
+constexpr int TMEM_COLS = 512;                 // two accumulators, 256 columns apart
+constexpr int kAccStride = 256;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM = 1024 + kStages * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-constexpr uint32_t IDESC = idesc_f16_f32(2 * BM, PBN);
 constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CTAs
-static_assert(SMEM <= 232448, "shared memory budget");
-static_assert((2 * kStages + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 
-// Pair tiles (256 rows x 256 columns): tiles [0, sk_first) whole and round-robin
+// PBN: tile columns (rows of B) per pair; each CTA stages PBN/2 rows of B.
+// Narrower tiles than 256 let the host fit the number of tiles to a whole
+// number of rounds over the pairs.  DIRECT: the epilogue stores straight from
+// TMEM-loaded registers (Out rows 32-byte aligned), which frees the 32 KB of
+// staging for a seventh pipeline stage.
+template <int PBN, bool DIRECT>
+struct PairCfg {
+    static constexpr int STAGES = DIRECT ? 7 : 6;
+    static constexpr int B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_BYTES = DIRECT ? 0 : 8 * 32 * 32 * 4;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(2 * BM, PBN);
+    // epilogue warps 2-5 store columns [0, SPLIT), warps 6-9 [SPLIT, PBN)
+    static constexpr int SPLIT = ((PBN / 32 + 1) / 2) * 32;
+    static_assert(PBN % 32 == 0 && PBN <= 256 && PBN >= 128, "tile width");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(B_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
+};
+
+// Pair tiles (256 rows x PBN columns): tiles [0, sk_first) whole and round-robin
 // over the pairs; then, for stream-K, pair q < S takes the k-block iterations
 // [I*q/S, I*(q+1)/S) of the remaining tiles (I = sk_iters, S = sk_pairs), cut
 // at tile borders.
+template <int PBN>
 struct PairIter {
     int tile, step, rank, pair;
     long long it, it0, end;
@@ -196,10 +212,16 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
     }
 }
 
+template <int PBN, bool DIRECT>
 __global__ void __launch_bounds__(kPairThreads, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const TcParams p)
 {
+    using C = PairCfg<PBN, DIRECT>;
+    constexpr int kStages = C::STAGES;
+    constexpr int B_BYTES = C::B_BYTES;
+    constexpr int STAGE_BYTES = C::STAGE_BYTES;
+    constexpr int EPI_BYTES = C::EPI_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* as = smem;
@@ -252,7 +274,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
             bool first = true, ok = true;
-            PairIter w(p, static_cast<int>(rank));
+            PairIter<PBN> w(p, static_cast<int>(rank));
             Seg s;
             while (ok && w.next(s)) {
                 const int yb = s.y0 + static_cast<int>(rank) * (PBN / 2);
@@ -302,7 +324,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             uint32_t phase = 0;
             int local = 0;
             bool first = true, ok = true;
-            PairIter w(p, 0);
+            PairIter<PBN> w(p, 0);
             Seg s;
             while (ok && w.next(s)) {
                 const int buf = local & 1;
@@ -312,7 +334,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * PBN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccStride);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
@@ -324,7 +346,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     const uint32_t ba = smem_u32(bs + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), IDESC,
+                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), C::IDESC,
                                         (kb > s.kb0 || k > 0) ? 1u : 0u);
                     }
                     const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
@@ -351,10 +373,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int ew = warp - 2;
         const int q = warp & 3;
-        const int c_begin = (ew >> 2) * (PBN / 2);
+        const int c_begin = (ew >> 2) ? C::SPLIT : 0;
+        const int c_end = (ew >> 2) ? PBN : C::SPLIT;
         float* stage_buf = epi + ew * 32 * 32;
         int local = 0;
-        PairIter w(p, static_cast<int>(rank));
+        PairIter<PBN> w(p, static_cast<int>(rank));
         Seg s;
         while (w.next(s)) {
             const int buf = local & 1;
@@ -365,12 +388,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             tc_fence_after();
             const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[buf]), 0);
-            if (s.partial) {
-                sk_epilogue(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, ew, c_begin, c_begin + PBN / 2,
-                            lane, static_cast<int>(rank), stage_buf, tempty_leader);
+            if (!DIRECT && s.partial) {
+                sk_epilogue(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, ew, c_begin, c_end, lane,
+                            static_cast<int>(rank), stage_buf, tempty_leader);
             } else {
-                epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * PBN), q, c_begin,
-                                      c_begin + PBN / 2, lane, stage_buf);
+                if (DIRECT)
+                    epilogue_store_direct(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, c_begin, c_end,
+                                          lane);
+                else
+                    epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, c_begin,
+                                          c_end, lane, stage_buf);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -389,12 +416,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
-cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr)
+cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaunchAttribute* attr)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kPairThreads, 1, 1);
-    cfg.dynamicSmemBytes = SMEM;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -407,29 +434,67 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     return cfg;
 }
 
+template <int PBN, bool DIRECT>
+cudaError_t configure_one(int* max_pairs)
+{
+    using C = PairCfg<PBN, DIRECT>;
+    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel<PBN, DIRECT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT>, &cfg);
+    if (e != cudaSuccess)
+        return e;
+    *max_pairs = std::min(*max_pairs, n);
+    return cudaSuccess;
+}
+
+template <int PBN, bool DIRECT>
+cudaError_t launch_one(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
+                       cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT>::SMEM, stream, attr);
+    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT>, tma, tmb, p);
+}
+
 }  // namespace
 
 cudaError_t tc05_pair_configure(int* max_pairs)
 {
-    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess)
-        return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel, &cfg);
+    int n = 1 << 30;
+    cudaError_t e = configure_one<256, false>(&n);
+    if (e == cudaSuccess) e = configure_one<224, false>(&n);
+    if (e == cudaSuccess) e = configure_one<192, false>(&n);
+    if (e == cudaSuccess) e = configure_one<256, true>(&n);
+    if (e == cudaSuccess) e = configure_one<224, true>(&n);
+    if (e == cudaSuccess) e = configure_one<192, true>(&n);
     if (e != cudaSuccess)
         return e;
     *max_pairs = n;
     return cudaSuccess;
 }
 
-cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
-                             cudaStream_t stream)
+cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
+                             bool direct, cudaStream_t stream)
 {
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2 * pairs, stream, attr);
-    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel, tma, tmb, p);
+    if (direct) {
+        switch (pbn) {
+        case 256: return launch_one<256, true>(tma, tmb, p, pairs, stream);
+        case 224: return launch_one<224, true>(tma, tmb, p, pairs, stream);
+        case 192: return launch_one<192, true>(tma, tmb, p, pairs, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (pbn) {
+    case 256: return launch_one<256, false>(tma, tmb, p, pairs, stream);
+    case 224: return launch_one<224, false>(tma, tmb, p, pairs, stream);
+    case 192: return launch_one<192, false>(tma, tmb, p, pairs, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gnt
