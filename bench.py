@@ -44,7 +44,12 @@ L2_BYTES = 129 * 1024 * 1024
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
-TRAFFIC = {"square_8192": (1337426784, "29e4f27e77b46a43")}
+TRAFFIC = {
+    "square_8192": (1308568688, "85ea9d2d90bbb862"),
+    "square_4096": (126687744, "85ea9d2d90bbb862"),
+    "ragged_batch16_3001x2047x1000": (512107264, "85ea9d2d90bbb862"),
+    "skinny_64x16384x8192": (273558016, "6100f28e7a6a69e2"),
+}
 
 
 KERNEL_SOURCES = {

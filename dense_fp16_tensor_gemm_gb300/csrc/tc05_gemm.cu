@@ -104,7 +104,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     // Everything above touched only this CTA's shared memory and TMEM; global
     // memory is read and written only after the preceding grids are done.
+    // Meanwhile the producer warms L2 with the first ring's worth of tiles.
     pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        WorkIter<BN> w0(p);
+        Seg s0;
+        if (w0.next(s0)) {
+            const int n = s0.kb1 - s0.kb0 < STAGES ? s0.kb1 - s0.kb0 : STAGES;
+            for (int i = 0; i < n; ++i) {
+                tma_prefetch_l2_3d(&tmx, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
+                tma_prefetch_l2_3d(&tmy, (s0.kb0 + i) * BK, s0.y0, s0.b * p.y_bmul);
+            }
+        }
+    }
     pdl_wait();
 
     if (warp == 0) {

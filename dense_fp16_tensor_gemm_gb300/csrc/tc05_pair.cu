@@ -265,6 +265,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        // warm L2 with this CTA's first ring of tiles while earlier grids finish
+        PairIter<PBN> w0(p, static_cast<int>(rank));
+        Seg s0;
+        if (w0.next(s0)) {
+            const int n = s0.kb1 - s0.kb0 < kStages ? s0.kb1 - s0.kb0 : kStages;
+            const int yb = s0.y0 + static_cast<int>(rank) * (PBN / 2);
+            for (int i = 0; i < n; ++i) {
+                tma_prefetch_l2_3d(&tma, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
+                tma_prefetch_l2_3d(&tmb, (s0.kb0 + i) * BK, yb, s0.b * p.y_bmul);
+            }
+        }
+    }
     pdl_wait();  // global memory only after the preceding grids are done
 
     if (warp == 0) {
