@@ -26,6 +26,12 @@ class Status(enum.IntEnum):
     SCRATCH_TOO_SMALL = 7
 
 
+class DType(enum.IntEnum):
+    F16 = 0
+    BF16 = 1
+    F32 = 2
+
+
 class Path(enum.IntEnum):
     AUTO = 0
     TC05 = 1
@@ -48,6 +54,8 @@ _SIGNATURES = {
     "gemm_nt_f16_f32_batched_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int, _vp]),
     "gemm_nt_f16_f32_from_host": (ctypes.c_int, [_vp] * 6 + [_i64] * 4 + [_vp]),
     "gemm_nt_f16_f32_batched_no_alloc": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [_vp]),
+    "gemm_nt_batched_ex": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int] + [_i64] * 10
+                           + [ctypes.c_int, _vp]),
     "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
     "gemm_nt_check": (ctypes.c_int, [_vp]),
     "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -102,6 +110,12 @@ def gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strid
                                                strideB, strideO, int(path), stream))
 
 
+def gemm_nt_batched_ex(A, B, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
+                       strideO, path=0, stream=0):
+    _check(load().gemm_nt_batched_ex(A, B, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo,
+                                     batch, strideA, strideB, strideO, int(path), stream))
+
+
 def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
                                      strideO, stream=0):
     """The batched product without any device allocation (fixed scratch array
@@ -150,46 +164,57 @@ def _matrix_ld(t, name):
     return t.stride(-2) if t.shape[-2] > 1 else max(t.shape[-1], 1)
 
 
-def gemm_nt(A, B, out=None, path=Path.AUTO, stream=None):
-    """Out = A @ B.T for torch CUDA tensors A (M,K) fp16, B (N,K) fp16.
+def _dtypes(A, B, out, out_dtype):
+    import torch
+    codes = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.float32: DType.F32}
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must both be float16 or both bfloat16")
+    dt = out.dtype if out is not None else (out_dtype or torch.float32)
+    if dt not in codes:
+        raise TypeError("out must be float32, float16 or bfloat16")
+    return codes[A.dtype], codes[dt], dt
+
+
+def gemm_nt(A, B, out=None, path=Path.AUTO, stream=None, out_dtype=None):
+    """Out = A @ B.T for torch CUDA tensors A (M,K), B (N,K), both fp16 or both
+    bf16, accumulated in fp32.
 
     Row strides may exceed the row length; the last dimension must be
-    contiguous.  ``out`` (M,N) fp32 is allocated if not given.  Runs on
+    contiguous.  ``out`` (M,N) is allocated if not given, as ``out_dtype``
+    (default float32; float16 or bfloat16 round to nearest even).  Runs on
     ``stream`` (default: torch's current stream).
     """
     import torch
-    if A.dtype != torch.float16 or B.dtype != torch.float16:
-        raise TypeError("A and B must be float16")
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
         raise ValueError("shapes: A (M,K), B (N,K)")
+    ab, ot, dt = _dtypes(A, B, out, out_dtype)
     M, K = A.shape
     N = B.shape[0]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    if out.dtype != torch.float32 or tuple(out.shape) != (M, N):
-        raise ValueError("out must be float32 of shape (M,N)")
-    gemm_nt_f16_f32_batched_path(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                                 _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
-                                 1, 0, 0, 0, path, _stream_handle(stream))
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must have shape (M,N)")
+    gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
+                       _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
+                       1, 0, 0, 0, path, _stream_handle(stream))
     return out
 
 
-def gemm_nt_batched(A, B, out=None, path=Path.AUTO, stream=None):
-    """Out[b] = A[b] @ B[b].T for torch CUDA tensors A (batch,M,K), B (batch,N,K)
-    fp16 (a batch stride of 0, e.g. from ``expand``, shares the operand)."""
+def gemm_nt_batched(A, B, out=None, path=Path.AUTO, stream=None, out_dtype=None):
+    """Out[b] = A[b] @ B[b].T for torch CUDA tensors A (batch,M,K), B (batch,N,K),
+    both fp16 or both bf16 (a batch stride of 0, e.g. from ``expand``, shares
+    the operand); ``out``/``out_dtype`` as in :func:`gemm_nt`."""
     import torch
-    if A.dtype != torch.float16 or B.dtype != torch.float16:
-        raise TypeError("A and B must be float16")
     if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0] or A.shape[2] != B.shape[2]:
         raise ValueError("shapes: A (batch,M,K), B (batch,N,K)")
+    ab, ot, dt = _dtypes(A, B, out, out_dtype)
     batch, M, K = A.shape
     N = B.shape[1]
     if out is None:
-        out = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
-    if out.dtype != torch.float32 or tuple(out.shape) != (batch, M, N):
-        raise ValueError("out must be float32 of shape (batch,M,N)")
-    gemm_nt_f16_f32_batched_path(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                                 _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
-                                 batch, A.stride(0), B.stride(0), out.stride(0), path,
-                                 _stream_handle(stream))
+        out = torch.empty((batch, M, N), dtype=dt, device=A.device)
+    if tuple(out.shape) != (batch, M, N):
+        raise ValueError("out must have shape (batch,M,N)")
+    gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
+                       _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
+                       batch, A.stride(0), B.stride(0), out.stride(0), path, _stream_handle(stream))
     return out

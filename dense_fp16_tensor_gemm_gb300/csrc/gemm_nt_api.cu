@@ -156,8 +156,14 @@ void reset_workspaces()
 struct Problem {
     const void* A;
     const void* B;
-    float* Out;
+    void* Out;
     int64_t M, N, K, lda, ldb, ldo, batch, sA, sB, sO;
+    int ab_type = GEMM_DTYPE_F16;   // element type of A and B
+    int out_type = GEMM_DTYPE_F32;  // element type of Out
+
+    int64_t out_esize() const { return out_type == GEMM_DTYPE_F32 ? 4 : 2; }
+    int kernel_out() const { return out_type == GEMM_DTYPE_F16 ? kOutF16 : (out_type == GEMM_DTYPE_BF16 ? kOutBF16 : kOutF32); }
+    uint32_t ab_fmt() const { return ab_type == GEMM_DTYPE_BF16 ? ((1u << 7) | (1u << 10)) : 0u; }
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -193,13 +199,17 @@ gemm_status_t validate(const Problem& q)
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.M)) * 2.0 > lim ||
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.N)) * 2.0 > lim)
         return GEMM_ERR_INVALID_VALUE;
-    if (!aligned(q.Out, 4) || (q.K > 0 && (!aligned(q.A, 2) || !aligned(q.B, 2))))
+    if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.out_type != GEMM_DTYPE_F32 && q.out_type != GEMM_DTYPE_F16 && q.out_type != GEMM_DTYPE_BF16)
+        return GEMM_ERR_INVALID_VALUE;
+    if (!aligned(q.Out, static_cast<uintptr_t>(q.out_esize())) || (q.K > 0 && (!aligned(q.A, 2) || !aligned(q.B, 2))))
         return GEMM_ERR_INVALID_VALUE;
     if (q.batch > 1 && q.sO < (q.M - 1) * q.ldo + q.N)
         return GEMM_ERR_OVERLAP;
     if (q.K > 0) {
         uintptr_t olo, ohi, alo, ahi, blo, bhi;
-        span(q.Out, 4, q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
+        span(q.Out, q.out_esize(), q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
         span(q.A, 2, q.batch, q.sA, q.M, q.lda, q.K, alo, ahi);
         span(q.B, 2, q.batch, q.sB, q.N, q.ldb, q.K, blo, bhi);
         if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
@@ -245,10 +255,11 @@ struct MapKey {
     const void* base;
     int64_t rows, K, ld, batch, stride;
     int box_rows;
+    bool bf16;
     bool operator==(const MapKey& o) const
     {
         return base == o.base && rows == o.rows && K == o.K && ld == o.ld && batch == o.batch &&
-               stride == o.stride && box_rows == o.box_rows;
+               stride == o.stride && box_rows == o.box_rows && bf16 == o.bf16;
     }
 };
 
@@ -263,7 +274,7 @@ struct MapCache {
 thread_local MapCache t_maps;
 
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-                int64_t stride, int box_rows, int* bmul)
+                int64_t stride, int box_rows, int* bmul, bool bf16)
 {
     auto enc = encode_fn();
     if (!enc)
@@ -276,16 +287,16 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     *bmul = batched ? 1 : 0;
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-              int64_t stride, int box_rows, int* bmul)
+              int64_t stride, int box_rows, int* bmul, bool bf16 = false)
 {
-    const MapKey k{base, rows, K, ld, batch, stride, box_rows};
+    const MapKey k{base, rows, K, ld, batch, stride, box_rows, bf16};
     MapCache& c = t_maps;
     for (int i = 0; i < c.count; ++i) {
         if (c.key[i] == k) {
@@ -294,7 +305,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64
             return true;
         }
     }
-    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul))
+    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul, bf16))
         return false;
     const int slot = c.next;
     c.key[slot] = k;
@@ -310,12 +321,13 @@ gemm_status_t zero_out(const Problem& q, cudaStream_t stream)
 {
     if (q.sO == q.M * q.ldo || q.batch == 1) {
         const int64_t rows = q.batch == 1 ? q.M : q.M * q.batch;
-        if (cudaMemset2DAsync(q.Out, q.ldo * 4, 0, q.N * 4, rows, stream) != cudaSuccess)
+        if (cudaMemset2DAsync(q.Out, q.ldo * q.out_esize(), 0, q.N * q.out_esize(), rows, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         return GEMM_OK;
     }
     for (int64_t b = 0; b < q.batch; ++b)
-        if (cudaMemset2DAsync(q.Out + b * q.sO, q.ldo * 4, 0, q.N * 4, q.M, stream) != cudaSuccess)
+        if (cudaMemset2DAsync(static_cast<uint8_t*>(q.Out) + b * q.sO * q.out_esize(), q.ldo * q.out_esize(), 0,
+                              q.N * q.out_esize(), q.M, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -355,10 +367,12 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     }
     p.x_box_bytes = xbox * 128;
     CUtensorMap tmx, tmy;
-    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul) ||
-        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul))
+    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
+        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
+    p.out_type = q.kernel_out();
+    p.ab_fmt = q.ab_fmt();
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(xrows);
@@ -375,7 +389,10 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     p.num_tiles = static_cast<int>(ntiles);
     p.group_x = 16;
     p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
-    p.vec4 = (!swap && aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.vec4 = (!swap && aligned(q.Out, static_cast<uintptr_t>(4 * q.out_esize())) && q.ldo % 4 == 0 &&
+              (q.batch == 1 || q.sO % 4 == 0))
+                 ? 1
+                 : 0;
     p.status = d.status;
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
@@ -384,7 +401,8 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         // no partial sums, nothing to zero
         p.mode = kModeRowSplit;
         grid = d.num_sms;
-    } else if (swap && ntiles < d.num_sms && p.total_iters >= 2 * static_cast<long long>(d.num_sms)) {
+    } else if (swap && q.out_type == GEMM_DTYPE_F32 && ntiles < d.num_sms &&
+               p.total_iters >= 2 * static_cast<long long>(d.num_sms)) {
         // Stream-K when there are too few tiles to fill the GPU: each CTA takes
         // an even share of the (tile, k-block) iterations; tiles cut between
         // CTAs are summed with atomics into a zeroed Out.
@@ -427,15 +445,15 @@ int pair_tile_width(int64_t M, int64_t N, int64_t batch, int pairs)
 
 // The split (stream-K) rule of the pair kernel, shared by both of its hosts:
 // far fewer tiles than pairs and K long enough.
-bool pair_split(int64_t ntiles, int num_kb, int pairs)
+bool pair_split(int64_t ntiles, int num_kb, int pairs, int out_type)
 {
-    return ntiles < pairs / 2 && num_kb >= 96;
+    return out_type == GEMM_DTYPE_F32 && ntiles < pairs / 2 && num_kb >= 96;
 }
 
 int pair_plan_width(const Problem& q, const DeviceState& d)
 {
     const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
-    if (pair_split(tiles256, static_cast<int>((q.K + 63) / 64), d.max_pairs))
+    if (pair_split(tiles256, static_cast<int>((q.K + 63) / 64), d.max_pairs, q.out_type))
         return 256;
     return pair_tile_width(q.M, q.N, q.batch, d.max_pairs);
 }
@@ -449,10 +467,12 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     TcParams p{};
     const int pbn = pair_plan_width(q, d);
     CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul))
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
+    p.out_type = q.kernel_out();
+    p.ab_fmt = q.ab_fmt();
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(q.M);
@@ -470,7 +490,10 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     p.group_x = 8;
     p.mode = kModeTiles;
     p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
-    p.vec4 = (aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.vec4 = (aligned(q.Out, static_cast<uintptr_t>(4 * q.out_esize())) && q.ldo % 4 == 0 &&
+              (q.batch == 1 || q.sO % 4 == 0))
+                 ? 1
+                 : 0;
     p.status = d.status;
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
@@ -482,7 +505,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     // whole tiles.
     constexpr int64_t kMaxPieces = 4;
     const int P = d.max_pairs;
-    const int64_t rem = pair_split(ntiles, p.num_kb, P) ? ntiles : 0;
+    const int64_t rem = pair_split(ntiles, p.num_kb, P, q.out_type) ? ntiles : 0;
     const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
     int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
     p.sk_first = p.num_tiles;
@@ -501,7 +524,8 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
         pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
     }
     // Out rows 32-byte aligned: the epilogue stores without staging
-    const bool direct = p.sk_pairs == 0 && aligned(q.Out, 32) && q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
+    const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
+                        q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
     if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
@@ -515,6 +539,7 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     p.A = static_cast<const uint16_t*>(q.A);
     p.B = static_cast<const uint16_t*>(q.B);
     p.out = q.Out;
+    p.out_type = q.kernel_out();
     p.M = static_cast<int>(q.M);
     p.N = static_cast<int>(q.N);
     p.K = static_cast<int>(q.K);
@@ -527,7 +552,7 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     p.stride_o = q.sO;
     p.vec_a = aligned(q.A, 16) && q.lda % 8 == 0 && (q.batch == 1 || q.sA % 8 == 0);
     p.vec_b = aligned(q.B, 16) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
-    return mmasync_launch(p, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return mmasync_launch(p, q.ab_type == GEMM_DTYPE_BF16, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 constexpr int kPipeChunks = 4;
@@ -680,10 +705,12 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     TcParams p{};
     const int pbn = pair_plan_width(q, *d);
     CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul))
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
+    p.out_type = q.kernel_out();
+    p.ab_fmt = q.ab_fmt();
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(q.M);
@@ -701,14 +728,17 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     p.group_x = 8;
     p.mode = kModeTiles;
     p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
-    p.vec4 = (aligned(q.Out, 16) && q.ldo % 4 == 0 && (q.batch == 1 || q.sO % 4 == 0)) ? 1 : 0;
+    p.vec4 = (aligned(q.Out, static_cast<uintptr_t>(4 * q.out_esize())) && q.ldo % 4 == 0 &&
+              (q.batch == 1 || q.sO % 4 == 0))
+                 ? 1
+                 : 0;
     p.status = d->status;
     p.wait_limit = wait_limit();
     p.fault = g_fault.load();
     // same split rule as run_tc05_pair
     constexpr int64_t kMaxPieces = 4;
     const int P = d->max_pairs;
-    const int64_t rem = pair_split(ntiles, p.num_kb, P) ? ntiles : 0;
+    const int64_t rem = pair_split(ntiles, p.num_kb, P, q.out_type) ? ntiles : 0;
     const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
     int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
     p.sk_first = p.num_tiles;
@@ -729,7 +759,8 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
         pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
     }
     // Out rows 32-byte aligned: the epilogue stores without staging
-    const bool direct = p.sk_pairs == 0 && aligned(q.Out, 32) && q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
+    const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
+                        q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
     if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
@@ -762,6 +793,17 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void* A, const void* B, float* 
                                            gemm_stream_t stream)
 {
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_batched_ex(const void* A, const void* B, void* Out, gemm_dtype_t ab_type, gemm_dtype_t out_type,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch,
+                                 int64_t strideA, int64_t strideB, int64_t strideO, gemm_path_t path,
+                                 gemm_stream_t stream)
+{
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    q.ab_type = static_cast<int>(ab_type);
+    q.out_type = static_cast<int>(out_type);
     return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "out_store.cuh"
+
 namespace gnt {
 
 // Work distribution of the tcgen05 kernel.
@@ -20,7 +22,9 @@ constexpr uint32_t kStatusTimeout = 1u;
 // Without swapping X = A and Y = B and Out[x][y]; with swapping (small M)
 // X = B, Y = A and the tile is written transposed, Out[y][x].
 struct TcParams {
-    float* out;
+    void* out;            // fp32, fp16 or bf16 elements (out_type)
+    int out_type;         // kOutF32, kOutF16 or kOutBF16
+    uint32_t ab_fmt;      // instruction-descriptor bits of the A/B element type (0: fp16)
     int64_t ldo;
     int64_t stride_o;
     int rows_x;
@@ -36,7 +40,7 @@ struct TcParams {
     long long total_iters;  // num_tiles * num_kb
     int x_bmul;           // 1 if X's tensor map has a batch dimension, 0 if shared
     int y_bmul;
-    int vec4;             // Out base and ldo allow 16-byte stores
+    int vec4;             // Out base and ldo allow 4-element vector stores
     int x_box_bytes;      // bytes of one X box (its height x 128 B; at most 16 KB)
     // Stream-K on the pair kernel: tiles [sk_first, num_tiles) are cut into
     // even k-block ranges, one per pair.  Each partial piece leaves its slice in
@@ -55,7 +59,8 @@ struct TcParams {
 struct MmaParams {
     const uint16_t* A;
     const uint16_t* B;
-    float* out;
+    void* out;
+    int out_type;
     int M, N, K, batch;
     int64_t lda, ldb, ldo;
     int64_t stride_a, stride_b, stride_o;
@@ -84,7 +89,7 @@ constexpr size_t pair_workspace_bytes(int pairs)
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
                              bool direct, cudaStream_t stream);
 
-cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream);
+cudaError_t mmasync_launch(const MmaParams& p, bool bf16, cudaStream_t stream);
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
                          cudaStream_t stream);
 

@@ -78,6 +78,27 @@ __device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, 
     }
 }
 
+// Out rows [row0, ...) of one 64x64 CTA tile through the D-fragment map.
+template <int OT>
+__device__ __forceinline__ void store_tile(const MmaParams& p, int b, int m0, int n0, int wm, int wn, int lane,
+                                           const float (&acc)[2][4][4])
+{
+    using S = OutStore<OT>;
+    typename S::T* Ob = static_cast<typename S::T*>(p.out) + static_cast<int64_t>(b) * p.stride_o;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = m0 + wm * 32 + mi * 16 + (lane >> 2) + 8 * (r >> 1);
+                const int col = n0 + wn * 32 + nb * 8 + 2 * (lane & 3) + (r & 1);
+                if (row < p.M && col < p.N)
+                    S::st1(Ob + static_cast<int64_t>(row) * p.ldo + col, acc[mi][nb][r]);
+            }
+}
+
+template <bool BF16>
 __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams p)
 {
     __shared__ __align__(16) uint16_t As[MBM * MPITCH];
@@ -127,22 +148,19 @@ __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams 
                 for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
                     for (int nb = 0; nb < 4; ++nb)
-                        mma_m16n8k16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
+                        if (BF16)
+                            mma_m16n8k16_bf16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
+                        else
+                            mma_m16n8k16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
             }
         }
 
-        float* Ob = p.out + static_cast<int64_t>(b) * p.stride_o;
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int nb = 0; nb < 4; ++nb)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int row = m0 + wm * 32 + mi * 16 + (lane >> 2) + 8 * (r >> 1);
-                    const int col = n0 + wn * 32 + nb * 8 + 2 * (lane & 3) + (r & 1);
-                    if (row < p.M && col < p.N)
-                        Ob[static_cast<int64_t>(row) * p.ldo + col] = acc[mi][nb][r];
-                }
+        if (p.out_type == kOutF16)
+            store_tile<kOutF16>(p, b, m0, n0, wm, wn, lane, acc);
+        else if (p.out_type == kOutBF16)
+            store_tile<kOutBF16>(p, b, m0, n0, wm, wn, lane, acc);
+        else
+            store_tile<kOutF32>(p, b, m0, n0, wm, wn, lane, acc);
     }
 }
 
@@ -176,12 +194,15 @@ __global__ void __launch_bounds__(32) probe_kernel(const uint16_t* A, const uint
 
 }  // namespace
 
-cudaError_t mmasync_launch(const MmaParams& p, cudaStream_t stream)
+cudaError_t mmasync_launch(const MmaParams& p, bool bf16, cudaStream_t stream)
 {
     dim3 grid((p.N + MBN - 1) / MBN, (p.M + MBM - 1) / MBM, p.batch < 65535 ? p.batch : 65535);
     if (grid.y > 65535)
         return cudaErrorInvalidConfiguration;
-    mmasync_gemm_kernel<<<grid, MThreads, 0, stream>>>(p);
+    if (bf16)
+        mmasync_gemm_kernel<true><<<grid, MThreads, 0, stream>>>(p);
+    else
+        mmasync_gemm_kernel<false><<<grid, MThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -132,56 +132,60 @@ __device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* a
 
 
 // Stores one 32x32 chunk of the accumulator held row-per-thread (lane i has
-// row x_row0 + i, columns col0..col0+31 in r[]): transpose through shared
+// row x_row0 + i, columns col0..col0+31 in v[]): transpose through shared
 // memory (16-byte slots XOR-swizzled by row) so the global stores are
 // row-contiguous across the warp.  Rows beyond nx and columns beyond rows_y
-// are not stored; `atomic` adds into Out instead of storing.
-__device__ __forceinline__ void store_rows_chunk(const TcParams& p, float* obase, int x_row0, int nx, int col0,
-                                                 const float (&v)[32], int lane, float* stage_buf, bool atomic)
+// are not stored; `atomic` adds into (fp32) Out instead of storing.  obase
+// points at element 0 of this batch's Out.
+template <int OT>
+__device__ __forceinline__ void store_rows_chunk(const TcParams& p, typename OutStore<OT>::T* obase, int x_row0,
+                                                 int nx, int col0, const float (&v)[32], int lane, float* stage_buf,
+                                                 bool atomic)
 {
+    using S = OutStore<OT>;
     float4* sb4 = reinterpret_cast<float4*>(stage_buf);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         sb4[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     __syncwarp();
     if (p.vec4 && !atomic) {
-        // 8 lanes per 128-byte row segment, 4 rows per instruction
+        // 8 lanes per 32-column row segment, 4 rows per instruction
         const int ch = lane & 7, rsub = lane >> 3;
         const int ncol = p.rows_y - (col0 + ch * 4);
-        float* dst = obase + static_cast<int64_t>(x_row0 + rsub) * p.ldo + col0 + ch * 4;
+        typename S::T* dst = obase + static_cast<int64_t>(x_row0 + rsub) * p.ldo + col0 + ch * 4;
         const int64_t step = 4 * p.ldo;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int rr = i * 4 + rsub;
-            const float4 v = sb4[rr * 8 + (ch ^ (rr & 7))];
+            const float4 w = sb4[rr * 8 + (ch ^ (rr & 7))];
             if (rr < nx) {
                 if (ncol >= 4) {
-                    __stcs(reinterpret_cast<float4*>(dst), v);
+                    S::st4(dst, w);
                 } else {
-                    if (ncol > 0) __stcs(dst, v.x);
-                    if (ncol > 1) __stcs(dst + 1, v.y);
-                    if (ncol > 2) __stcs(dst + 2, v.z);
+                    if (ncol > 0) S::st1(dst, w.x);
+                    if (ncol > 1) S::st1(dst + 1, w.y);
+                    if (ncol > 2) S::st1(dst + 2, w.z);
                 }
             }
             dst += step;
         }
     } else if (col0 + lane < p.rows_y) {
-        // one 4-byte column per lane, 32 rows
-        float* dst = obase + static_cast<int64_t>(x_row0) * p.ldo + col0 + lane;
+        // one column per lane, 32 rows
+        typename S::T* dst = obase + static_cast<int64_t>(x_row0) * p.ldo + col0 + lane;
         const float* src = stage_buf + (lane & 3);
         const int g = lane >> 2;
         if (atomic) {
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
-                const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
-                if (rr < nx) atomicAdd(dst, v);
+                const float w = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                if (rr < nx) S::add1(dst, w);
                 dst += p.ldo;
             }
         } else {
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
-                const float v = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
-                if (rr < nx) __stcs(dst, v);
+                const float w = src[rr * 32 + ((g ^ (rr & 7)) << 2)];
+                if (rr < nx) S::st1(dst, w);
                 dst += p.ldo;
             }
         }
@@ -194,14 +198,15 @@ __device__ __forceinline__ void store_rows_chunk(const TcParams& p, float* obase
 // where `tacc` is the TMEM address of the accumulator's first column.
 // Rows >= s.xend and columns >= rows_y are not stored; `stage_buf` is this
 // warp's 32x32 fp32 staging area (unused when SWAP).  Partial segments (a
-// k range short of all of K) add into Out with atomics.
-template <bool SWAP>
+// k range short of all of K) add into (fp32) Out with atomics.
+template <bool SWAP, int OT>
 __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, uint32_t tacc, int q,
                                                int c_begin, int c_end, int lane, float* stage_buf)
 {
+    using S = OutStore<OT>;
     const bool partial = s.partial;
     const uint32_t tbase = tacc + (static_cast<uint32_t>(q * 32) << 16);
-    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    typename S::T* obase = static_cast<typename S::T*>(p.out) + static_cast<int64_t>(s.b) * p.stride_o;
     const int x_row0 = s.x0 + q * 32;
     const int nx = s.xend - x_row0;  // valid rows of this quadrant (may exceed 32)
     const int y0 = s.y0;
@@ -213,20 +218,20 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, 
         tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
         if (SWAP) {
             // Thread <-> x (consecutive Out columns): each j is one
-            // coalesced 128-byte row segment across the warp.
+            // coalesced row segment across the warp.
             const int ny = p.rows_y - (y0 + c);
             if (lane < nx) {
-                float* dst = obase + static_cast<int64_t>(y0 + c) * p.ldo + (x_row0 + lane);
+                typename S::T* dst = obase + static_cast<int64_t>(y0 + c) * p.ldo + (x_row0 + lane);
                 if (partial) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (j < ny) atomicAdd(dst, __uint_as_float(r[j]));
+                        if (j < ny) S::add1(dst, __uint_as_float(r[j]));
                         dst += p.ldo;
                     }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (j < ny) __stcs(dst, __uint_as_float(r[j]));
+                        if (j < ny) S::st1(dst, __uint_as_float(r[j]));
                         dst += p.ldo;
                     }
                 }
@@ -236,20 +241,23 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, 
 #pragma unroll
             for (int k = 0; k < 32; ++k)
                 v[k] = __uint_as_float(r[k]);
-            store_rows_chunk(p, obase, x_row0, nx, y0 + c, v, lane, stage_buf, partial);
+            store_rows_chunk<OT>(p, obase, x_row0, nx, y0 + c, v, lane, stage_buf, partial);
         }
     }
 }
 
-// Direct epilogue for Out rows whose starts are 32-byte aligned (ldo a
-// multiple of 8, base 32-byte aligned): no shared-memory staging.  TMEM is
-// read with the 16x256b shape, which hands each quad of lanes 8 consecutive
-// columns of one row, and each float2 store of a warp writes 8 whole 32-byte
-// sectors.  Same coverage and masking as epilogue_store.
+// Direct epilogue for Out rows whose starts are aligned to 8 elements (ldo a
+// multiple of 8, base aligned to 8 elements): no shared-memory staging.  TMEM
+// is read with the 16x256b shape, which hands each quad of lanes 8
+// consecutive columns of one row, so each pair store of a warp writes whole
+// 8-element row segments (32 bytes of fp32).  Same coverage and masking as
+// epilogue_store.
+template <int OT>
 __device__ __forceinline__ void epilogue_store_direct(const TcParams& p, const Seg& s, uint32_t tacc, int q,
                                                       int c_begin, int c_end, int lane)
 {
-    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    using S = OutStore<OT>;
+    typename S::T* obase = static_cast<typename S::T*>(p.out) + static_cast<int64_t>(s.b) * p.stride_o;
     const int x_row0 = s.x0 + q * 32;
     const int nx = s.xend - x_row0;
     const int rsub = lane >> 2;
@@ -268,16 +276,16 @@ __device__ __forceinline__ void epilogue_store_direct(const TcParams& p, const S
             for (int half = 0; half < 2; ++half) {
                 const int row = h * 16 + half * 8 + rsub;  // within the quadrant
                 if (row < nx) {
-                    float* dst = obase + static_cast<int64_t>(x_row0 + row) * p.ldo + s.y0 + c + csub;
+                    typename S::T* dst = obase + static_cast<int64_t>(x_row0 + row) * p.ldo + s.y0 + c + csub;
                     const int ncol = p.rows_y - (s.y0 + c + csub);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float v0 = __uint_as_float(r[4 * j + 2 * half]);
                         const float v1 = __uint_as_float(r[4 * j + 2 * half + 1]);
                         if (ncol - 8 * j >= 2)
-                            __stcs(reinterpret_cast<float2*>(dst + 8 * j), make_float2(v0, v1));
+                            S::st2(dst + 8 * j, v0, v1);
                         else if (ncol - 8 * j == 1)
-                            __stcs(dst + 8 * j, v0);
+                            S::st1(dst + 8 * j, v0);
                     }
                 }
             }

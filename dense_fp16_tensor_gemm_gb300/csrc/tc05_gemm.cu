@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         tc_mma_f16(d_tmem, sw128_kmajor_desc(xa + k * 32), sw128_kmajor_desc(ya + k * 32),
-                                   C::IDESC, (kb > s.kb0 || k > 0) ? 1u : 0u);
+                                   C::IDESC | p.ab_fmt, (kb > s.kb0 || k > 0) ? 1u : 0u);
                     }
                     const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
                     first = false;
@@ -235,8 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            epilogue_store<SWAP>(p, s, tmem_base + static_cast<uint32_t>(buf * BN), q, c_begin, c_begin + BN / 2,
-                                 lane, stage_buf);
+            {
+                const uint32_t tacc = tmem_base + static_cast<uint32_t>(buf * BN);
+                if (p.out_type == kOutF16)
+                    epilogue_store<SWAP, kOutF16>(p, s, tacc, q, c_begin, c_begin + BN / 2, lane, stage_buf);
+                else if (p.out_type == kOutBF16)
+                    epilogue_store<SWAP, kOutBF16>(p, s, tacc, q, c_begin, c_begin + BN / 2, lane, stage_buf);
+                else
+                    epilogue_store<SWAP, kOutF32>(p, s, tacc, q, c_begin, c_begin + BN / 2, lane, stage_buf);
+            }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[buf]));
             ++local;

@@ -139,6 +139,7 @@ __device__ __forceinline__ int sk_slot(const TcParams& p, int t, int q)
 // piece, sum the pieces in k order and store Out.  Nothing here waits on other
 // CTAs, so no co-residency is assumed; the sum order, and with it every bit of
 // Out, does not depend on which piece arrives last.
+template <int OT>
 __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uint32_t tacc, int q, int ew,
                                             int c_begin, int c_end, int lane, int rank, float* stage_buf,
                                             uint32_t tempty_leader)
@@ -178,7 +179,7 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
     __threadfence();
     if (lane == 0)
         *counter = 0;  // ready for the next launch
-    float* obase = p.out + static_cast<int64_t>(s.b) * p.stride_o;
+    typename OutStore<OT>::T* obase = static_cast<typename OutStore<OT>::T*>(p.out) + static_cast<int64_t>(s.b) * p.stride_o;
     const int x_row0 = s.x0 + q * 32;
     const int nx = s.xend - x_row0;
 #pragma unroll 1
@@ -208,7 +209,7 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
                 acc[k] = two ? t + v1[k] : t;
             }
         }
-        store_rows_chunk(p, obase, x_row0, nx, s.y0 + c, acc, lane, stage_buf, false);
+        store_rows_chunk<OT>(p, obase, x_row0, nx, s.y0 + c, acc, lane, stage_buf, false);
     }
 }
 
@@ -359,7 +360,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     const uint32_t ba = smem_u32(bs + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), C::IDESC,
+                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32),
+                                        C::IDESC | p.ab_fmt,
                                         (kb > s.kb0 || k > 0) ? 1u : 0u);
                     }
                     const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
@@ -401,16 +403,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             tc_fence_after();
             const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[buf]), 0);
+            const uint32_t tacc = tmem_base + static_cast<uint32_t>(buf * kAccStride);
             if (!DIRECT && s.partial) {
-                sk_epilogue(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, ew, c_begin, c_end, lane,
-                            static_cast<int>(rank), stage_buf, tempty_leader);
+                // the host splits only products with fp32 Out
+                sk_epilogue<kOutF32>(p, s, tacc, q, ew, c_begin, c_end, lane, static_cast<int>(rank), stage_buf,
+                                     tempty_leader);
             } else {
-                if (DIRECT)
-                    epilogue_store_direct(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, c_begin, c_end,
-                                          lane);
-                else
-                    epilogue_store<false>(p, s, tmem_base + static_cast<uint32_t>(buf * kAccStride), q, c_begin,
-                                          c_end, lane, stage_buf);
+                if (DIRECT) {
+                    if (p.out_type == kOutF16)
+                        epilogue_store_direct<kOutF16>(p, s, tacc, q, c_begin, c_end, lane);
+                    else if (p.out_type == kOutBF16)
+                        epilogue_store_direct<kOutBF16>(p, s, tacc, q, c_begin, c_end, lane);
+                    else
+                        epilogue_store_direct<kOutF32>(p, s, tacc, q, c_begin, c_end, lane);
+                } else {
+                    if (p.out_type == kOutF16)
+                        epilogue_store<false, kOutF16>(p, s, tacc, q, c_begin, c_end, lane, stage_buf);
+                    else if (p.out_type == kOutBF16)
+                        epilogue_store<false, kOutBF16>(p, s, tacc, q, c_begin, c_end, lane, stage_buf);
+                    else
+                        epilogue_store<false, kOutF32>(p, s, tacc, q, c_begin, c_end, lane, stage_buf);
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)

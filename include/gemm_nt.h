@@ -59,6 +59,13 @@ typedef enum gemm_status {
                                         scratch than the library's fixed array holds */
 } gemm_status_t;
 
+/* Element types of gemm_nt_batched_ex. */
+typedef enum gemm_dtype {
+    GEMM_DTYPE_F16 = 0,  /* IEEE binary16 */
+    GEMM_DTYPE_BF16 = 1, /* bfloat16: the upper half of an IEEE binary32 */
+    GEMM_DTYPE_F32 = 2   /* IEEE binary32 (Out only) */
+} gemm_dtype_t;
+
 /* Kernel choice.  GEMM_PATH_AUTO lets the library pick (see gemm_nt_select_path). */
 typedef enum gemm_path {
     GEMM_PATH_AUTO = 0,
@@ -103,6 +110,28 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *
                                            int64_t batch, int64_t strideA, int64_t strideB,
                                            int64_t strideO, gemm_path_t path,
                                            gemm_stream_t stream);
+
+/*
+ * The strided batched product with other element types: A and B both fp16 or
+ * both bf16 ("Warp Matrix Instructions", "Other Fragment Shapes and
+ * Transfers", names the float16 and bfloat16 forms of the warp MMA; the
+ * tcgen05 kind::f16 MMA of "Blackwell Tensor Cores" takes either), products
+ * accumulated in fp32 as always, and Out stored as fp32, or rounded to nearest
+ * even into fp16 or bf16 (Out's element size is then 2 bytes; ldo and strideO
+ * still count elements).  Same conventions, layouts and error behaviour as
+ * gemm_nt_f16_f32_batched_path; gemm_nt_f16_f32_batched_path(...) equals
+ * gemm_nt_batched_ex(..., GEMM_DTYPE_F16, GEMM_DTYPE_F32, ...).  An fp16 Out
+ * overflows to infinity beyond 65504.  Products that would split K across CTAs
+ * (few output tiles, long K) run on whole tiles when Out is not fp32, since
+ * the partial sums are kept in fp32 only.  Any other dtype value:
+ * GEMM_ERR_INVALID_VALUE.
+ */
+gemm_status_t gemm_nt_batched_ex(const void *A, const void *B, void *Out,
+                                 gemm_dtype_t ab_type, gemm_dtype_t out_type,
+                                 int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldo,
+                                 int64_t batch, int64_t strideA, int64_t strideB,
+                                 int64_t strideO, gemm_path_t path, gemm_stream_t stream);
 
 /*
  * Host-side pipeline for callers whose data lives in host memory: copies A and

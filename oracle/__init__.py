@@ -13,9 +13,16 @@ Accumulator's Lifetime" (the same product with a TMEM float32 accumulator);
 double replaces float32 as the accumulator so the oracle is at least as
 accurate as any fp32 implementation.
 
+The same product for bfloat16 inputs ("Warp Matrix Instructions", "Other
+Fragment Shapes and Transfers") is ``gemm_nt(..., dtype="bf16")``, with inputs
+given as uint16 bit patterns.
+
 Parity rule used by the tests (stated once here so every test uses the same):
     |Out - ref| <= 1e-3 * absdot + 1e-6    elementwise, and
     Out == ref exactly when every partial sum is an integer below 2**24.
+A 16-bit Out adds the rounding of ref into its format (half a unit in the
+last place: 2**-11 relative for float16, 2**-8 for bfloat16), and in the exact
+case Out == round_output(ref) exactly.
 """
 import ctypes
 
@@ -57,6 +64,14 @@ class Oracle:
         lib.oracle_gemm_nt_sampled.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
+        self.has_bf16 = hasattr(lib, "oracle_gemm_nt_bf16")
+        if self.has_bf16:
+            lib.oracle_bf16_to_double_array.argtypes = [u16p, f64p, i64]
+            lib.oracle_bf16_to_double_array.restype = None
+            lib.oracle_gemm_nt_bf16.argtypes = lib.oracle_gemm_nt.argtypes
+            lib.oracle_gemm_nt_bf16.restype = None
+            lib.oracle_gemm_nt_sampled_bf16.argtypes = lib.oracle_gemm_nt_sampled.argtypes
+            lib.oracle_gemm_nt_sampled_bf16.restype = None
         self.lib = lib
         self.path = path
 
@@ -72,11 +87,21 @@ class Oracle:
                                              _ptr(out, ctypes.c_double), b.size)
         return out
 
-    def gemm_nt(self, A, B, nthreads: int = 0):
-        """Full product.  A: (M,K) or (batch,M,K) fp16; B: (N,K) or (batch,N,K).
+    def bf16_to_double(self, bits) -> np.ndarray:
+        """Decode bfloat16 bit patterns (uint16) to float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_bf16_to_double_array(_ptr(b, ctypes.c_uint16), _ptr(out, ctypes.c_double), b.size)
+        return out
+
+    def gemm_nt(self, A, B, nthreads: int = 0, dtype: str = "f16"):
+        """Full product.  A: (M,K) or (batch,M,K); B: (N,K) or (batch,N,K);
+        float16 arrays, or uint16 bit patterns of fp16 (dtype "f16") or
+        bfloat16 (dtype "bf16").
 
         Returns (ref, absdot), float64 arrays of shape (M,N) or (batch,M,N).
         """
+        fn = self._fn("oracle_gemm_nt", dtype)
         a, b = _u16(A), _u16(B)
         squeeze = a.ndim == 2
         if squeeze:
@@ -87,14 +112,21 @@ class Oracle:
         N = b.shape[1]
         ref = np.empty((batch, M, N), dtype=np.float64)
         absdot = np.empty((batch, M, N), dtype=np.float64)
-        self.lib.oracle_gemm_nt(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16),
-                                _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double),
-                                batch, M, N, K, K, K, N, M * K, N * K, M * N, int(nthreads))
+        fn(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16),
+           _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double),
+           batch, M, N, K, K, K, N, M * K, N * K, M * N, int(nthreads))
         if squeeze:
             ref, absdot = ref[0], absdot[0]
         return ref, absdot
 
-    def gemm_nt_sampled(self, A, B, bidx, iidx, jidx, nthreads: int = 0):
+    def _fn(self, name, dtype):
+        if dtype == "f16":
+            return getattr(self.lib, name)
+        if dtype == "bf16" and self.has_bf16:
+            return getattr(self.lib, name + "_bf16")
+        raise ValueError("unknown input type %r" % dtype)
+
+    def gemm_nt_sampled(self, A, B, bidx, iidx, jidx, nthreads: int = 0, dtype: str = "f16"):
         """Selected elements (bidx[s], iidx[s], jidx[s]) of the product.
 
         A, B as in :meth:`gemm_nt` (2-D inputs take bidx = 0).  Returns
@@ -115,11 +147,10 @@ class Oracle:
             raise IndexError("sample index out of range")
         ref = np.empty(ii.shape, dtype=np.float64)
         absdot = np.empty(ii.shape, dtype=np.float64)
-        self.lib.oracle_gemm_nt_sampled(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16),
-                                        _ptr(bb, ctypes.c_int64), _ptr(ii, ctypes.c_int64),
-                                        _ptr(jj, ctypes.c_int64), ii.size, K, K, K, M * K, N * K,
-                                        _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double),
-                                        int(nthreads))
+        self._fn("oracle_gemm_nt_sampled", dtype)(
+            _ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), _ptr(bb, ctypes.c_int64),
+            _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, M * K, N * K,
+            _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double), int(nthreads))
         return ref, absdot
 
 
@@ -142,15 +173,52 @@ def half_to_double(bits):
     return default().half_to_double(bits)
 
 
-def gemm_nt(A, B, nthreads: int = 0):
-    return default().gemm_nt(A, B, nthreads)
+def bf16_to_double(bits):
+    return default().bf16_to_double(bits)
 
 
-def gemm_nt_sampled(A, B, bidx, iidx, jidx, nthreads: int = 0):
-    return default().gemm_nt_sampled(A, B, bidx, iidx, jidx, nthreads)
+def gemm_nt(A, B, nthreads: int = 0, dtype: str = "f16"):
+    return default().gemm_nt(A, B, nthreads, dtype)
 
 
-def within_tolerance(out, ref, absdot):
-    """Elementwise parity predicate |out-ref| <= 1e-3*absdot + 1e-6."""
+def gemm_nt_sampled(A, B, bidx, iidx, jidx, nthreads: int = 0, dtype: str = "f16"):
+    return default().gemm_nt_sampled(A, B, bidx, iidx, jidx, nthreads, dtype)
+
+
+# Half the spacing of an output format relative to the value (the largest
+# error of rounding to nearest), and half its smallest subnormal.
+OUT_ROUNDING = {"f32": (2.0 ** -24, 2.0 ** -150), "f16": (2.0 ** -11, 2.0 ** -25),
+                "bf16": (2.0 ** -8, 2.0 ** -134)}
+
+
+def round_output(ref, out_dtype: str):
+    """The value a ``out_dtype`` Out element holds when the fp32 accumulator
+    equals ``ref`` exactly (integer inputs with partial sums below 2**24): ref
+    rounded once to nearest, ties to even, in that format; float64 result.
+
+    float16: numpy's float32 -> float16 cast.  bfloat16: written out on the
+    binary32 bits -- add 0x7FFF plus the lowest kept bit, keep the upper 16."""
+    r = np.asarray(ref, dtype=np.float64)
+    f = r.astype(np.float32)
+    if not np.array_equal(f.astype(np.float64), r, equal_nan=True):
+        raise ValueError("round_output needs results that float32 holds exactly")
+    if out_dtype == "f32":
+        return f.astype(np.float64)
+    if out_dtype == "f16":
+        return f.astype(np.float16).astype(np.float64)
+    if out_dtype == "bf16":
+        u = np.ascontiguousarray(f).view(np.uint32).astype(np.uint64)
+        kept = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+        return kept.astype(np.uint32).view(np.float32).astype(np.float64)
+    raise ValueError("unknown output type %r" % out_dtype)
+
+
+def within_tolerance(out, ref, absdot, out_dtype: str = "f32"):
+    """Elementwise parity predicate |out-ref| <= 1e-3*absdot + 1e-6, widened
+    for a 16-bit Out by the rounding of ref into that format."""
     out = np.asarray(out, dtype=np.float64)
-    return np.abs(out - ref) <= 1e-3 * absdot + 1e-6
+    tol = 1e-3 * absdot + 1e-6
+    if out_dtype != "f32":
+        rel, tiny = OUT_ROUNDING[out_dtype]
+        tol = tol + rel * np.abs(ref) + tiny
+    return np.abs(out - ref) <= tol

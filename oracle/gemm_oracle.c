@@ -61,6 +61,36 @@ double oracle_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/*
+ * bfloat16 -> double, exact.  bfloat16 is the upper half of an IEEE binary32:
+ * 1 sign bit, 8 exponent bits with bias 127, 7 fraction bits; exponent 0
+ * encodes zero and subnormals (fraction * 2^-133), exponent 255 Inf or NaN.
+ * (The float16 and bfloat16 forms of the product are named together in "Warp
+ * Matrix Instructions", "Other Fragment Shapes and Transfers".)
+ */
+double oracle_bf16_to_double(uint16_t h)
+{
+    const unsigned sign = (h >> 15) & 1u;
+    const unsigned expo = (h >> 7) & 0xffu;
+    const unsigned frac = h & 0x7fu;
+    double v;
+    if (expo == 0) {
+        v = (double)frac * pow2i(-133);
+    } else if (expo == 255) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        /* (1 + frac/128) * 2^(expo-127) = (128 + frac) * 2^(expo-134) */
+        v = (double)(128u + frac) * pow2i((int)expo - 134);
+    }
+    return sign ? -v : v;
+}
+
+void oracle_bf16_to_double_array(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = oracle_bf16_to_double(src[t]);
+}
+
 /* Decode n fp16 bit patterns to double (vectorised convenience for Python). */
 void oracle_half_to_double_array(const uint16_t *src, double *dst, int64_t n)
 {
@@ -133,6 +163,56 @@ void oracle_gemm_nt_sampled(const uint16_t *A, const uint16_t *B,
         const uint16_t *b_row = B + bidx[s] * sB + jidx[s] * ldb;
         dot_nt(a_row, b_row, K, ref + s, absdot ? absdot + s : 0);
     }
+}
+
+/* The same product for bfloat16 inputs: element (i, j) is the sequential-k
+ * double sum of bf16 products (each exact in double: 8 x 8 significant bits). */
+static void dot_nt_bf16(const uint16_t *a_row, const uint16_t *b_row, int64_t K, double *ref, double *absdot)
+{
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double p = oracle_bf16_to_double(a_row[k]) * oracle_bf16_to_double(b_row[k]);
+        acc += p;
+        aacc += fabs(p);
+    }
+    *ref = acc;
+    if (absdot)
+        *absdot = aacc;
+}
+
+void oracle_gemm_nt_bf16(const uint16_t *A, const uint16_t *B, double *ref, double *absdot,
+                         int64_t batch, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldr,
+                         int64_t sA, int64_t sB, int64_t sR, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bi = 0; bi < batch * M; ++bi) {
+        const int64_t b = bi / M, i = bi % M;
+        const uint16_t *a_row = A + b * sA + i * lda;
+        for (int64_t j = 0; j < N; ++j) {
+            double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
+            dot_nt_bf16(a_row, B + b * sB + j * ldb, K, ref + b * sR + i * ldr + j, ab);
+        }
+    }
+}
+
+void oracle_gemm_nt_sampled_bf16(const uint16_t *A, const uint16_t *B,
+                                 const int64_t *bidx, const int64_t *iidx, const int64_t *jidx,
+                                 int64_t n, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t sA, int64_t sB, double *ref, double *absdot, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t s = 0; s < n; ++s)
+        dot_nt_bf16(A + bidx[s] * sA + iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, ref + s,
+                    absdot ? absdot + s : 0);
 }
 
 /* Number of threads the OpenMP runtime would use by default. */

@@ -12,7 +12,10 @@ Sources:
     against the fp32 product of randn inputs.
   * "Blackwell Tensor Cores", "The Accumulator's Lifetime": the same product
     for A (128,64), B (64,64), same check.
-  * IEEE 754 binary16 (the fp16 format) and exact rational arithmetic.
+  * "Warp Matrix Instructions", "Other Fragment Shapes and Transfers": the
+    same product with bfloat16 inputs.
+  * IEEE 754 binary16 (the fp16 format), bfloat16 (the upper 16 bits of an
+    IEEE binary32) and exact rational arithmetic.
 """
 from fractions import Fraction
 
@@ -201,5 +204,83 @@ def pin_batched_and_sampled(orc, seed=13):
     assert np.array_equal(sabs, wabs[bb, ii, jj].astype(np.float64))
 
 
+def bf16_values(bits):
+    """bfloat16 bit patterns -> float64 through the format's definition: the
+    pattern is the upper half of an IEEE binary32 whose lower half is zero."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_bits(x):
+    """float64 values that bfloat16 holds exactly -> their bit patterns."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32)
+    assert np.all(u & 0xFFFF == 0), "value is not a bfloat16"
+    return (u >> 16).astype(np.uint16)
+
+
+def pin_bf16_decoder_exhaustive(orc):
+    """All 65536 bfloat16 bit patterns decode to the binary32 they head."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.bf16_to_double(bits)
+    want = bf16_values(bits)
+    nan_g, nan_w = np.isnan(got), np.isnan(want)
+    assert np.array_equal(nan_g, nan_w), "NaN patterns decode differently"
+    assert np.array_equal(got[~nan_g], want[~nan_w]), "bf16 decoder mismatch"
+    assert np.array_equal(np.signbit(got[~nan_g]), np.signbit(want[~nan_w]))
+
+
+def pin_bf16_exact_tiny(orc, seed=21):
+    """bfloat16 products over random tiny shapes, with subnormals and values
+    near the format's extremes, equal the exact rational sum within the double
+    summation bound; batched and sampled elements agree with the full product."""
+    rng = np.random.default_rng(seed)
+    specials = np.array([0.0, -0.0, 2.0 ** -133, -(2.0 ** -126), 2.0 ** -127 * 3, 1.0, -1.5,
+                         2.0 ** 100 * 1.9921875, 255.0, -(2.0 ** -60)])
+    for (batch, M, N, K) in ((1, 3, 4, 9), (2, 5, 3, 17), (1, 1, 1, 1), (2, 4, 2, 33)):
+        vals_a = rng.choice(specials, size=(batch, M, K))
+        vals_b = rng.choice(specials, size=(batch, N, K))
+        mix_a = rng.random((batch, M, K)) < 0.5
+        mix_b = rng.random((batch, N, K)) < 0.5
+        # random normals truncated to bfloat16 (clear the low 16 bits of the binary32)
+        na = (rng.standard_normal((batch, M, K)).astype(np.float32).view(np.uint32) & 0xFFFF0000)
+        nb = (rng.standard_normal((batch, N, K)).astype(np.float32).view(np.uint32) & 0xFFFF0000)
+        a = np.where(mix_a, vals_a, na.view(np.float32).astype(np.float64))
+        b = np.where(mix_b, vals_b, nb.view(np.float32).astype(np.float64))
+        A, B = bf16_bits(a), bf16_bits(b)
+        ref, absdot = orc.gemm_nt(A, B, dtype="bf16")
+        assert np.all(np.isfinite(ref)) and np.all(np.isfinite(absdot)), "exact sums here are finite"
+        av, bv = bf16_values(A), bf16_values(B)
+        g = gamma(max(K - 1, 0))
+        for bi in range(batch):
+            for i in range(M):
+                for j in range(N):
+                    terms = [Fraction(float(av[bi, i, k])) * Fraction(float(bv[bi, j, k])) for k in range(K)]
+                    ex = sum(terms, Fraction(0))
+                    exa = sum((abs(t) for t in terms), Fraction(0))
+                    err = abs(Fraction(float(ref[bi, i, j])) - ex)
+                    assert err <= Fraction(g) * exa * Fraction(1 + 2 * U) + Fraction(2 * U) * abs(ex) \
+                        + Fraction(1, 2 ** 1074), "bf16 product differs from the exact sum"
+                    assert abs(Fraction(float(absdot[bi, i, j])) - exa) <= Fraction(g + 2 * U) * exa \
+                        + Fraction(1, 2 ** 1074), "bf16 absdot differs from the exact sum"
+        bb = rng.integers(0, batch, size=20)
+        ii = rng.integers(0, M, size=20)
+        jj = rng.integers(0, N, size=20)
+        sref, sabs = orc.gemm_nt_sampled(A, B, bb, ii, jj, dtype="bf16")
+        assert np.array_equal(sref, ref[bb, ii, jj]) and np.array_equal(sabs, absdot[bb, ii, jj])
+
+
+def pin_bf16_integer_exact(orc, seed=22):
+    """bfloat16 holds the integers in [-256, 256] exactly; with integer inputs
+    every partial sum is an integer below 2**53, so the product is exact."""
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-200, 201, size=(2, 13, 150))
+    B = rng.integers(-4, 5, size=(2, 9, 150))
+    ref, absdot = orc.gemm_nt(bf16_bits(A), bf16_bits(B), dtype="bf16")
+    assert np.array_equal(ref, np.einsum("bik,bjk->bij", A, B).astype(np.float64)), "bf16 integer product"
+    assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A), np.abs(B)).astype(np.float64))
+
+
 ALL_PINS = [pin_decoder_exhaustive, pin_bruteforce_tiny, pin_k1_exact, pin_worked_examples,
-            pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled]
+            pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled,
+            pin_bf16_decoder_exhaustive, pin_bf16_exact_tiny, pin_bf16_integer_exact]

@@ -113,3 +113,19 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(gnt, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         gnt.load(str(tmp_path / "nope.so"))
+
+
+def test_dtype_validation(lib):
+    """gemm_nt_batched_ex: unknown or unsupported element types, and an Out base
+    not aligned to its own element size, are rejected on the host."""
+    f = lib.gemm_nt_batched_ex
+    D = gnt.DType
+    base = (8, 8, 8, 8, 8, 8, 1, 64, 64, 64, 0, None)
+    assert f(FAKE_A, FAKE_B, FAKE_O, D.F32, D.F32, *base) == gnt.Status.INVALID_VALUE  # fp32 inputs
+    assert f(FAKE_A, FAKE_B, FAKE_O, 7, D.F32, *base) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, FAKE_B, FAKE_O, D.BF16, 9, *base) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, FAKE_B, FAKE_O + 1, D.F16, D.BF16, *base) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, FAKE_B, FAKE_O + 2, D.F16, D.F32, *base) == gnt.Status.INVALID_VALUE
+    # a 16-bit Out of 8x8 ends 128 bytes after its base: ending inside B overlaps
+    assert f(FAKE_A, FAKE_B, FAKE_B - 120, D.BF16, D.F16, *base) == gnt.Status.OVERLAP
+    assert f(FAKE_A, FAKE_B, FAKE_O, D.BF16, D.F16, 0, 8, 8, 8, 8, 8, 1, 64, 64, 64, 0, None) == 0

@@ -59,3 +59,31 @@ def test_within_tolerance_predicate():
 def _golden(name):
     import os
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+
+
+def test_round_output_matches_library_casts():
+    """round_output against torch's float32 -> float16 / bfloat16 casts (round
+    to nearest even), hand-picked ties, and the float32 identity."""
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(5).standard_normal(1 << 15).astype(np.float32) * np.float32(3e3)
+    x = np.concatenate([x, np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 2049.0, 2051.0, -2051.0, 0.0],
+                                    dtype=np.float32)])
+    t = torch.from_numpy(x)
+    assert np.array_equal(oracle.round_output(x, "f16"), t.to(torch.float16).double().numpy())
+    assert np.array_equal(oracle.round_output(x, "bf16"), t.to(torch.bfloat16).double().numpy())
+    assert np.array_equal(oracle.round_output(x, "f32"), x.astype(np.float64))
+    # ties go to even: 2049 -> 2048 and 2051 -> 2052 in float16; 1 + 2^-8 -> 1 in bfloat16
+    assert oracle.round_output(np.array([2049.0, 2051.0]), "f16").tolist() == [2048.0, 2052.0]
+    assert oracle.round_output(np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8]), "bf16").tolist() == \
+        [1.0, 1 + 2.0 ** -6]
+    with pytest.raises(ValueError):
+        oracle.round_output(np.array([1 + 2.0 ** -40]), "f16")
+
+
+def test_within_tolerance_widens_for_16_bit_outputs():
+    ref = np.array([1000.0, 1000.0])
+    absdot = np.array([0.0, 0.0])
+    out = np.array([1000.0 + 0.48, 1000.0 + 3.8])
+    assert oracle.within_tolerance(out, ref, absdot, "f16").tolist() == [True, False]
+    assert oracle.within_tolerance(out, ref, absdot, "bf16").tolist() == [True, True]
+    assert oracle.within_tolerance(out, ref, absdot, "f32").tolist() == [False, False]

@@ -25,6 +25,13 @@ MUTANTS = [
     ("sampled_ij_swapped", "iidx[s] * lda", "jidx[s] * lda"),
     ("product_sign", "oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k])",
      "-oracle_half_to_double(a_row[k]) * oracle_half_to_double(b_row[k])"),
+    ("bf16_exponent_bias", "(int)expo - 134", "(int)expo - 133"),
+    ("bf16_subnormal_scale", "pow2i(-133)", "pow2i(-134)"),
+    ("bf16_fraction_width", "const unsigned frac = h & 0x7fu;", "const unsigned frac = h & 0x3fu;"),
+    ("bf16_last_term_dropped", "oracle_bf16_to_double(a_row[k]) * oracle_bf16_to_double(b_row[k])",
+     "(k + 1 < K ? oracle_bf16_to_double(a_row[k]) * oracle_bf16_to_double(b_row[k]) : 0.0)"),
+    ("bf16_sampled_ij_swapped", "iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, ref + s,\n",
+     "jidx[s] * lda, B + bidx[s] * sB + iidx[s] * ldb, K, ref + s,\n"),
 ]
 
 

@@ -15,6 +15,11 @@ Recipe (one ``numpy.random.default_rng(seed)`` stream per workload):
     normal(0, 0.02) yields some fp16 subnormals, which are kept.
 Float draws are made in chunks of 2**24 values; the stream is sequential, so
 the chunking does not change the values.
+
+bfloat16 inputs (``dtype="bf16"``) come from the same draws: each float64 value
+is cast to float32 (numpy, round to nearest even) and the float32 is rounded to
+its upper 16 bits, again to nearest with ties to even.  They are returned as
+uint16 bit patterns (numpy has no bfloat16 type).
 """
 from dataclasses import dataclass
 
@@ -80,19 +85,46 @@ def _draw(rng, n, dist, sigma):
     return out
 
 
-def make_inputs(batch, M, N, K, dist="uniform", sigma=1.0, seed=0):
-    """Return (A, B) as float16 arrays of shape (batch,M,K), (batch,N,K)
-    (or (M,K), (N,K) when batch == 0 is passed to mean "unbatched")."""
+def float32_to_bf16_bits(x):
+    """Round float32 values to bfloat16, nearest with ties to even, returning
+    the uint16 bit patterns.  Inputs here are finite, so no NaN case is needed."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    return ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+
+
+def _draw_bf16(rng, n, dist, sigma):
+    out = np.empty(n, dtype=np.uint16)
+    if dist == "int4":
+        out[:] = float32_to_bf16_bits(rng.integers(-4, 5, size=n, dtype=np.int8).astype(np.float32))
+        return out
+    for s in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s)
+        if dist == "uniform":
+            v = rng.uniform(-1.0, 1.0, size=m)
+        elif dist == "normal":
+            v = sigma * rng.standard_normal(size=m)
+        else:
+            raise ValueError("unknown distribution %r" % dist)
+        out[s:s + m] = float32_to_bf16_bits(v.astype(np.float32))
+    return out
+
+
+def make_inputs(batch, M, N, K, dist="uniform", sigma=1.0, seed=0, dtype="f16"):
+    """Return (A, B) of shape (batch,M,K), (batch,N,K) (or (M,K), (N,K) when
+    batch == 0 is passed to mean "unbatched"): float16 arrays for dtype "f16",
+    uint16 bfloat16 bit patterns for dtype "bf16"."""
     rng = np.random.default_rng(seed)
     nb = max(batch, 1)
-    A = _draw(rng, nb * M * K, dist, sigma).reshape(nb, M, K)
-    B = _draw(rng, nb * N * K, dist, sigma).reshape(nb, N, K)
+    draw = {"f16": _draw, "bf16": _draw_bf16}[dtype]
+    A = draw(rng, nb * M * K, dist, sigma).reshape(nb, M, K)
+    B = draw(rng, nb * N * K, dist, sigma).reshape(nb, N, K)
     if batch == 0:
         return A[0], B[0]
     return A, B
 
 
-def workload_inputs(name):
+def workload_inputs(name, dtype="f16"):
     """Inputs of a named workload: 2-D for batch 1, 3-D otherwise."""
     w = WORKLOADS[name]
-    return make_inputs(0 if w.batch == 1 else w.batch, w.M, w.N, w.K, w.dist, w.sigma, w.seed)
+    return make_inputs(0 if w.batch == 1 else w.batch, w.M, w.N, w.K, w.dist, w.sigma, w.seed, dtype)
