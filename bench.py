@@ -45,10 +45,10 @@ L2_BYTES = 129 * 1024 * 1024
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1308568688, "85ea9d2d90bbb862"),
-    "square_4096": (126687744, "85ea9d2d90bbb862"),
-    "ragged_batch16_3001x2047x1000": (512107264, "85ea9d2d90bbb862"),
-    "skinny_64x16384x8192": (273558016, "6100f28e7a6a69e2"),
+    "square_8192": (1075181056 + 248084736, "661fcf4aeb053738"),
+    "square_4096": (91189504 + 34833152, "661fcf4aeb053738"),
+    "ragged_batch16_3001x2047x1000": (170580480 + 341193216, "661fcf4aeb053738"),
+    "skinny_64x16384x8192": (269558272 + 3643392, "adfe06414e4704fd"),
 }
 
 
@@ -161,20 +161,20 @@ def dist_init():
     return world, rank, local
 
 
-def oracle_cpu_sample(w, A, B, target_s):
+def oracle_cpu_sample(w, A, B, target_s, dtype="f16"):
     """Time the CPU oracle on whole rows of the workload (batch 0), sized to
     about target_s seconds.  Returns (tflops, seconds, rows, threads)."""
     import oracle
     A0 = A if A.ndim == 2 else A[0]
     B0 = B if B.ndim == 2 else B[0]
     probe = min(8, A0.shape[0])
-    oracle.gemm_nt(A0[:1], B0)  # thread pool start-up
+    oracle.gemm_nt(A0[:1], B0, dtype=dtype)  # thread pool start-up
     t0 = time.perf_counter()
-    oracle.gemm_nt(A0[:probe], B0)
+    oracle.gemm_nt(A0[:probe], B0, dtype=dtype)
     per_row = max(time.perf_counter() - t0, 1e-4) / probe
     rows = int(max(1, min(A0.shape[0], target_s / per_row)))
     t0 = time.perf_counter()
-    oracle.gemm_nt(A0[:rows], B0)
+    oracle.gemm_nt(A0[:rows], B0, dtype=dtype)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * B0.shape[0] * A0.shape[1]
     return flops / dt / 1e12, dt, rows, oracle.max_threads()
@@ -185,12 +185,12 @@ def run_reference(args, w):
     world, rank, _ = dist_init()
     if rank != 0:
         return 0
-    A, B = workloads.workload_inputs(w.name)
+    A, B = workloads.workload_inputs(w.name, args.ab_dtype)
     per_step = max(1.0, args.cpu_seconds / 5)
     vals = []
     rows_used = None
     for i in range(args.warmup + args.steps):
-        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, per_step)
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, per_step, args.ab_dtype)
         if i >= args.warmup:
             vals.append((tf, dt))
             rows_used = rows
@@ -202,7 +202,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, None),
+        "config": workload_config(w, None, args.ab_dtype, args.out_dtype),
         "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -211,14 +211,16 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, flush):
-    cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) fp16 row-major, "
-                       "fp32 accumulate, fp32 Out" % (
+def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None):
+    cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) %s row-major, "
+                       "fp32 accumulate, %s Out" % (
                            w.name, w.description, "%d," % w.batch if w.batch > 1 else "", w.M, w.K,
-                           "%d," % w.batch if w.batch > 1 else "", w.N, w.K),
-           "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed}
+                           "%d," % w.batch if w.batch > 1 else "", w.N, w.K, ab, out),
+           "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "ab_dtype": ab,
+           "out_dtype": out}
+    alg_bytes = alg_bytes or w.bytes
     if flush is not None:
-        cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (w.bytes / 2 ** 20)
+        cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (alg_bytes / 2 ** 20)
                      if not flush else "L2 flushed between timed steps (256 MiB write)")
     return cfg
 
@@ -234,6 +236,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16"],
+                    help="element type of A and B (bf16: the same draws rounded to bfloat16)")
+    ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
+                    help="element type of Out (16-bit: fp32 accumulator rounded to nearest even)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -258,25 +264,32 @@ def main():
 
     gnt.load()
     path = gnt.Path[args.path]
-    A, B = workloads.workload_inputs(w.name)
-    a = torch.from_numpy(A).cuda()
-    b = torch.from_numpy(B).cuda()
+    default_types = args.ab_dtype == "f16" and args.out_dtype == "f32"
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    codes = {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}
+    A, B = workloads.workload_inputs(w.name, args.ab_dtype)
+    a = torch.from_numpy(A.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
+    b = torch.from_numpy(B.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
     batched = A.ndim == 3
-    out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=torch.float32,
+    out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=tdt[args.out_dtype],
                       device="cuda")
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
+    nb = w.batch if batched else 1
+    sA, sB, sO = (w.M * w.K, w.N * w.K, w.M * w.N) if batched else (0, 0, 0)
 
     def step():
-        if batched:
+        if default_types:
             gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
-                                             w.K, w.K, w.N, w.batch, w.M * w.K, w.N * w.K, w.M * w.N,
-                                             path, sh)
+                                             w.K, w.K, w.N, nb, sA, sB, sO, path, sh)
         else:
-            gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
-                                             w.K, w.K, w.N, 1, 0, 0, 0, path, sh)
+            gnt.gemm_nt_batched_ex(a.data_ptr(), b.data_ptr(), out.data_ptr(), codes[args.ab_dtype],
+                                   codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB, sO,
+                                   path, sh)
 
-    flush = w.bytes <= 2 * L2_BYTES
+    # algorithmic bytes: A and B read once (2 bytes each), Out written once
+    alg_bytes = float(w.batch) * (2 * w.M * w.K + 2 * w.N * w.K + out.element_size() * w.M * w.N)
+    flush = alg_bytes <= 2 * L2_BYTES
     scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
 
     for _ in range(args.warmup):
@@ -325,13 +338,20 @@ def main():
 
     # ---- end to end through the host-buffer entry point
     e2e_steps = args.e2e_steps or max(3, args.steps // 4)
-    ha = torch.from_numpy(A).pin_memory()
-    hb = torch.from_numpy(B).pin_memory()
-    ho = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+    ha = torch.from_numpy(A.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
+    hb = torch.from_numpy(B.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
+    ho = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
 
     def e2e_step():
-        gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
-                                      b.data_ptr(), out.data_ptr(), w.M, w.N, w.K, w.batch, sh)
+        if default_types:
+            gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
+                                          b.data_ptr(), out.data_ptr(), w.M, w.N, w.K, w.batch, sh)
+        else:
+            # no pipelined host entry for these types: whole copies on the stream
+            a.copy_(ha, non_blocking=True)
+            b.copy_(hb, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -354,24 +374,24 @@ def main():
         return 0
 
     peaks = measured_peaks()
-    ai = w.flops / w.bytes
+    ai = w.flops / alg_bytes
     tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12
     tr = TRAFFIC.get(w.name)
-    traffic = tr[0] if tr and tr[1] == kernel_source_sha(w.name) else None
+    traffic = tr[0] if default_types and tr and tr[1] == kernel_source_sha(w.name) else None
     if tensor_bound:
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["tflops"], "traffic": traffic,
                 "peak_source": "%s bf16 dense burst (kind::f16 runs fp16 at the bf16 rate)" % peaks["source"]}
     else:
-        achieved = w.bytes / (kernel_ms * 1e-3) / 1e9
+        achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": "%s HBM copy bandwidth" % peaks["source"]}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, args.cpu_seconds)
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, args.cpu_seconds, args.ab_dtype)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": "%d full rows of batch 0 (%d x %d outputs, K=%d), %.1f s" % (
                    rows, rows, w.N, w.K, dt)}
@@ -379,13 +399,13 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": workload_config(w, flush),
+        "vs_baseline": None, "dtype": args.ab_dtype, "data": "synthetic",
+        "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
-                "d2h_bytes_per_step": int(out.numel() * 4)},
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "clocks": clocks,
         "gpu_launches": args.steps,
         "host_us_per_step": host_us,
