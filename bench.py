@@ -14,6 +14,9 @@ JSON line.
              A, B -> device, product, Out -> pinned host, every step
   roofline   the dominant kernel against the measured peak (MEASURED_PEAKS.json)
   cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+  hot        (workloads that fit in L2) the same steps back to back, no flush
+  context_cublas  cuBLAS (torch.mm / torch.bmm, fp32 Out where torch offers it)
+             on the same operands, timed the same way after the timed region
   --impl reference  times that oracle alone (the reference arm of this bench)
 
 Inputs of the default workload (512 MiB touched per step) exceed the 129 MB L2,
@@ -211,13 +214,18 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None):
+def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K"):
     cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) %s row-major, "
                        "fp32 accumulate, %s Out" % (
                            w.name, w.description, "%d," % w.batch if w.batch > 1 else "", w.M, w.K,
                            "%d," % w.batch if w.batch > 1 else "", w.N, w.K, ab, out),
            "batch": w.batch, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "ab_dtype": ab,
            "out_dtype": out}
+    if a_major != "K" or b_major != "K":
+        cfg["a_major"], cfg["b_major"] = a_major, b_major
+        cfg["workload"] += "; A stored %s, B stored %s" % (
+            "(K,M) row-major" if a_major == "MN" else "(M,K) row-major",
+            "(K,N) row-major" if b_major == "MN" else "(N,K) row-major")
     alg_bytes = alg_bytes or w.bytes
     if flush is not None:
         cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (alg_bytes / 2 ** 20)
@@ -236,6 +244,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS context timing")
+    ap.add_argument("--a-major", default="K", choices=["K", "MN"],
+                    help="MN: A handed to the library as its transpose, (K, M) row-major")
+    ap.add_argument("--b-major", default="K", choices=["K", "MN"],
+                    help="MN: B handed to the library as its transpose, (K, N) row-major (the NN product)")
     ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16"],
                     help="element type of A and B (bf16: the same draws rounded to bfloat16)")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
@@ -265,21 +278,32 @@ def main():
     gnt.load()
     path = gnt.Path[args.path]
     default_types = args.ab_dtype == "f16" and args.out_dtype == "f32"
+    a_mn, b_mn = args.a_major == "MN", args.b_major == "MN"
+    default_layout = not a_mn and not b_mn
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     codes = {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}
     A, B = workloads.workload_inputs(w.name, args.ab_dtype)
-    a = torch.from_numpy(A.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
-    b = torch.from_numpy(B.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
     batched = A.ndim == 3
+    # stored operands: an MN-major one is its transpose, row-major
+    As = np.ascontiguousarray(np.swapaxes(A, -1, -2)) if a_mn else A
+    Bs = np.ascontiguousarray(np.swapaxes(B, -1, -2)) if b_mn else B
+    lda, ldb = As.shape[-1], Bs.shape[-1]
+    a = torch.from_numpy(As.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
+    b = torch.from_numpy(Bs.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
     out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=tdt[args.out_dtype],
                       device="cuda")
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     nb = w.batch if batched else 1
     sA, sB, sO = (w.M * w.K, w.N * w.K, w.M * w.N) if batched else (0, 0, 0)
+    majors = {"K": gnt.Major.K, "MN": gnt.Major.MN}
 
     def step():
-        if default_types:
+        if not default_layout:
+            gnt.gemm_nt_batched_major(a.data_ptr(), majors[args.a_major], b.data_ptr(), majors[args.b_major],
+                                      out.data_ptr(), codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K,
+                                      lda, ldb, w.N, nb, sA, sB, sO, path, sh)
+        elif default_types:
             gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
                                              w.K, w.K, w.N, nb, sA, sB, sO, path, sh)
         else:
@@ -335,15 +359,73 @@ def main():
     ms_step = max_over_ranks(total_ms / args.steps, world, "cuda")
     value = job_tflops(w.flops, world, ms_step)
     kernel_ms = total_ms / args.steps
+    step_ms_median = statistics.median(per_launch) if flush else None
+
+    def timed(fn, n):
+        """Mean ms per call of fn over n calls, CUDA events on the stream;
+        L2 flushed before each call when the workload fits in L2."""
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        if flush:
+            for i in range(n):
+                scratch.fill_(float(i))
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+                fn()
+                s1.record(stream)
+                ts.append((s0, s1))
+        else:
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(n):
+                fn()
+            s1.record(stream)
+            ts.append((s0, s1))
+        torch.cuda.synchronize()
+        return sum(x.elapsed_time(y) for x, y in ts) / n
+
+    # ---- hot-L2 figure for workloads that fit in L2 (steps back to back, no flush)
+    hot = None
+    if flush:
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        h0.record(stream)
+        for _ in range(args.steps):
+            step()
+        h1.record(stream)
+        torch.cuda.synchronize()
+        hot_ms = h0.elapsed_time(h1) / args.steps
+        hot = {"value": w.flops / (hot_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": hot_ms,
+               "l2": "inputs resident in L2 from the previous step (no flush)"}
+
+    # ---- context: cuBLAS on the same operands, timed the same way
+    cublas = None
+    if not args.no_cublas:
+        # the logical operands: A (M, K) and B^T (K, N), views of the stored ones
+        al = a.transpose(-1, -2) if a_mn else a
+        bt = b if b_mn else b.transpose(-1, -2)
+        mm = torch.bmm if batched else torch.mm
+        try:
+            mm(al, bt, out_dtype=torch.float32)
+            cub_fn, cub_out = (lambda: mm(al, bt, out_dtype=torch.float32)), "f32"
+        except (TypeError, RuntimeError, NotImplementedError):
+            cub_fn, cub_out = (lambda: mm(al, bt)), args.ab_dtype
+        cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
+        cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
+                  "call": "torch.%s(A, B^T%s) -> %s Out" % (
+                      "bmm" if batched else "mm", ", out_dtype=float32" if cub_out == "f32" else "", cub_out),
+                  "ratio": (w.flops / (kernel_ms * 1e-3) / 1e12) / (w.flops / (cub_ms * 1e-3) / 1e12)}
 
     # ---- end to end through the host-buffer entry point
     e2e_steps = args.e2e_steps or max(3, args.steps // 4)
-    ha = torch.from_numpy(A.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
-    hb = torch.from_numpy(B.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
+    ha = torch.from_numpy(As.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
+    hb = torch.from_numpy(Bs.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
     ho = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
 
     def e2e_step():
-        if default_types:
+        if default_types and default_layout:
             gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
                                           b.data_ptr(), out.data_ptr(), w.M, w.N, w.K, w.batch, sh)
         else:
@@ -377,7 +459,7 @@ def main():
     ai = w.flops / alg_bytes
     tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12
     tr = TRAFFIC.get(w.name)
-    traffic = tr[0] if default_types and tr and tr[1] == kernel_source_sha(w.name) else None
+    traffic = tr[0] if default_types and default_layout and tr and tr[1] == kernel_source_sha(w.name) else None
     if tensor_bound:
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
@@ -400,7 +482,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.ab_dtype, "data": "synthetic",
-        "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes),
+        "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes, args.a_major, args.b_major),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s",
@@ -410,6 +492,11 @@ def main():
         "gpu_launches": args.steps,
         "host_us_per_step": host_us,
         "path": args.path,
+        "ms_per_step_median": step_ms_median,
+        "hot": hot,
+        "context_cublas": cublas,
+        "device": {"name": torch.cuda.get_device_name(local),
+                   "sms": torch.cuda.get_device_properties(local).multi_processor_count},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

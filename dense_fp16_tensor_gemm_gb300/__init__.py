@@ -32,6 +32,11 @@ class DType(enum.IntEnum):
     F32 = 2
 
 
+class Major(enum.IntEnum):
+    K = 0   # operand (rows, K) stored row-major
+    MN = 1  # operand stored as its transpose, (K, rows) row-major
+
+
 class Path(enum.IntEnum):
     AUTO = 0
     TC05 = 1
@@ -56,6 +61,8 @@ _SIGNATURES = {
     "gemm_nt_f16_f32_batched_no_alloc": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10 + [_vp]),
     "gemm_nt_batched_ex": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int] + [_i64] * 10
                            + [ctypes.c_int, _vp]),
+    "gemm_nt_batched_major": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int]
+                              + [_i64] * 10 + [ctypes.c_int, _vp]),
     "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
     "gemm_nt_check": (ctypes.c_int, [_vp]),
     "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -114,6 +121,12 @@ def gemm_nt_batched_ex(A, B, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, bat
                        strideO, path=0, stream=0):
     _check(load().gemm_nt_batched_ex(A, B, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo,
                                      batch, strideA, strideB, strideO, int(path), stream))
+
+
+def gemm_nt_batched_major(A, a_major, B, b_major, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch,
+                          strideA, strideB, strideO, path=0, stream=0):
+    _check(load().gemm_nt_batched_major(A, int(a_major), B, int(b_major), Out, int(ab_type), int(out_type), M, N,
+                                        K, lda, ldb, ldo, batch, strideA, strideB, strideO, int(path), stream))
 
 
 def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,

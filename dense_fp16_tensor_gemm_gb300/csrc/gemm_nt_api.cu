@@ -160,6 +160,16 @@ struct Problem {
     int64_t M, N, K, lda, ldb, ldo, batch, sA, sB, sO;
     int ab_type = GEMM_DTYPE_F16;   // element type of A and B
     int out_type = GEMM_DTYPE_F32;  // element type of Out
+    int a_major = GEMM_MAJOR_K;     // A(i,k) at A[i*lda + k] (K) or A[k*lda + i] (MN)
+    int b_major = GEMM_MAJOR_K;
+
+    bool a_mn() const { return a_major == GEMM_MAJOR_MN; }
+    bool b_mn() const { return b_major == GEMM_MAJOR_MN; }
+    // stored matrices: (rows, cols) row-major with pitch lda / ldb
+    int64_t a_rows() const { return a_mn() ? K : M; }
+    int64_t a_cols() const { return a_mn() ? M : K; }
+    int64_t b_rows() const { return b_mn() ? K : N; }
+    int64_t b_cols() const { return b_mn() ? N : K; }
 
     int64_t out_esize() const { return out_type == GEMM_DTYPE_F32 ? 4 : 2; }
     int kernel_out() const { return out_type == GEMM_DTYPE_F16 ? kOutF16 : (out_type == GEMM_DTYPE_BF16 ? kOutBF16 : kOutF32); }
@@ -189,15 +199,19 @@ gemm_status_t validate(const Problem& q)
         return GEMM_ERR_INVALID_VALUE;
     if (q.K > 0 && (!q.A || !q.B))
         return GEMM_ERR_INVALID_VALUE;
-    if (q.ldo < q.N || (q.K > 0 && (q.lda < q.K || q.ldb < q.K)))
+    if (q.a_major != GEMM_MAJOR_K && q.a_major != GEMM_MAJOR_MN)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.b_major != GEMM_MAJOR_K && q.b_major != GEMM_MAJOR_MN)
+        return GEMM_ERR_INVALID_VALUE;
+    if (q.ldo < q.N || (q.K > 0 && (q.lda < q.a_cols() || q.ldb < q.b_cols())))
         return GEMM_ERR_INVALID_VALUE;
     if (q.sA < 0 || q.sB < 0 || q.sO < 0)
         return GEMM_ERR_INVALID_VALUE;
     // 64-bit extent limits (keep every byte offset below 2^62)
     const double lim = 4.0e18;
     if (static_cast<double>(q.batch) * static_cast<double>(std::max(q.sO, q.ldo * q.M)) * 4.0 > lim ||
-        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.M)) * 2.0 > lim ||
-        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.N)) * 2.0 > lim)
+        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.a_rows())) * 2.0 > lim ||
+        static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.b_rows())) * 2.0 > lim)
         return GEMM_ERR_INVALID_VALUE;
     if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16)
         return GEMM_ERR_INVALID_VALUE;
@@ -210,8 +224,8 @@ gemm_status_t validate(const Problem& q)
     if (q.K > 0) {
         uintptr_t olo, ohi, alo, ahi, blo, bhi;
         span(q.Out, q.out_esize(), q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
-        span(q.A, 2, q.batch, q.sA, q.M, q.lda, q.K, alo, ahi);
-        span(q.B, 2, q.batch, q.sB, q.N, q.ldb, q.K, blo, bhi);
+        span(q.A, 2, q.batch, q.sA, q.a_rows(), q.lda, q.a_cols(), alo, ahi);
+        span(q.B, 2, q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
         if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
             return GEMM_ERR_OVERLAP;
     }
@@ -229,7 +243,7 @@ bool tma_ok(const Problem& q)
     if (q.batch > 1 && ((q.sA % 8) || (q.sB % 8)))
         return false;
     // a batch dimension in a tensor map must step over whole matrices
-    if (q.batch > 1 && ((q.sA != 0 && q.sA < q.M * q.lda) || (q.sB != 0 && q.sB < q.N * q.ldb)))
+    if (q.batch > 1 && ((q.sA != 0 && q.sA < q.a_rows() * q.lda) || (q.sB != 0 && q.sB < q.b_rows() * q.ldb)))
         return false;
     const int64_t lim = int64_t(1) << 39;  // elements of 2 bytes
     if (q.lda >= lim || q.ldb >= lim || q.sA >= lim || q.sB >= lim)
@@ -256,10 +270,11 @@ struct MapKey {
     int64_t rows, K, ld, batch, stride;
     int box_rows;
     bool bf16;
+    bool mn;
     bool operator==(const MapKey& o) const
     {
         return base == o.base && rows == o.rows && K == o.K && ld == o.ld && batch == o.batch &&
-               stride == o.stride && box_rows == o.box_rows && bf16 == o.bf16;
+               stride == o.stride && box_rows == o.box_rows && bf16 == o.bf16 && mn == o.mn;
     }
 };
 
@@ -273,18 +288,22 @@ struct MapCache {
 
 thread_local MapCache t_maps;
 
+// An operand of `rows` rows (M or N) and K columns.  K-major: dims {K, rows,
+// batch}, box {64, box_rows}.  MN-major (stored as (K, rows) with pitch ld):
+// dims {rows, K, batch}, box {64 rows, 64 K}; box_rows is then ignored.
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-                int64_t stride, int box_rows, int* bmul, bool bf16)
+                int64_t stride, int box_rows, int* bmul, bool bf16, bool mn)
 {
     auto enc = encode_fn();
     if (!enc)
         return false;
     const bool batched = batch > 1 && stride > 0;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+    const int64_t inner = mn ? rows : K, outer = mn ? K : rows;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                           static_cast<cuuint64_t>(batched ? batch : 1)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
-                             static_cast<cuuint64_t>((batched ? stride : rows * ld) * 2)};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+                             static_cast<cuuint64_t>((batched ? stride : outer * ld) * 2)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(mn ? 64 : box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     *bmul = batched ? 1 : 0;
     CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -294,9 +313,9 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
 }
 
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-              int64_t stride, int box_rows, int* bmul, bool bf16 = false)
+              int64_t stride, int box_rows, int* bmul, bool bf16 = false, bool mn = false)
 {
-    const MapKey k{base, rows, K, ld, batch, stride, box_rows, bf16};
+    const MapKey k{base, rows, K, ld, batch, stride, box_rows, bf16, mn};
     MapCache& c = t_maps;
     for (int i = 0; i < c.count; ++i) {
         if (c.key[i] == k) {
@@ -305,7 +324,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64
             return true;
         }
     }
-    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul, bf16))
+    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul, bf16, mn))
         return false;
     const int slot = c.next;
     c.key[slot] = k;
@@ -346,6 +365,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     const int64_t xrows = swap ? q.N : q.M, yrows = swap ? q.M : q.N;
     const int64_t xld = swap ? q.ldb : q.lda, yld = swap ? q.lda : q.ldb;
     const int64_t xs = swap ? q.sB : q.sA, ys = swap ? q.sA : q.sB;
+    const bool x_mn = swap ? q.b_mn() : q.a_mn(), y_mn = swap ? q.a_mn() : q.b_mn();
     int bn;
     if (swap) {
         if (yrows > 64)
@@ -358,8 +378,9 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     // Row split (swapped operands, one batch, one column tile, 64..128 rows of
     // X per CTA): every CTA takes an even share of the rows over all of K, with
     // an X box just tall enough for that share (a multiple of 8 rows).
-    const bool rowsplit = swap && q.batch == 1 && yrows <= bn && xrows >= 64 * static_cast<int64_t>(d.num_sms) &&
-                          xrows <= 128 * static_cast<int64_t>(d.num_sms);
+    // (K-major X only: an MN-major box is whole 64-row chunks.)
+    const bool rowsplit = swap && !x_mn && q.batch == 1 && yrows <= bn &&
+                          xrows >= 64 * static_cast<int64_t>(d.num_sms) && xrows <= 128 * static_cast<int64_t>(d.num_sms);
     int xbox = 128;
     if (rowsplit) {
         const int64_t share = (xrows + d.num_sms - 1) / d.num_sms;
@@ -367,12 +388,14 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     }
     p.x_box_bytes = xbox * 128;
     CUtensorMap tmx, tmy;
-    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
-        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
+    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16, x_mn) ||
+        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16, y_mn))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.out_type = q.kernel_out();
-    p.ab_fmt = q.ab_fmt();
+    p.x_mn = x_mn ? 1 : 0;
+    p.y_mn = y_mn ? 1 : 0;
+    p.idesc_bits = q.ab_fmt() | (x_mn ? 1u << 15 : 0u) | (y_mn ? 1u << 16 : 0u);
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(xrows);
@@ -452,6 +475,8 @@ bool pair_split(int64_t ntiles, int num_kb, int pairs, int out_type)
 
 int pair_plan_width(const Problem& q, const DeviceState& d)
 {
+    if (q.b_mn())
+        return 256;  // each CTA's half of B must be whole 64-row chunks
     const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
     if (pair_split(tiles256, static_cast<int>((q.K + 63) / 64), d.max_pairs, q.out_type))
         return 256;
@@ -467,12 +492,16 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     TcParams p{};
     const int pbn = pair_plan_width(q, d);
     CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16,
+                  q.a_mn()) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16,
+                  q.b_mn()))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.out_type = q.kernel_out();
-    p.ab_fmt = q.ab_fmt();
+    p.x_mn = q.a_mn() ? 1 : 0;
+    p.y_mn = q.b_mn() ? 1 : 0;
+    p.idesc_bits = q.ab_fmt() | (q.a_mn() ? 1u << 15 : 0u) | (q.b_mn() ? 1u << 16 : 0u);
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(q.M);
@@ -552,6 +581,8 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     p.stride_o = q.sO;
     p.vec_a = aligned(q.A, 16) && q.lda % 8 == 0 && (q.batch == 1 || q.sA % 8 == 0);
     p.vec_b = aligned(q.B, 16) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
+    p.a_mn = q.a_mn() ? 1 : 0;
+    p.b_mn = q.b_mn() ? 1 : 0;
     return mmasync_launch(p, q.ab_type == GEMM_DTYPE_BF16, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -710,7 +741,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.out_type = q.kernel_out();
-    p.ab_fmt = q.ab_fmt();
+    p.idesc_bits = q.ab_fmt();
     p.ldo = q.ldo;
     p.stride_o = q.sO;
     p.rows_x = static_cast<int>(q.M);
@@ -804,6 +835,19 @@ gemm_status_t gemm_nt_batched_ex(const void* A, const void* B, void* Out, gemm_d
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
     q.ab_type = static_cast<int>(ab_type);
     q.out_type = static_cast<int>(out_type);
+    return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_batched_major(const void* A, gemm_major_t a_major, const void* B, gemm_major_t b_major,
+                                    void* Out, gemm_dtype_t ab_type, gemm_dtype_t out_type, int64_t M, int64_t N,
+                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
+                                    int64_t strideB, int64_t strideO, gemm_path_t path, gemm_stream_t stream)
+{
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    q.ab_type = static_cast<int>(ab_type);
+    q.out_type = static_cast<int>(out_type);
+    q.a_major = static_cast<int>(a_major);
+    q.b_major = static_cast<int>(b_major);
     return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
 }
 

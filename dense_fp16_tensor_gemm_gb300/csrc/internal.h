@@ -24,7 +24,10 @@ constexpr uint32_t kStatusTimeout = 1u;
 struct TcParams {
     void* out;            // fp32, fp16 or bf16 elements (out_type)
     int out_type;         // kOutF32, kOutF16 or kOutBF16
-    uint32_t ab_fmt;      // instruction-descriptor bits of the A/B element type (0: fp16)
+    uint32_t idesc_bits;  // instruction-descriptor bits ORed into every MMA: A/B element
+                          // type (0: fp16) and the A (bit 15) / B (bit 16) MN-major flags
+    int x_mn;             // 1: X is MN-major (tiles of 64 rows x 64 K per TMA box)
+    int y_mn;             // 1: Y is MN-major
     int64_t ldo;
     int64_t stride_o;
     int rows_x;
@@ -66,6 +69,8 @@ struct MmaParams {
     int64_t stride_a, stride_b, stride_o;
     int vec_a;  // A rows and base 16-byte aligned
     int vec_b;
+    int a_mn;   // 1: A is MN-major, A(i, k) at A[k*lda + i]
+    int b_mn;   // 1: B is MN-major, B(j, k) at B[k*ldb + j]
 };
 
 // tcgen05 kernel family.  bn in {64, 128, 256}; swap selects the transposed

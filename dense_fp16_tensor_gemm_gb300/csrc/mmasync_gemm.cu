@@ -19,6 +19,13 @@
 // time through shared memory with 80-byte row pitch (16-byte aligned rows,
 // conflict-free ldmatrix).  Out-of-range rows and the K tail are zero-filled
 // while staging, and stores are masked.
+//
+// An MN-major operand (A stored as (K, M), B as (K, N)) is staged as it lies,
+// 32 K-rows of 64 elements with a 144-byte pitch, i.e. a column-major shared
+// tile of the operand; "copy -> ldstmatrix" ("Algorithm" step 3) reads such a
+// tile with the .trans form of ldmatrix, whose lane t receives elements
+// (2(t%4), t/4) and (2(t%4)+1, t/4) of each 8x8 block: with K on the block's
+// rows that is exactly the fragment the row-major tile gives.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -28,7 +35,10 @@ namespace {
 
 constexpr int MBM = 64, MBN = 64, MBK = 32, MPAD = 8;
 constexpr int MPITCH = MBK + MPAD;  // 40 fp16 = 80 bytes
+constexpr int MNPITCH = 64 + 8;     // MN-major tile: 72 fp16 = 144 bytes per K-row
 constexpr int MThreads = 128;
+constexpr int kTileElems = MBM * MPITCH;  // >= MBK * MNPITCH
+static_assert(MBK * MNPITCH <= kTileElems, "MN-major tile fits the slot");
 
 // Stage one (rows x 32) operand tile into shared memory, zero-filling
 // everything outside rows < nrows and k < K.
@@ -78,6 +88,55 @@ __device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, 
     }
 }
 
+// Stage one MN-major operand tile, rows [mn0, mn0 + 64) x k in [k0, k0 + 32),
+// from src (element (r, k) at src[k*ld + r]) into sdst[kk][r - mn0], zero
+// outside r < nmn and k < K.
+__device__ __forceinline__ void stage_tile_mn(uint16_t* sdst, const uint16_t* src, int64_t ld, int mn0, int nmn,
+                                              int k0, int K, bool vec)
+{
+    const int tid = threadIdx.x;
+    if (vec) {
+        // 32 K-rows x 8 chunks of 8 elements, two chunks per thread.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = tid + i * MThreads;
+            const int kk = c >> 3;
+            const int rc = (c & 7) * 8;
+            const int k = k0 + kk;
+            const int r = mn0 + rc;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (k < K) {
+                const uint16_t* g = src + static_cast<int64_t>(k) * ld + r;
+                if (r + 8 <= nmn) {
+                    v = *reinterpret_cast<const uint4*>(g);
+                } else if (r < nmn) {
+                    uint16_t tmp[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        tmp[e] = (r + e < nmn) ? g[e] : uint16_t(0);
+                    v = make_uint4(tmp[0] | (uint32_t(tmp[1]) << 16), tmp[2] | (uint32_t(tmp[3]) << 16),
+                                   tmp[4] | (uint32_t(tmp[5]) << 16), tmp[6] | (uint32_t(tmp[7]) << 16));
+                }
+            }
+            *reinterpret_cast<uint4*>(sdst + kk * MNPITCH + rc) = v;
+        }
+    } else {
+        // Element-wise, consecutive threads on consecutive rows of the operand.
+#pragma unroll 4
+        for (int i = 0; i < (MBK * 64) / MThreads; ++i) {
+            const int e = tid + i * MThreads;
+            const int kk = e >> 6;
+            const int rr = e & 63;
+            const int k = k0 + kk;
+            const int r = mn0 + rr;
+            uint16_t v = 0;
+            if (r < nmn && k < K)
+                v = src[static_cast<int64_t>(k) * ld + r];
+            sdst[kk * MNPITCH + rr] = v;
+        }
+    }
+}
+
 // Out rows [row0, ...) of one 64x64 CTA tile through the D-fragment map.
 template <int OT>
 __device__ __forceinline__ void store_tile(const MmaParams& p, int b, int m0, int n0, int wm, int wn, int lane,
@@ -101,8 +160,8 @@ __device__ __forceinline__ void store_tile(const MmaParams& p, int b, int m0, in
 template <bool BF16>
 __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams p)
 {
-    __shared__ __align__(16) uint16_t As[MBM * MPITCH];
-    __shared__ __align__(16) uint16_t Bs[MBN * MPITCH];
+    __shared__ __align__(16) uint16_t As[kTileElems];
+    __shared__ __align__(16) uint16_t Bs[kTileElems];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -123,26 +182,50 @@ __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams 
 
         for (int k0 = 0; k0 < p.K; k0 += MBK) {
             __syncthreads();  // previous tile fully consumed
-            stage_tile(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
-            stage_tile(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
+            if (p.a_mn)
+                stage_tile_mn(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
+            else
+                stage_tile(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
+            if (p.b_mn)
+                stage_tile_mn(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
+            else
+                stage_tile(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
             __syncthreads();
 #pragma unroll
             for (int ks = 0; ks < MBK; ks += 16) {
+                // Lane l addresses row l%8 of 8x8 block q = l/8.
+                const int q = lane >> 3, r8 = lane & 7;
                 uint32_t af[2][4];
 #pragma unroll
                 for (int mi = 0; mi < 2; ++mi) {
-                    const int row = wm * 32 + mi * 16 + (lane & 15);
-                    const int col = ks + (lane >> 4) * 8;
-                    ldmatrix_x4(smem_u32(As + row * MPITCH + col), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+                    if (p.a_mn) {
+                        // block q: rows m + 8(q%2), k + 8(q/2); K runs down the shared tile
+                        const int krow = ks + (q >> 1) * 8 + r8;
+                        const int col = wm * 32 + mi * 16 + (q & 1) * 8;
+                        ldmatrix_x4_trans(smem_u32(As + krow * MNPITCH + col), af[mi][0], af[mi][1], af[mi][2],
+                                          af[mi][3]);
+                    } else {
+                        const int row = wm * 32 + mi * 16 + (lane & 15);
+                        const int col = ks + (lane >> 4) * 8;
+                        ldmatrix_x4(smem_u32(As + row * MPITCH + col), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+                    }
                 }
                 uint32_t bfr[4][2];
 #pragma unroll
                 for (int nj = 0; nj < 2; ++nj) {
-                    // lanes 0-7: n 0-7 @k, 8-15: n 0-7 @k+8, 16-23: n 8-15 @k, 24-31: n 8-15 @k+8
-                    const int row = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    const int col = ks + ((lane >> 3) & 1) * 8;
-                    ldmatrix_x4(smem_u32(Bs + row * MPITCH + col), bfr[2 * nj][0], bfr[2 * nj][1],
-                                bfr[2 * nj + 1][0], bfr[2 * nj + 1][1]);
+                    if (p.b_mn) {
+                        // block q: k + 8(q%2), n + 8(q/2)
+                        const int krow = ks + (q & 1) * 8 + r8;
+                        const int col = wn * 32 + nj * 16 + (q >> 1) * 8;
+                        ldmatrix_x4_trans(smem_u32(Bs + krow * MNPITCH + col), bfr[2 * nj][0], bfr[2 * nj][1],
+                                          bfr[2 * nj + 1][0], bfr[2 * nj + 1][1]);
+                    } else {
+                        // lanes 0-7: n 0-7 @k, 8-15: n 0-7 @k+8, 16-23: n 8-15 @k, 24-31: n 8-15 @k+8
+                        const int row = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
+                        const int col = ks + ((lane >> 3) & 1) * 8;
+                        ldmatrix_x4(smem_u32(Bs + row * MPITCH + col), bfr[2 * nj][0], bfr[2 * nj][1],
+                                    bfr[2 * nj + 1][0], bfr[2 * nj + 1][1]);
+                    }
                 }
 #pragma unroll
                 for (int mi = 0; mi < 2; ++mi)

@@ -38,6 +38,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// As mbar_try_wait, letting the thread sleep (until the phase completes, or at
+// most `hint_ns` nanoseconds) instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
@@ -123,6 +138,19 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+__device__ __forceinline__ void tc_mma_f16_w(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)
@@ -186,6 +214,47 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand tile: TMA writes it as
+// chunks of 64 rows (MN) x 64 K, each chunk 64 K-rows of 128 bytes (64 fp16 of
+// MN) with 128-byte swizzle, 8 KB per chunk.  In the MN-major swizzled layout
+// the leading byte offset steps from one 64-element MN chunk to the next
+// (8192 B) and the stride byte offset from one 8-row K group to the next
+// (1024 B).  Stepping K by 16 inside a chunk moves two K groups: +2048 bytes.
+constexpr uint32_t kMnChunkBytes = 64 * 64 * 2;
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(kMnChunkBytes >> 4) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Descriptor of the k-th 16-wide K slice of a stage slot holding an operand in
+// either order.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t slot, bool mn_major, int k)
+{
+    return mn_major ? sw128_mnmajor_desc(slot + static_cast<uint32_t>(k) * 2048u)
+                    : sw128_kmajor_desc(slot + static_cast<uint32_t>(k) * 32u);
+}
+
+// A shared-memory descriptor split into its 32-bit halves, for issue loops
+// that step through a ring of stage slots by additions only.  `lo` holds the
+// start address (>> 4) of the first slot and the leading byte offset; `hi` the
+// stride byte offset, version and swizzle; `kstep` is what one 16-wide K slice
+// adds to `lo` (32 B for K-major tiles, 2048 B for MN-major ones, >> 4).
+struct DescWords {
+    uint32_t lo, hi, kstep;
+};
+
+__device__ __forceinline__ DescWords desc_words(uint32_t slot0, bool mn_major)
+{
+    const uint64_t d = mn_major ? sw128_mnmajor_desc(slot0) : sw128_kmajor_desc(slot0);
+    return {static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32), mn_major ? 2048u >> 4 : 32u >> 4};
 }
 
 // Instruction descriptor for kind::f16: A and B fp16, D fp32, both K-major,
@@ -271,6 +340,20 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc,
         : "memory");
 }
 
+// The same MMAs with the descriptors given as 32-bit halves (see DescWords).
+__device__ __forceinline__ void tc_mma_f16_pair_w(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo,
+                                                  uint32_t bhi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at this shared offset in every CTA of `cta_mask`
 // when the pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
@@ -307,6 +390,18 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32
                                             uint32_t& r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(saddr)
+                 : "memory");
+}
+
+// The transposing form: of the 8x8 tile whose 8 rows the lanes address, lane
+// t receives the elements (2*(t%4), t/4) and (2*(t%4)+1, t/4), i.e. the
+// fragment of the tile's transpose.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(saddr)
                  : "memory");

@@ -11,6 +11,45 @@ namespace tc {
 constexpr int BM = 128;  // MMA rows per CTA (TMEM lanes)
 constexpr int BK = 64;   // K per stage: 64 fp16 = one 128-byte swizzle row
 
+// One operand tile of ROWS rows x BK into a stage slot.  K-major: one box
+// {BK, ROWS} at (k, row).  MN-major: ROWS/64 boxes {64 rows, BK} at (row + 64j,
+// k), 8 KB apart (the chunks sw128_mnmajor_desc expects).  Either way the slot
+// receives ROWS x 128 bytes.  PAIR: the completion is signalled on the
+// leader CTA's barrier (bar is a cluster address).  Only tiles of whole
+// 64-row chunks can be MN-major (the host never sets mn for others).
+template <int ROWS, bool PAIR = false>
+__device__ __forceinline__ void load_operand(uint32_t slot, const CUtensorMap* map, uint32_t bar, bool mn, int k,
+                                             int row, int b)
+{
+    if (ROWS % 64 == 0 && mn) {
+#pragma unroll
+        for (int j = 0; j < ROWS / 64; ++j) {
+            if (PAIR)
+                tma_load_3d_pair(slot + j * kMnChunkBytes, map, bar, row + 64 * j, k, b);
+            else
+                tma_load_3d(slot + j * kMnChunkBytes, map, bar, row + 64 * j, k, b);
+        }
+    } else {
+        if (PAIR)
+            tma_load_3d_pair(slot, map, bar, k, row, b);
+        else
+            tma_load_3d(slot, map, bar, k, row, b);
+    }
+}
+
+// The same tile, fetched into L2 only.
+template <int ROWS>
+__device__ __forceinline__ void prefetch_operand(const CUtensorMap* map, bool mn, int k, int row, int b)
+{
+    if (ROWS % 64 == 0 && mn) {
+#pragma unroll
+        for (int j = 0; j < ROWS / 64; ++j)
+            tma_prefetch_l2_3d(map, row + 64 * j, k, b);
+    } else {
+        tma_prefetch_l2_3d(map, k, row, b);
+    }
+}
+
 // Tile index -> (batch, x tile, y tile).  Within a batch, tiles are taken in
 // groups of group_x x-tiles, column by column, so CTAs running at the same time
 // share X rows and Y rows in L2.
@@ -107,21 +146,28 @@ struct WorkIter {
     }
 };
 
-// Bounded wait.  Returns false if the limit passed or another role aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
-                                             unsigned long long limit)
+// The slow path of wait_bounded, kept out of line so the issue loops that call
+// it stay short: sleep in try_wait until the phase completes, giving up when
+// another thread has raised the abort flag or after `limit` cycles.
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                       unsigned long long limit)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 1000000u))
             return true;
         if (*abort_flag)
             return false;
         if (static_cast<unsigned long long>(clock64() - t0) > limit)
             return false;
     }
+}
+
+// Bounded wait.  Returns false if the limit passed or another role aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                             unsigned long long limit)
+{
+    return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, limit);
 }
 
 __device__ __forceinline__ void raise_timeout(const TcParams& p, volatile int* abort_flag)

@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w0.next(s0)) {
             const int n = s0.kb1 - s0.kb0 < STAGES ? s0.kb1 - s0.kb0 : STAGES;
             for (int i = 0; i < n; ++i) {
-                tma_prefetch_l2_3d(&tmx, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
-                tma_prefetch_l2_3d(&tmy, (s0.kb0 + i) * BK, s0.y0, s0.b * p.y_bmul);
+                prefetch_operand<XR>(&tmx, p.x_mn, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
+                prefetch_operand<BN>(&tmy, p.y_mn, (s0.kb0 + i) * BK, s0.y0, s0.b * p.y_bmul);
             }
         }
     }
@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
                         mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES);
-                        tma_load_3d(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * BK, s.x0, s.b * p.x_bmul);
-                        tma_load_3d(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * BK, s.y0, s.b * p.y_bmul);
+                        load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * BK, s.x0,
+                                         s.b * p.x_bmul);
+                        load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * BK, s.y0,
+                                         s.b * p.y_bmul);
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -165,11 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // An MMA issue blocks until the tensor core accepts it, about one MMA
+        // ahead of the one executing, so the work between k-blocks is kept to
+        // additions (stage addresses, descriptor words) and the waits' fast path.
         if (lane == 0) {
+            const uint32_t idesc = C::IDESC | p.idesc_bits;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+            const DescWords dx = desc_words(smem_u32(xs), p.x_mn != 0);
+            const DescWords dy = desc_words(smem_u32(ys), p.y_mn != 0);
+            uint32_t fa = full0, ea = empty0, xlo = dx.lo, ylo = dy.lo;
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
-            bool first = true, ok = true;
+            bool skip_release = p.fault == 2 && blockIdx.x == 0;  // test hook: lose one stage release
+            bool ok = true;
             WorkIter<BN> w(p);
             Seg s;
             while (ok && w.next(s)) {
@@ -182,26 +193,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
-                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                    if (!wait_bounded(fa, phase, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xa = smem_u32(xs + stage * C::X_BYTES);
-                    const uint32_t ya = smem_u32(ys + stage * C::Y_BYTES);
+                    tc_mma_f16_w(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        tc_mma_f16(d_tmem, sw128_kmajor_desc(xa + k * 32), sw128_kmajor_desc(ya + k * 32),
-                                   C::IDESC | p.ab_fmt, (kb > s.kb0 || k > 0) ? 1u : 0u);
-                    }
-                    const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
-                    first = false;
-                    if (!skip)
-                        tc_commit(smem_u32(&empty[stage]));
+                    for (int k = 1; k < BK / 16; ++k)
+                        tc_mma_f16_w(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi, idesc, 1u);
+                    if (!skip_release)
+                        tc_commit(ea);
+                    skip_release = false;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
+                        fa = full0;
+                        ea = empty0;
+                        xlo = dx.lo;
+                        ylo = dy.lo;
+                    } else {
+                        fa += 8;
+                        ea += 8;
+                        xlo += C::X_BYTES >> 4;
+                        ylo += C::Y_BYTES >> 4;
                     }
                 }
                 if (!ok)

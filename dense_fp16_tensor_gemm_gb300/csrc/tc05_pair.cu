@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const int n = s0.kb1 - s0.kb0 < kStages ? s0.kb1 - s0.kb0 : kStages;
             const int yb = s0.y0 + static_cast<int>(rank) * (PBN / 2);
             for (int i = 0; i < n; ++i) {
-                tma_prefetch_l2_3d(&tma, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
-                tma_prefetch_l2_3d(&tmb, (s0.kb0 + i) * BK, yb, s0.b * p.y_bmul);
+                prefetch_operand<BM>(&tma, p.x_mn, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
+                prefetch_operand<PBN / 2>(&tmb, p.y_mn, (s0.kb0 + i) * BK, yb, s0.b * p.y_bmul);
             }
         }
     }
@@ -308,10 +308,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                             filled |= 1u << stage;
                             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        tma_load_3d_pair(smem_u32(as + stage * A_BYTES), &tma, fb_leader, kb * BK, s.x0,
-                                         s.b * p.x_bmul);
-                        tma_load_3d_pair(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, kb * BK, yb,
-                                         s.b * p.y_bmul);
+                        load_operand<BM, true>(smem_u32(as + stage * A_BYTES), &tma, fb_leader, p.x_mn, kb * BK,
+                                               s.x0, s.b * p.x_bmul);
+                        load_operand<PBN / 2, true>(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, p.y_mn,
+                                                    kb * BK, yb, s.b * p.y_bmul);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -334,10 +334,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader)
         if (lane == 0 && leader) {
+            // The tensor core accepts about one MMA beyond the one it is
+            // executing, and an MMA issue blocks until accepted, so whatever this
+            // thread does between one k-block's last MMA and the next k-block's
+            // first must fit in one MMA's time (~128 cycles at N = 256).  The
+            // loop therefore steps stage addresses and descriptor words by
+            // additions, and leaves the line only when a wait has to sleep.
+            const uint32_t idesc = C::IDESC | p.idesc_bits;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+            const DescWords da = desc_words(smem_u32(as), p.x_mn != 0);
+            const DescWords db = desc_words(smem_u32(bs), p.y_mn != 0);
+            uint32_t fa = full0, ea = empty0, alo = da.lo, blo = db.lo;
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
-            bool first = true, ok = true;
+            bool skip_release = p.fault == 2 && blockIdx.x == 0;  // test hook: lose one stage release
+            bool ok = true;
             PairIter<PBN> w(p, 0);
             Seg s;
             while (ok && w.next(s)) {
@@ -350,27 +362,31 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccStride);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
-                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                    if (!wait_bounded(fa, phase, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t aa = smem_u32(as + stage * A_BYTES);
-                    const uint32_t ba = smem_u32(bs + stage * B_BYTES);
+                    tc_mma_f16_pair_w(d_tmem, alo, da.hi, blo, db.hi, idesc, kb != s.kb0);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        tc_mma_f16_pair(d_tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32),
-                                        C::IDESC | p.ab_fmt,
-                                        (kb > s.kb0 || k > 0) ? 1u : 0u);
-                    }
-                    const bool skip = p.fault == 2 && blockIdx.x == 0 && first;
-                    first = false;
-                    if (!skip)
-                        tc_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
+                    for (int k = 1; k < BK / 16; ++k)
+                        tc_mma_f16_pair_w(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi, idesc, 1u);
+                    if (!skip_release)
+                        tc_commit_pair_mc(ea, 0x3);
+                    skip_release = false;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
+                        fa = full0;
+                        ea = empty0;
+                        alo = da.lo;
+                        blo = db.lo;
+                    } else {
+                        fa += 8;
+                        ea += 8;
+                        alo += A_BYTES >> 4;
+                        blo += B_BYTES >> 4;
                     }
                 }
                 if (!ok)

@@ -133,6 +133,48 @@ gemm_status_t gemm_nt_batched_ex(const void *A, const void *B, void *Out,
                                  int64_t batch, int64_t strideA, int64_t strideB,
                                  int64_t strideO, gemm_path_t path, gemm_stream_t stream);
 
+/* Storage order of one operand of gemm_nt_batched_major.  The operand is the
+ * logical (rows, K) matrix of the product (A: rows = M; B: rows = N).
+ *   GEMM_MAJOR_K : element (r, k) at base[r*ld + k], ld >= K  -- row-major (rows, K),
+ *                  the layout of every other entry point;
+ *   GEMM_MAJOR_MN: element (r, k) at base[k*ld + r], ld >= rows -- row-major (K, rows),
+ *                  i.e. the operand's transpose stored row-major. */
+typedef enum gemm_major {
+    GEMM_MAJOR_K = 0,
+    GEMM_MAJOR_MN = 1
+} gemm_major_t;
+
+/*
+ * The product Out[b] = A[b] @ B[b].T with each operand stored K-major or
+ * MN-major: with B MN-major, B is given as a row-major (K, N) matrix and the
+ * call computes the plain row-major product A @ B ("NN"); with A MN-major too,
+ * A is given as (K, M) and the call computes A.T @ B ("TN").  "Warp Matrix
+ * Instructions" ("Other Fragment Shapes and Transfers") names ldmatrix's
+ * .trans form, and "copy -> ldstmatrix" ("Algorithm" step 3) selects it for a
+ * column-major shared tile whose column stride is a multiple of 8 elements:
+ * the warp kernel stages an MN-major operand that way.  The tcgen05 kernels
+ * (the pages show them K-major only) read it through the instruction
+ * descriptor's transpose bit and an MN-major 128-byte-swizzled shared-memory
+ * descriptor, as the PTX ISA defines them.
+ *
+ * Arguments as gemm_nt_batched_ex, plus a_major and b_major; lda and ldb are
+ * the row pitches of the stored matrices (ld >= K for K-major, ld >= M or N
+ * for MN-major) and strideA / strideB the batch strides, all in elements.
+ * gemm_nt_batched_ex(...) equals this call with both operands GEMM_MAJOR_K.
+ * The tensor-core kernels need 16-byte aligned A/B bases and ld, strides that
+ * are multiples of 8 elements (else the warp kernel runs, as for K-major).
+ * An MN-major operand on the CTA-pair kernel always uses 256-wide tiles, and
+ * the skinny kernel's row split (an even share of rows per CTA) is K-major
+ * only.  Any other major value: GEMM_ERR_INVALID_VALUE.
+ */
+gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const void *B,
+                                    gemm_major_t b_major, void *Out,
+                                    gemm_dtype_t ab_type, gemm_dtype_t out_type,
+                                    int64_t M, int64_t N, int64_t K,
+                                    int64_t lda, int64_t ldb, int64_t ldo,
+                                    int64_t batch, int64_t strideA, int64_t strideB,
+                                    int64_t strideO, gemm_path_t path, gemm_stream_t stream);
+
 /*
  * Host-side pipeline for callers whose data lives in host memory: copies A and
  * B (packed: lda = ldb = K, strideA = M*K, strideB = N*K) from host to the

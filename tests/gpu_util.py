@@ -77,3 +77,85 @@ def sample_indices(batch, M, N, n_random, rows=(), cols=(), seed=0):
             c = c % N
             bs.append(np.full(M, b)); is_.append(np.arange(M)); js.append(np.full(M, c))
     return np.concatenate(bs), np.concatenate(is_), np.concatenate(js)
+
+
+TORCH_DTYPES = ("f16", "bf16", "f32")
+
+
+def torch_dtype(name):
+    import torch
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+def dtype_code(name):
+    return {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}[name]
+
+
+def to_device(bits, ab, ld=None, offset=0):
+    """(batch, rows, cols) host array of 16-bit values (float16, or uint16
+    bfloat16 patterns) -> device tensor of dtype `ab` with row pitch `ld`;
+    padding and the `offset` elements before the base hold NaN.  Returns
+    (tensor, base pointer)."""
+    import torch
+    x = np.ascontiguousarray(bits).view(np.int16)
+    batch, rows, cols = x.shape
+    ld = ld or cols
+    t = torch.full((offset + batch * rows * ld,), float("nan"), dtype=torch_dtype(ab))
+    t[offset:].view(batch, rows, ld)[:, :, :cols] = torch.from_numpy(x).view(torch_dtype(ab))
+    t = t.cuda()
+    return t, t.data_ptr() + 2 * offset
+
+
+def run_general(A, B, ab, out, path, a_mn=False, b_mn=False, lda=None, ldb=None, ldo=None, out_offset=0,
+                a_offset=0):
+    """Out = A @ B.T through gemm_nt_batched_major, A (batch, M, K) and B
+    (batch, N, K) the logical operands; an MN-major operand is handed to the
+    library as its transpose (batch, K, rows), row pitch lda / ldb (default:
+    the stored row length, rounded up to 8 for an MN-major operand).  Returns Out
+    as float64 numpy (batch, M, N) after checking that nothing beyond column N
+    or before the Out base was written."""
+    import torch
+    batch, M, K = A.shape
+    N = B.shape[1]
+    As = np.ascontiguousarray(np.swapaxes(A, 1, 2)) if a_mn else A
+    Bs = np.ascontiguousarray(np.swapaxes(B, 1, 2)) if b_mn else B
+    # default pitch of an MN-major operand: its row length (M or N) rounded up
+    # to 8 elements, the alignment the tensor-core kernels need
+    lda = lda or ((As.shape[2] + 7) // 8 * 8 if a_mn else As.shape[2])
+    ldb = ldb or ((Bs.shape[2] + 7) // 8 * 8 if b_mn else Bs.shape[2])
+    ldo = ldo or N
+    a, pa = to_device(As, ab, lda, a_offset)
+    b, pb = to_device(Bs, ab, ldb)
+    o = torch.full((out_offset + batch * M * ldo,), float("nan"), dtype=torch_dtype(out), device="cuda")
+    esize = o.element_size()
+    stream = torch.cuda.current_stream().cuda_stream
+    gnt.gemm_nt_batched_major(pa, gnt.Major.MN if a_mn else gnt.Major.K, pb, gnt.Major.MN if b_mn else gnt.Major.K,
+                              o.data_ptr() + esize * out_offset, dtype_code(ab), dtype_code(out), M, N, K,
+                              lda, ldb, ldo, batch, As.shape[1] * lda, Bs.shape[1] * ldb, M * ldo, path, stream)
+    gnt.gemm_nt_check(stream)
+    host = o.double().cpu().numpy()
+    assert np.all(np.isnan(host[:out_offset])), "kernel wrote before the Out base"
+    host = host[out_offset:].reshape(batch, M, ldo)
+    if ldo > N:
+        assert np.all(np.isnan(host[:, :, N:])), "kernel wrote past column N"
+    return host[:, :, :N]
+
+
+def check_tol(out, ref, absdot, out_dtype, what):
+    """Elementwise parity within oracle.within_tolerance for Out's type."""
+    assert not np.isnan(out).any(), "%s: unwritten elements" % what
+    ok = oracle.within_tolerance(out, ref, absdot, out_dtype)
+    if not ok.all():
+        i = tuple(np.argwhere(~ok)[0])
+        raise AssertionError("%s: %d of %d out of tolerance; first %s out=%r ref=%r absdot=%r"
+                             % (what, int((~ok).sum()), ok.size, i, out[i], ref[i], absdot[i]))
+
+
+def check_exact(out, ref, out_dtype, what):
+    """Out equals the oracle's rounding of an exact result into Out's type."""
+    want = oracle.round_output(ref, out_dtype)
+    bad = out != want
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError("%s: %d of %d differ from the rounded exact result; first %s out=%r want=%r"
+                             % (what, int(bad.sum()), bad.size, i, out[i], want[i]))

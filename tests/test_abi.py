@@ -129,3 +129,25 @@ def test_dtype_validation(lib):
     # a 16-bit Out of 8x8 ends 128 bytes after its base: ending inside B overlaps
     assert f(FAKE_A, FAKE_B, FAKE_B - 120, D.BF16, D.F16, *base) == gnt.Status.OVERLAP
     assert f(FAKE_A, FAKE_B, FAKE_O, D.BF16, D.F16, 0, 8, 8, 8, 8, 8, 1, 64, 64, 64, 0, None) == 0
+
+
+def test_major_validation(lib):
+    """gemm_nt_batched_major: an MN-major operand's pitch counts its stored rows'
+    length (M or N), unknown majors are rejected, and the overlap check uses the
+    stored extent."""
+    f = lib.gemm_nt_batched_major
+    D, Mj = gnt.DType, gnt.Major
+    M, N, K = 16, 24, 8
+    tail = (D.F16, D.F32, M, N, K)
+    # A MN-major (stored K x M): lda must be >= M, not just >= K
+    assert f(FAKE_A, Mj.MN, FAKE_B, Mj.K, FAKE_O, *tail, 8, 8, N, 1, 0, 0, 0, 0, None) == gnt.Status.INVALID_VALUE
+    # B MN-major (stored K x N): ldb >= N
+    assert f(FAKE_A, Mj.K, FAKE_B, Mj.MN, FAKE_O, *tail, 8, 16, N, 1, 0, 0, 0, 0, None) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, 2, FAKE_B, Mj.K, FAKE_O, *tail, 8, 8, N, 1, 0, 0, 0, 0, None) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, Mj.K, FAKE_B, -1, FAKE_O, *tail, 8, 8, N, 1, 0, 0, 0, 0, None) == gnt.Status.INVALID_VALUE
+    # stored A is K x M = 8 x 16 fp16 = 256 bytes: Out 200 bytes after it overlaps
+    assert f(FAKE_A, Mj.MN, FAKE_B, Mj.K, FAKE_A + 200, *tail, 16, 8, N, 1, 0, 0, 0, 0, None) == \
+        gnt.Status.OVERLAP
+    # an empty product returns before any pointer check
+    assert f(FAKE_A, Mj.MN, FAKE_B, Mj.K, FAKE_A + 256, D.F16, D.F32, 0, N, K, 16, 8, N, 1, 0, 0, 0, 0,
+             None) == 0

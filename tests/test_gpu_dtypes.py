@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import dense_fp16_tensor_gemm_gb300 as gnt
+import gpu_util
 import oracle
 import workloads
 
@@ -22,38 +23,20 @@ AB = ["f16", "bf16"]
 OUT = ["f32", "f16", "bf16"]
 
 
-def _torch_dtype(name):
-    import torch
-    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
-
-
-def _code(name):
-    return {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}[name]
+_torch_dtype = gpu_util.torch_dtype
+_code = gpu_util.dtype_code
+_to_device = gpu_util.to_device
+check = gpu_util.check_tol
+check_exact = gpu_util.check_exact
 
 
 def _inputs(batch, M, N, K, ab, dist="normal", seed=0):
-    A, B = workloads.make_inputs(batch, M, N, K, dist, 1.0, seed=seed, dtype=ab)
-    return A, B
-
-
-def _to_device(bits, ab, ld=None, offset=0):
-    """uint16/float16 host array (batch,rows,K) -> device tensor of dtype `ab`
-    with row pitch `ld`; padding and the `offset` elements before the base
-    hold NaN.  Returns (tensor, base pointer)."""
-    import torch
-    x = np.ascontiguousarray(bits).view(np.int16)
-    batch, rows, K = x.shape
-    ld = ld or K
-    t = torch.full((offset + batch * rows * ld,), float("nan"), dtype=_torch_dtype(ab))
-    t[offset:].view(batch, rows, ld)[:, :, :K] = torch.from_numpy(x).view(_torch_dtype(ab))
-    t = t.cuda()
-    return t, t.data_ptr() + 2 * offset
+    return workloads.make_inputs(batch, M, N, K, dist, 1.0, seed=seed, dtype=ab)
 
 
 def run_ex(A, B, ab, out, path, ldo=None, out_offset=0, lda=None, ldb=None):
-    """Out = A @ B.T through gemm_nt_batched_ex; returns Out as float64 numpy
-    of shape (batch, M, N), after checking that nothing beyond column N or
-    before the base was written."""
+    """Out = A @ B.T through gemm_nt_batched_ex (K-major operands); Out as
+    float64 numpy (batch, M, N), nothing written outside it."""
     import torch
     batch, M, K = A.shape
     N = B.shape[1]
@@ -74,24 +57,6 @@ def run_ex(A, B, ab, out, path, ldo=None, out_offset=0, lda=None, ldb=None):
     if ldo > N:
         assert np.all(np.isnan(host[:, :, N:])), "kernel wrote past column N"
     return host[:, :, :N]
-
-
-def check(out, ref, absdot, out_dtype, what):
-    assert not np.isnan(out).any(), "%s: unwritten elements" % what
-    ok = oracle.within_tolerance(out, ref, absdot, out_dtype)
-    if not ok.all():
-        i = tuple(np.argwhere(~ok)[0])
-        raise AssertionError("%s: %d of %d out of tolerance; first %s out=%r ref=%r absdot=%r"
-                             % (what, int((~ok).sum()), ok.size, i, out[i], ref[i], absdot[i]))
-
-
-def check_exact(out, ref, out_dtype, what):
-    want = oracle.round_output(ref, out_dtype)
-    bad = out != want
-    if bad.any():
-        i = tuple(np.argwhere(bad)[0])
-        raise AssertionError("%s: %d of %d differ from the rounded exact result; first %s out=%r want=%r"
-                             % (what, int(bad.sum()), bad.size, i, out[i], want[i]))
 
 
 @pytest.mark.parametrize("out", OUT)
