@@ -48,10 +48,10 @@ L2_BYTES = 129 * 1024 * 1024
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1075181056 + 248084736, "661fcf4aeb053738"),
-    "square_4096": (91189504 + 34833152, "661fcf4aeb053738"),
-    "ragged_batch16_3001x2047x1000": (170580480 + 341193216, "661fcf4aeb053738"),
-    "skinny_64x16384x8192": (269558272 + 3643392, "adfe06414e4704fd"),
+    "square_8192": (1091781888 + 249862912, "c31affbf9a141447"),
+    "square_4096": (91180544 + 35043840, "c31affbf9a141447"),
+    "ragged_batch16_3001x2047x1000": (171515904 + 342115840, "c31affbf9a141447"),
+    "skinny_64x16384x8192": (269560832 + 3447808, "def5b1e2ec4e9763"),
 }
 
 
