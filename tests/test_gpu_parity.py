@@ -44,10 +44,11 @@ def test_small_shapes(path, M, N, K):
 
 # Swapped-operand shapes covering its three work distributions on a 152-SM
 # GB300: whole tiles (few k-blocks), stream-K (few tiles, long K) and the row
-# split (64..128 rows of N per CTA).
+# split (64..128 rows of N per CTA: N = 9728 and 19456 are its two ends).
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 64), (7, 2000, 136), (64, 4096, 520), (33, 1500, 1000),
                                    (16, 4096, 8192), (64, 16384, 256), (50, 12001, 200),
-                                   (3, 19456, 72)])
+                                   (3, 19456, 72), (1, 9728, 512), (32, 9728, 264), (33, 19456, 136),
+                                   (64, 13000, 1000)])
 def test_skinny_shapes(M, N, K):
     A, B = workloads.make_inputs(0, M, N, K, "normal", 0.02, seed=M + N + K)
     ref, absdot = oracle.gemm_nt(A, B)
