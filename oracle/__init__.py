@@ -15,7 +15,8 @@ accurate as any fp32 implementation.
 
 The same product for bfloat16 inputs ("Warp Matrix Instructions", "Other
 Fragment Shapes and Transfers") is ``gemm_nt(..., dtype="bf16")``, with inputs
-given as uint16 bit patterns.
+given as uint16 bit patterns; for the 8-bit floats E4M3 and E5M2 it is
+``dtype="e4m3"`` / ``"e5m2"`` with uint8 bit patterns.
 
 Parity rule used by the tests (stated once here so every test uses the same):
     |Out - ref| <= 1e-3 * absdot + 1e-6    elementwise, and
@@ -37,6 +38,16 @@ def _u16(x):
         x = x.view(np.uint16)
     if x.dtype != np.uint16:
         raise TypeError("oracle inputs must be float16 (or their uint16 bit patterns)")
+    return np.ascontiguousarray(x)
+
+
+F8_TYPES = ("e4m3", "e5m2")
+
+
+def _u8(x):
+    x = np.asarray(x)
+    if x.dtype != np.uint8:
+        raise TypeError("8-bit float inputs are given as uint8 bit patterns")
     return np.ascontiguousarray(x)
 
 
@@ -72,6 +83,16 @@ class Oracle:
             lib.oracle_gemm_nt_bf16.restype = None
             lib.oracle_gemm_nt_sampled_bf16.argtypes = lib.oracle_gemm_nt_sampled.argtypes
             lib.oracle_gemm_nt_sampled_bf16.restype = None
+        self.has_f8 = hasattr(lib, "oracle_gemm_nt_f8")
+        if self.has_f8:
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_f8_to_double_array.argtypes = [u8p, f64p, i64, ctypes.c_int]
+            lib.oracle_f8_to_double_array.restype = None
+            lib.oracle_gemm_nt_f8.argtypes = [u8p, u8p, f64p, f64p] + [i64] * 10 + [ctypes.c_int, ctypes.c_int]
+            lib.oracle_gemm_nt_f8.restype = None
+            lib.oracle_gemm_nt_sampled_f8.argtypes = [u8p, u8p, i64p, i64p, i64p, i64, i64, i64, i64, i64, i64,
+                                                      f64p, f64p, ctypes.c_int, ctypes.c_int]
+            lib.oracle_gemm_nt_sampled_f8.restype = None
         self.lib = lib
         self.path = path
 
@@ -94,13 +115,23 @@ class Oracle:
         self.lib.oracle_bf16_to_double_array(_ptr(b, ctypes.c_uint16), _ptr(out, ctypes.c_double), b.size)
         return out
 
+    def f8_to_double(self, bits, dtype: str) -> np.ndarray:
+        """Decode 8-bit float patterns (uint8; dtype "e4m3" or "e5m2") to float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_f8_to_double_array(_ptr(b, ctypes.c_uint8), _ptr(out, ctypes.c_double), b.size,
+                                           1 if dtype == "e5m2" else 0)
+        return out
+
     def gemm_nt(self, A, B, nthreads: int = 0, dtype: str = "f16"):
         """Full product.  A: (M,K) or (batch,M,K); B: (N,K) or (batch,N,K);
-        float16 arrays, or uint16 bit patterns of fp16 (dtype "f16") or
-        bfloat16 (dtype "bf16").
+        float16 arrays, or bit patterns: uint16 for fp16 (dtype "f16") and
+        bfloat16 ("bf16"), uint8 for the 8-bit floats "e4m3" and "e5m2".
 
         Returns (ref, absdot), float64 arrays of shape (M,N) or (batch,M,N).
         """
+        if dtype in F8_TYPES:
+            return self._gemm_nt_f8(A, B, nthreads, dtype)
         fn = self._fn("oracle_gemm_nt", dtype)
         a, b = _u16(A), _u16(B)
         squeeze = a.ndim == 2
@@ -119,6 +150,26 @@ class Oracle:
             ref, absdot = ref[0], absdot[0]
         return ref, absdot
 
+    def _gemm_nt_f8(self, A, B, nthreads, dtype):
+        if not self.has_f8:
+            raise ValueError("this oracle build has no 8-bit float product")
+        a, b = _u8(A), _u8(B)
+        squeeze = a.ndim == 2
+        if squeeze:
+            a, b = a[None], b[None]
+        if a.ndim != 3 or b.ndim != 3 or a.shape[0] != b.shape[0] or a.shape[2] != b.shape[2]:
+            raise ValueError("shape mismatch: A %s, B %s" % (np.shape(A), np.shape(B)))
+        batch, M, K = a.shape
+        N = b.shape[1]
+        ref = np.empty((batch, M, N), dtype=np.float64)
+        absdot = np.empty((batch, M, N), dtype=np.float64)
+        self.lib.oracle_gemm_nt_f8(_ptr(a, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(ref, ctypes.c_double),
+                                   _ptr(absdot, ctypes.c_double), batch, M, N, K, K, K, N, M * K, N * K, M * N,
+                                   int(nthreads), 1 if dtype == "e5m2" else 0)
+        if squeeze:
+            ref, absdot = ref[0], absdot[0]
+        return ref, absdot
+
     def _fn(self, name, dtype):
         if dtype == "f16":
             return getattr(self.lib, name)
@@ -132,7 +183,8 @@ class Oracle:
         A, B as in :meth:`gemm_nt` (2-D inputs take bidx = 0).  Returns
         (ref, absdot), float64 arrays of length len(iidx).
         """
-        a, b = _u16(A), _u16(B)
+        f8 = dtype in F8_TYPES
+        a, b = (_u8(A), _u8(B)) if f8 else (_u16(A), _u16(B))
         if a.ndim == 2:
             a, b = a[None], b[None]
         batch, M, K = a.shape
@@ -147,6 +199,13 @@ class Oracle:
             raise IndexError("sample index out of range")
         ref = np.empty(ii.shape, dtype=np.float64)
         absdot = np.empty(ii.shape, dtype=np.float64)
+        if f8:
+            self.lib.oracle_gemm_nt_sampled_f8(
+                _ptr(a, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(bb, ctypes.c_int64),
+                _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, M * K, N * K,
+                _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double), int(nthreads),
+                1 if dtype == "e5m2" else 0)
+            return ref, absdot
         self._fn("oracle_gemm_nt_sampled", dtype)(
             _ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), _ptr(bb, ctypes.c_int64),
             _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, M * K, N * K,
@@ -175,6 +234,10 @@ def half_to_double(bits):
 
 def bf16_to_double(bits):
     return default().bf16_to_double(bits)
+
+
+def f8_to_double(bits, dtype):
+    return default().f8_to_double(bits, dtype)
 
 
 def gemm_nt(A, B, nthreads: int = 0, dtype: str = "f16"):

@@ -85,6 +85,56 @@ double oracle_bf16_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/*
+ * 8-bit floating point -> double, exact.  E4M3 (the variant without
+ * infinities): 1 sign bit, 4 exponent bits with bias 7, 3 fraction bits;
+ * exponent 0 encodes zero and subnormals (fraction * 2^-9); the pattern with
+ * every exponent and fraction bit set is NaN, so the largest value is 448.
+ * E5M2: 1 sign bit, 5 exponent bits with bias 15, 2 fraction bits, laid out as
+ * the upper byte of an IEEE binary16 (subnormals fraction * 2^-16, exponent 31
+ * Inf or NaN).  ("Blackwell Tensor Cores" names the block-scaled low-precision
+ * MMA forms beside kind::f16; these are their 8-bit element types.)
+ */
+double oracle_e4m3_to_double(uint8_t h)
+{
+    const unsigned sign = (h >> 7) & 1u;
+    const unsigned expo = (h >> 3) & 0xfu;
+    const unsigned frac = h & 0x7u;
+    double v;
+    if (expo == 15 && frac == 7) {
+        v = NAN;
+    } else if (expo == 0) {
+        v = (double)frac * pow2i(-9);
+    } else {
+        /* (1 + frac/8) * 2^(expo-7) = (8 + frac) * 2^(expo-10) */
+        v = (double)(8u + frac) * pow2i((int)expo - 10);
+    }
+    return sign ? -v : v;
+}
+
+double oracle_e5m2_to_double(uint8_t h)
+{
+    const unsigned sign = (h >> 7) & 1u;
+    const unsigned expo = (h >> 2) & 0x1fu;
+    const unsigned frac = h & 0x3u;
+    double v;
+    if (expo == 0) {
+        v = (double)frac * pow2i(-16);
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        /* (1 + frac/4) * 2^(expo-15) = (4 + frac) * 2^(expo-17) */
+        v = (double)(4u + frac) * pow2i((int)expo - 17);
+    }
+    return sign ? -v : v;
+}
+
+void oracle_f8_to_double_array(const uint8_t *src, double *dst, int64_t n, int e5m2)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = e5m2 ? oracle_e5m2_to_double(src[t]) : oracle_e4m3_to_double(src[t]);
+}
+
 void oracle_bf16_to_double_array(const uint16_t *src, double *dst, int64_t n)
 {
     for (int64_t t = 0; t < n; ++t)
@@ -213,6 +263,60 @@ void oracle_gemm_nt_sampled_bf16(const uint16_t *A, const uint16_t *B,
     for (int64_t s = 0; s < n; ++s)
         dot_nt_bf16(A + bidx[s] * sA + iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, ref + s,
                     absdot ? absdot + s : 0);
+}
+
+/* The same product for 8-bit inputs (e5m2 != 0: E5M2, else E4M3): element
+ * (i, j) is the sequential-k double sum of exact products (4 x 4 or 3 x 3
+ * significant bits). */
+static void dot_nt_f8(const uint8_t *a_row, const uint8_t *b_row, int64_t K, int e5m2, double *ref,
+                      double *absdot)
+{
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k]);
+        const double b = e5m2 ? oracle_e5m2_to_double(b_row[k]) : oracle_e4m3_to_double(b_row[k]);
+        const double p = a * b;
+        acc += p;
+        aacc += fabs(p);
+    }
+    *ref = acc;
+    if (absdot)
+        *absdot = aacc;
+}
+
+void oracle_gemm_nt_f8(const uint8_t *A, const uint8_t *B, double *ref, double *absdot,
+                       int64_t batch, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldr,
+                       int64_t sA, int64_t sB, int64_t sR, int nthreads, int e5m2)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bi = 0; bi < batch * M; ++bi) {
+        const int64_t b = bi / M, i = bi % M;
+        const uint8_t *a_row = A + b * sA + i * lda;
+        for (int64_t j = 0; j < N; ++j) {
+            double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
+            dot_nt_f8(a_row, B + b * sB + j * ldb, K, e5m2, ref + b * sR + i * ldr + j, ab);
+        }
+    }
+}
+
+void oracle_gemm_nt_sampled_f8(const uint8_t *A, const uint8_t *B,
+                               const int64_t *bidx, const int64_t *iidx, const int64_t *jidx,
+                               int64_t n, int64_t K, int64_t lda, int64_t ldb,
+                               int64_t sA, int64_t sB, double *ref, double *absdot, int nthreads, int e5m2)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t s = 0; s < n; ++s)
+        dot_nt_f8(A + bidx[s] * sA + iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, e5m2, ref + s,
+                  absdot ? absdot + s : 0);
 }
 
 /* Number of threads the OpenMP runtime would use by default. */

@@ -15,7 +15,8 @@ Sources:
   * "Warp Matrix Instructions", "Other Fragment Shapes and Transfers": the
     same product with bfloat16 inputs.
   * IEEE 754 binary16 (the fp16 format), bfloat16 (the upper 16 bits of an
-    IEEE binary32) and exact rational arithmetic.
+    IEEE binary32), the 8-bit floats E4M3 and E5M2, and exact rational
+    arithmetic.
 """
 from fractions import Fraction
 
@@ -281,6 +282,79 @@ def pin_bf16_integer_exact(orc, seed=22):
     assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A), np.abs(B)).astype(np.float64))
 
 
+def f8_bits(x, dtype):
+    """float64 values that the 8-bit format holds exactly -> uint8 bit patterns
+    (through torch's casts; asserts the values are exact)."""
+    import torch
+    tt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    t = torch.from_numpy(np.asarray(x, dtype=np.float64))
+    q = t.to(tt)
+    assert torch.equal(q.to(torch.float64), t), "value is not an %s" % dtype
+    return q.view(torch.uint8).numpy().copy()
+
+
+def pin_f8_decoders_exhaustive(orc):
+    """All 256 patterns of each 8-bit format: E5M2 against the binary16 it is
+    the upper byte of (numpy), E4M3 against torch's float8_e4m3fn cast."""
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = orc.f8_to_double(bits, "e5m2")
+    want = (bits.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    n = np.isnan(want)
+    assert np.array_equal(np.isnan(got), n) and np.array_equal(got[~n], want[~n]), "e5m2 decoder mismatch"
+    import torch
+    got = orc.f8_to_double(bits, "e4m3")
+    want = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    n = np.isnan(want)
+    assert np.array_equal(np.isnan(got), n), "e4m3 NaN patterns"
+    assert np.array_equal(got[~n], want[~n]), "e4m3 decoder mismatch"
+    assert np.array_equal(np.signbit(got[~n]), np.signbit(want[~n]))
+
+
+def pin_f8_exact_tiny(orc, seed=31):
+    """8-bit products over random tiny shapes, with subnormals and the formats'
+    extremes, against exact rational sums; sampled = full."""
+    rng = np.random.default_rng(seed)
+    specials = {"e4m3": [0.0, -0.0, 2.0 ** -9, -(2.0 ** -6), 448.0, -448.0, 1.125, 3.5, 2.0 ** -7 * 5],
+                "e5m2": [0.0, 2.0 ** -16, -(2.0 ** -14), 57344.0, -1.25, 0.75, 2.0 ** -15 * 3]}
+    for dtype in ("e4m3", "e5m2"):
+        vals = np.array(specials[dtype])
+        for (batch, M, N, K) in ((1, 3, 4, 9), (2, 4, 3, 33)):
+            a = rng.choice(vals, size=(batch, M, K))
+            b = rng.choice(vals, size=(batch, N, K))
+            A, B = f8_bits(a, dtype), f8_bits(b, dtype)
+            ref, absdot = orc.gemm_nt(A, B, dtype=dtype)
+            assert np.all(np.isfinite(ref)), "exact sums here are finite"
+            g = gamma(max(K - 1, 0))
+            for bi in range(batch):
+                for i in range(M):
+                    for j in range(N):
+                        terms = [Fraction(float(a[bi, i, k])) * Fraction(float(b[bi, j, k])) for k in range(K)]
+                        ex = sum(terms, Fraction(0))
+                        exa = sum((abs(t) for t in terms), Fraction(0))
+                        assert abs(Fraction(float(ref[bi, i, j])) - ex) <= Fraction(g) * exa * Fraction(1 + 2 * U) \
+                            + Fraction(2 * U) * abs(ex) + Fraction(1, 2 ** 1074), "%s product" % dtype
+                        assert abs(Fraction(float(absdot[bi, i, j])) - exa) <= Fraction(g + 2 * U) * exa \
+                            + Fraction(1, 2 ** 1074), "%s absdot" % dtype
+            bb = rng.integers(0, batch, size=12)
+            ii = rng.integers(0, M, size=12)
+            jj = rng.integers(0, N, size=12)
+            sref, sabs = orc.gemm_nt_sampled(A, B, bb, ii, jj, dtype=dtype)
+            assert np.array_equal(sref, ref[bb, ii, jj]) and np.array_equal(sabs, absdot[bb, ii, jj])
+
+
+def pin_f8_integer_exact(orc, seed=32):
+    """Integers in [-4, 4] are exact in both 8-bit formats; the products and
+    sums are then exact integers."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("e4m3", "e5m2"):
+        A = rng.integers(-4, 5, size=(2, 11, 97))
+        B = rng.integers(-4, 5, size=(2, 7, 97))
+        ref, absdot = orc.gemm_nt(f8_bits(A, dtype), f8_bits(B, dtype), dtype=dtype)
+        assert np.array_equal(ref, np.einsum("bik,bjk->bij", A, B).astype(np.float64)), "%s integers" % dtype
+        assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A), np.abs(B)).astype(np.float64))
+
+
 ALL_PINS = [pin_decoder_exhaustive, pin_bruteforce_tiny, pin_k1_exact, pin_worked_examples,
             pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled,
-            pin_bf16_decoder_exhaustive, pin_bf16_exact_tiny, pin_bf16_integer_exact]
+            pin_bf16_decoder_exhaustive, pin_bf16_exact_tiny, pin_bf16_integer_exact,
+            pin_f8_decoders_exhaustive, pin_f8_exact_tiny, pin_f8_integer_exact]

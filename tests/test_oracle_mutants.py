@@ -30,6 +30,14 @@ MUTANTS = [
     ("bf16_fraction_width", "const unsigned frac = h & 0x7fu;", "const unsigned frac = h & 0x3fu;"),
     ("bf16_last_term_dropped", "oracle_bf16_to_double(a_row[k]) * oracle_bf16_to_double(b_row[k])",
      "(k + 1 < K ? oracle_bf16_to_double(a_row[k]) * oracle_bf16_to_double(b_row[k]) : 0.0)"),
+    ("e4m3_exponent_bias", "(int)expo - 10", "(int)expo - 9"),
+    ("e4m3_subnormal_scale", "v = (double)frac * pow2i(-9);", "v = (double)frac * pow2i(-10);"),
+    ("e4m3_nan_as_value", "if (expo == 15 && frac == 7) {", "if (expo == 15 && frac == 8) {"),
+    ("e5m2_exponent_bias", "(int)expo - 17", "(int)expo - 16"),
+    ("f8_formats_swapped", "const double a = e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k]);",
+     "const double a = e5m2 ? oracle_e4m3_to_double(a_row[k]) : oracle_e5m2_to_double(a_row[k]);"),
+    ("f8_abs_missing", "        aacc += fabs(p);\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8",
+     "        aacc += p;\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8"),
     ("bf16_sampled_ij_swapped", "iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, ref + s,\n",
      "jidx[s] * lda, B + bidx[s] * sB + iidx[s] * ldb, K, ref + s,\n"),
 ]

@@ -63,3 +63,16 @@ def test_bf16_inputs_follow_the_same_draws():
     assert np.array_equal(dec(a), a16.astype(np.float32)) and np.array_equal(dec(b), b16.astype(np.float32))
     a, _ = workloads.make_inputs(0, 64, 8, 100, "normal", 0.02, seed=7, dtype="bf16")
     assert a.shape == (64, 100) and abs(float(dec(a).std()) - 0.02) < 2e-3
+
+
+def test_f8_inputs_follow_the_same_draws():
+    torch = __import__("pytest").importorskip("torch")
+    for dtype, tt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        a16, _ = workloads.make_inputs(0, 20, 10, 40, "int4", seed=4)
+        a, b = workloads.make_inputs(0, 20, 10, 40, "int4", seed=4, dtype=dtype)
+        assert a.dtype == np.uint8 and a.shape == (20, 40) and b.shape == (10, 40)
+        dec = torch.from_numpy(a.copy()).view(tt).to(torch.float64).numpy()
+        assert np.array_equal(dec, a16.astype(np.float64))
+        x, _ = workloads.make_inputs(0, 64, 8, 256, "normal", 1.0, seed=5, dtype=dtype)
+        v = torch.from_numpy(x.copy()).view(tt).to(torch.float64).numpy()
+        assert np.isfinite(v).all() and abs(float(v.std()) - 1.0) < 0.1

@@ -20,6 +20,11 @@ bfloat16 inputs (``dtype="bf16"``) come from the same draws: each float64 value
 is cast to float32 (numpy, round to nearest even) and the float32 is rounded to
 its upper 16 bits, again to nearest with ties to even.  They are returned as
 uint16 bit patterns (numpy has no bfloat16 type).
+
+8-bit float inputs (``dtype="e4m3"`` or ``"e5m2"``) also come from the same
+draws: float64 -> float32 (numpy), then torch's float32 -> float8 cast (round
+to nearest even; every drawn value lies inside both formats' ranges).  They are
+returned as uint8 bit patterns.
 """
 from dataclasses import dataclass
 
@@ -110,13 +115,37 @@ def _draw_bf16(rng, n, dist, sigma):
     return out
 
 
+def _draw_f8(dtype):
+    import torch
+    tt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[dtype]
+
+    def draw(rng, n, dist, sigma):
+        out = np.empty(n, dtype=np.uint8)
+        if dist == "int4":
+            v = rng.integers(-4, 5, size=n, dtype=np.int8).astype(np.float32)
+            out[:] = torch.from_numpy(v).to(tt).view(torch.uint8).numpy()
+            return out
+        for s in range(0, n, _CHUNK):
+            m = min(_CHUNK, n - s)
+            if dist == "uniform":
+                v = rng.uniform(-1.0, 1.0, size=m)
+            elif dist == "normal":
+                v = sigma * rng.standard_normal(size=m)
+            else:
+                raise ValueError("unknown distribution %r" % dist)
+            out[s:s + m] = torch.from_numpy(v.astype(np.float32)).to(tt).view(torch.uint8).numpy()
+        return out
+    return draw
+
+
 def make_inputs(batch, M, N, K, dist="uniform", sigma=1.0, seed=0, dtype="f16"):
     """Return (A, B) of shape (batch,M,K), (batch,N,K) (or (M,K), (N,K) when
     batch == 0 is passed to mean "unbatched"): float16 arrays for dtype "f16",
-    uint16 bfloat16 bit patterns for dtype "bf16"."""
+    uint16 bfloat16 bit patterns for dtype "bf16", uint8 patterns for "e4m3"
+    and "e5m2"."""
     rng = np.random.default_rng(seed)
     nb = max(batch, 1)
-    draw = {"f16": _draw, "bf16": _draw_bf16}[dtype]
+    draw = {"f16": _draw, "bf16": _draw_bf16}[dtype] if dtype in ("f16", "bf16") else _draw_f8(dtype)
     A = draw(rng, nb * M * K, dist, sigma).reshape(nb, M, K)
     B = draw(rng, nb * N * K, dist, sigma).reshape(nb, N, K)
     if batch == 0:
