@@ -249,8 +249,8 @@ def main():
                     help="MN: A handed to the library as its transpose, (K, M) row-major")
     ap.add_argument("--b-major", default="K", choices=["K", "MN"],
                     help="MN: B handed to the library as its transpose, (K, N) row-major (the NN product)")
-    ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16"],
-                    help="element type of A and B (bf16: the same draws rounded to bfloat16)")
+    ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16", "e4m3", "e5m2"],
+                    help="element type of A and B (bf16, e4m3, e5m2: the same draws rounded to that type)")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of Out (16-bit: fp32 accumulator rounded to nearest even)")
     args = ap.parse_args()
@@ -280,16 +280,21 @@ def main():
     default_types = args.ab_dtype == "f16" and args.out_dtype == "f32"
     a_mn, b_mn = args.a_major == "MN", args.b_major == "MN"
     default_layout = not a_mn and not b_mn
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    codes = {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+           "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    codes = {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32,
+             "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2}
+    f8 = args.ab_dtype in ("e4m3", "e5m2")
+    ab_es = 1 if f8 else 2
+    raw = np.uint8 if f8 else np.int16
     A, B = workloads.workload_inputs(w.name, args.ab_dtype)
     batched = A.ndim == 3
     # stored operands: an MN-major one is its transpose, row-major
     As = np.ascontiguousarray(np.swapaxes(A, -1, -2)) if a_mn else A
     Bs = np.ascontiguousarray(np.swapaxes(B, -1, -2)) if b_mn else B
     lda, ldb = As.shape[-1], Bs.shape[-1]
-    a = torch.from_numpy(As.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
-    b = torch.from_numpy(Bs.view(np.int16)).view(tdt[args.ab_dtype]).cuda()
+    a = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).cuda()
+    b = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).cuda()
     out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=tdt[args.out_dtype],
                       device="cuda")
     stream = torch.cuda.current_stream()
@@ -311,8 +316,8 @@ def main():
                                    codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB, sO,
                                    path, sh)
 
-    # algorithmic bytes: A and B read once (2 bytes each), Out written once
-    alg_bytes = float(w.batch) * (2 * w.M * w.K + 2 * w.N * w.K + out.element_size() * w.M * w.N)
+    # algorithmic bytes: A and B read once, Out written once
+    alg_bytes = float(w.batch) * (ab_es * w.M * w.K + ab_es * w.N * w.K + out.element_size() * w.M * w.N)
     flush = alg_bytes <= 2 * L2_BYTES
     scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
 
@@ -407,21 +412,38 @@ def main():
         al = a.transpose(-1, -2) if a_mn else a
         bt = b if b_mn else b.transpose(-1, -2)
         mm = torch.bmm if batched else torch.mm
-        try:
-            mm(al, bt, out_dtype=torch.float32)
-            cub_fn, cub_out = (lambda: mm(al, bt, out_dtype=torch.float32)), "f32"
-        except (TypeError, RuntimeError, NotImplementedError):
-            cub_fn, cub_out = (lambda: mm(al, bt)), args.ab_dtype
-        cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
-        cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
-                  "call": "torch.%s(A, B^T%s) -> %s Out" % (
-                      "bmm" if batched else "mm", ", out_dtype=float32" if cub_out == "f32" else "", cub_out),
-                  "ratio": (w.flops / (kernel_ms * 1e-3) / 1e12) / (w.flops / (cub_ms * 1e-3) / 1e12)}
+        cub_fn = None
+        if f8:
+            # cuBLAS's 8-bit path: scaled matmul with unit scales (2-D only;
+            # it wants the second operand column-major, which B^T of a
+            # row-major B is)
+            one = torch.ones((), dtype=torch.float32, device="cuda")
+            if not batched and not a_mn and not b_mn:
+                try:
+                    torch._scaled_mm(al, bt, scale_a=one, scale_b=one, out_dtype=torch.float32)
+                    cub_fn, cub_out = (lambda: torch._scaled_mm(al, bt, scale_a=one, scale_b=one,
+                                                                out_dtype=torch.float32)), "f32"
+                except (TypeError, RuntimeError, NotImplementedError):
+                    cub_fn = None
+        else:
+            try:
+                mm(al, bt, out_dtype=torch.float32)
+                cub_fn, cub_out = (lambda: mm(al, bt, out_dtype=torch.float32)), "f32"
+            except (TypeError, RuntimeError, NotImplementedError):
+                cub_fn, cub_out = (lambda: mm(al, bt)), args.ab_dtype
+        if cub_fn is not None:
+            cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
+            cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
+                      "call": ("torch._scaled_mm(A, B^T, unit scales) -> f32 Out" if f8 else
+                               "torch.%s(A, B^T%s) -> %s Out" % ("bmm" if batched else "mm",
+                                                                ", out_dtype=float32" if cub_out == "f32" else "",
+                                                                cub_out)),
+                      "ratio": (w.flops / (kernel_ms * 1e-3) / 1e12) / (w.flops / (cub_ms * 1e-3) / 1e12)}
 
     # ---- end to end through the host-buffer entry point
     e2e_steps = args.e2e_steps or max(3, args.steps // 4)
-    ha = torch.from_numpy(As.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
-    hb = torch.from_numpy(Bs.view(np.int16)).view(tdt[args.ab_dtype]).pin_memory()
+    ha = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
+    hb = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
     ho = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
 
     def e2e_step():
@@ -457,14 +479,19 @@ def main():
 
     peaks = measured_peaks()
     ai = w.flops / alg_bytes
-    tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12
+    # the 8-bit MMA runs at twice the 16-bit rate: its peak is the measured
+    # bf16 one times that nominal ratio (4.5 / 2.25 PFLOP/s dense)
+    tpeak = peaks["tflops"] * (2.0 if f8 else 1.0)
+    tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > tpeak * 1e12
     tr = TRAFFIC.get(w.name)
     traffic = tr[0] if default_types and default_layout and tr and tr[1] == kernel_source_sha(w.name) else None
     if tensor_bound:
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["tflops"], "traffic": traffic,
-                "peak_source": "%s bf16 dense burst (kind::f16 runs fp16 at the bf16 rate)" % peaks["source"]}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": achieved / tpeak, "traffic": traffic,
+                "peak_source": ("%s bf16 dense burst x 2 (the nominal fp8 / bf16 ratio)" % peaks["source"]
+                                if f8 else
+                                "%s bf16 dense burst (kind::f16 runs fp16 at the bf16 rate)" % peaks["source"])}
     else:
         achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -30,6 +30,8 @@ class DType(enum.IntEnum):
     F16 = 0
     BF16 = 1
     F32 = 2
+    E4M3 = 3  # 8-bit floats (A and B only)
+    E5M2 = 4
 
 
 class Major(enum.IntEnum):
@@ -179,11 +181,13 @@ def _matrix_ld(t, name):
 
 def _dtypes(A, B, out, out_dtype):
     import torch
-    codes = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.float32: DType.F32}
-    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
-        raise TypeError("A and B must both be float16 or both bfloat16")
+    codes = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.float32: DType.F32,
+             torch.float8_e4m3fn: DType.E4M3, torch.float8_e5m2: DType.E5M2}
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16, torch.float8_e4m3fn,
+                                             torch.float8_e5m2):
+        raise TypeError("A and B must have the same type: float16, bfloat16, float8_e4m3fn or float8_e5m2")
     dt = out.dtype if out is not None else (out_dtype or torch.float32)
-    if dt not in codes:
+    if dt not in (torch.float32, torch.float16, torch.bfloat16):
         raise TypeError("out must be float32, float16 or bfloat16")
     return codes[A.dtype], codes[dt], dt
 

@@ -172,8 +172,17 @@ struct Problem {
     int64_t b_cols() const { return b_mn() ? N : K; }
 
     int64_t out_esize() const { return out_type == GEMM_DTYPE_F32 ? 4 : 2; }
+    bool is_f8() const { return ab_type == GEMM_DTYPE_E4M3 || ab_type == GEMM_DTYPE_E5M2; }
+    int64_t ab_esize() const { return is_f8() ? 1 : 2; }
+    // k-blocks of one 128-byte stage row: 64 elements of 16 bits, 128 of 8
+    int64_t kblocks() const { return (K + 127 / ab_esize()) / (128 / ab_esize()); }
     int kernel_out() const { return out_type == GEMM_DTYPE_F16 ? kOutF16 : (out_type == GEMM_DTYPE_BF16 ? kOutBF16 : kOutF32); }
-    uint32_t ab_fmt() const { return ab_type == GEMM_DTYPE_BF16 ? ((1u << 7) | (1u << 10)) : 0u; }
+    // A/B format fields of the instruction descriptor (bits 7-9, 10-12): 1 is
+    // bf16 for kind::f16 and E5M2 for kind::f8f6f4; 0 is fp16 or E4M3.
+    uint32_t ab_fmt() const
+    {
+        return (ab_type == GEMM_DTYPE_BF16 || ab_type == GEMM_DTYPE_E5M2) ? ((1u << 7) | (1u << 10)) : 0u;
+    }
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -213,19 +222,22 @@ gemm_status_t validate(const Problem& q)
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.a_rows())) * 2.0 > lim ||
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.b_rows())) * 2.0 > lim)
         return GEMM_ERR_INVALID_VALUE;
-    if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16)
+    if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16 && q.ab_type != GEMM_DTYPE_E4M3 &&
+        q.ab_type != GEMM_DTYPE_E5M2)
         return GEMM_ERR_INVALID_VALUE;
     if (q.out_type != GEMM_DTYPE_F32 && q.out_type != GEMM_DTYPE_F16 && q.out_type != GEMM_DTYPE_BF16)
         return GEMM_ERR_INVALID_VALUE;
-    if (!aligned(q.Out, static_cast<uintptr_t>(q.out_esize())) || (q.K > 0 && (!aligned(q.A, 2) || !aligned(q.B, 2))))
+    if (!aligned(q.Out, static_cast<uintptr_t>(q.out_esize())) ||
+        (q.K > 0 && (!aligned(q.A, static_cast<uintptr_t>(q.ab_esize())) ||
+                     !aligned(q.B, static_cast<uintptr_t>(q.ab_esize())))))
         return GEMM_ERR_INVALID_VALUE;
     if (q.batch > 1 && q.sO < (q.M - 1) * q.ldo + q.N)
         return GEMM_ERR_OVERLAP;
     if (q.K > 0) {
         uintptr_t olo, ohi, alo, ahi, blo, bhi;
         span(q.Out, q.out_esize(), q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
-        span(q.A, 2, q.batch, q.sA, q.a_rows(), q.lda, q.a_cols(), alo, ahi);
-        span(q.B, 2, q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
+        span(q.A, q.ab_esize(), q.batch, q.sA, q.a_rows(), q.lda, q.a_cols(), alo, ahi);
+        span(q.B, q.ab_esize(), q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
         if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
             return GEMM_ERR_OVERLAP;
     }
@@ -238,14 +250,18 @@ bool tma_ok(const Problem& q)
 {
     if (!aligned(q.A, 16) || !aligned(q.B, 16))
         return false;
-    if ((q.lda % 8) || (q.ldb % 8))
+    const int64_t v = 16 / q.ab_esize();  // elements in 16 bytes
+    if ((q.lda % v) || (q.ldb % v))
         return false;
-    if (q.batch > 1 && ((q.sA % 8) || (q.sB % 8)))
+    if (q.batch > 1 && ((q.sA % v) || (q.sB % v)))
+        return false;
+    // 8-bit operands are staged K-major only (MN-major ones run on the warp kernel)
+    if (q.is_f8() && (q.a_mn() || q.b_mn()))
         return false;
     // a batch dimension in a tensor map must step over whole matrices
     if (q.batch > 1 && ((q.sA != 0 && q.sA < q.a_rows() * q.lda) || (q.sB != 0 && q.sB < q.b_rows() * q.ldb)))
         return false;
-    const int64_t lim = int64_t(1) << 39;  // elements of 2 bytes
+    const int64_t lim = (int64_t(1) << 40) / q.ab_esize();  // strides below 2^40 bytes
     if (q.lda >= lim || q.ldb >= lim || q.sA >= lim || q.sB >= lim)
         return false;
     return true;
@@ -269,12 +285,12 @@ struct MapKey {
     const void* base;
     int64_t rows, K, ld, batch, stride;
     int box_rows;
-    bool bf16;
+    int dtype;
     bool mn;
     bool operator==(const MapKey& o) const
     {
         return base == o.base && rows == o.rows && K == o.K && ld == o.ld && batch == o.batch &&
-               stride == o.stride && box_rows == o.box_rows && bf16 == o.bf16 && mn == o.mn;
+               stride == o.stride && box_rows == o.box_rows && dtype == o.dtype && mn == o.mn;
     }
 };
 
@@ -288,12 +304,15 @@ struct MapCache {
 
 thread_local MapCache t_maps;
 
-// An operand of `rows` rows (M or N) and K columns.  K-major: dims {K, rows,
-// batch}, box {64, box_rows}.  MN-major (stored as (K, rows) with pitch ld):
+// An operand of `rows` rows (M or N) and K columns of `dtype` (a gemm_dtype_t
+// input type).  K-major: dims {K, rows, batch}, box {one 128-byte row of K,
+// box_rows}.  MN-major (stored as (K, rows) with pitch ld; 16-bit types only):
 // dims {rows, K, batch}, box {64 rows, 64 K}; box_rows is then ignored.
 bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-                int64_t stride, int box_rows, int* bmul, bool bf16, bool mn)
+                int64_t stride, int box_rows, int* bmul, int dtype, bool mn)
 {
+    const bool f8 = dtype == GEMM_DTYPE_E4M3 || dtype == GEMM_DTYPE_E5M2;
+    const int64_t es = f8 ? 1 : 2;
     auto enc = encode_fn();
     if (!enc)
         return false;
@@ -301,21 +320,24 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
     const int64_t inner = mn ? rows : K, outer = mn ? K : rows;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                           static_cast<cuuint64_t>(batched ? batch : 1)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
-                             static_cast<cuuint64_t>((batched ? stride : outer * ld) * 2)};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(mn ? 64 : box_rows), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es),
+                             static_cast<cuuint64_t>((batched ? stride : outer * ld) * es)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(mn ? 64 : box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     *bmul = batched ? 1 : 0;
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    const CUtensorMapDataType ty = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : (dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUresult r = enc(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
-              int64_t stride, int box_rows, int* bmul, bool bf16 = false, bool mn = false)
+              int64_t stride, int box_rows, int* bmul, int dtype = GEMM_DTYPE_F16, bool mn = false)
 {
-    const MapKey k{base, rows, K, ld, batch, stride, box_rows, bf16, mn};
+    const MapKey k{base, rows, K, ld, batch, stride, box_rows, dtype, mn};
     MapCache& c = t_maps;
     for (int i = 0; i < c.count; ++i) {
         if (c.key[i] == k) {
@@ -324,7 +346,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64
             return true;
         }
     }
-    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul, bf16, mn))
+    if (!encode_map(map, base, rows, K, ld, batch, stride, box_rows, bmul, dtype, mn))
         return false;
     const int slot = c.next;
     c.key[slot] = k;
@@ -388,8 +410,8 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     }
     p.x_box_bytes = xbox * 128;
     CUtensorMap tmx, tmy;
-    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16, x_mn) ||
-        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16, y_mn))
+    if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type, x_mn) ||
+        !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type, y_mn))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.out_type = q.kernel_out();
@@ -403,7 +425,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     p.batch = static_cast<int>(q.batch);
     p.tiles_x = static_cast<int>((xrows + 127) / 128);
     p.tiles_y = static_cast<int>((yrows + bn - 1) / bn);
-    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    p.num_kb = static_cast<int>(q.kblocks());
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
     const int64_t ntiles = tpb * q.batch;
     if (ntiles > INT32_MAX)
@@ -438,7 +460,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         p.mode = kModeTiles;
         grid = static_cast<int>(std::min<int64_t>(ntiles, d.num_sms));
     }
-    if (tc05_launch(tmx, tmy, p, bn, swap, grid, stream) != cudaSuccess)
+    if (tc05_launch(tmx, tmy, p, bn, swap, grid, q.is_f8(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -478,7 +500,7 @@ int pair_plan_width(const Problem& q, const DeviceState& d)
     if (q.b_mn())
         return 256;  // each CTA's half of B must be whole 64-row chunks
     const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
-    if (pair_split(tiles256, static_cast<int>((q.K + 63) / 64), d.max_pairs, q.out_type))
+    if (pair_split(tiles256, static_cast<int>(q.kblocks()), d.max_pairs, q.out_type))
         return 256;
     return pair_tile_width(q.M, q.N, q.batch, d.max_pairs);
 }
@@ -492,9 +514,9 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     TcParams p{};
     const int pbn = pair_plan_width(q, d);
     CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16,
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type,
                   q.a_mn()) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16,
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type,
                   q.b_mn()))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
@@ -509,7 +531,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     p.batch = static_cast<int>(q.batch);
     p.tiles_x = static_cast<int>((q.M + 255) / 256);
     p.tiles_y = static_cast<int>((q.N + pbn - 1) / pbn);
-    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    p.num_kb = static_cast<int>(q.kblocks());
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
     const int64_t ntiles = tpb * q.batch;
     if (ntiles > INT32_MAX)
@@ -555,7 +577,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     // Out rows 32-byte aligned: the epilogue stores without staging
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
                         q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
-    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.is_f8(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -579,11 +601,12 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     p.stride_a = q.sA;
     p.stride_b = q.sB;
     p.stride_o = q.sO;
-    p.vec_a = aligned(q.A, 16) && q.lda % 8 == 0 && (q.batch == 1 || q.sA % 8 == 0);
-    p.vec_b = aligned(q.B, 16) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
+    const uintptr_t v8 = static_cast<uintptr_t>(8 * q.ab_esize());  // 8 elements
+    p.vec_a = aligned(q.A, v8) && q.lda % 8 == 0 && (q.batch == 1 || q.sA % 8 == 0);
+    p.vec_b = aligned(q.B, v8) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
     p.a_mn = q.a_mn() ? 1 : 0;
     p.b_mn = q.b_mn() ? 1 : 0;
-    return mmasync_launch(p, q.ab_type == GEMM_DTYPE_BF16, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return mmasync_launch(p, q.ab_type, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 constexpr int kPipeChunks = 4;
@@ -736,8 +759,8 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     TcParams p{};
     const int pbn = pair_plan_width(q, *d);
     CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type == GEMM_DTYPE_BF16) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type == GEMM_DTYPE_BF16))
+    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type) ||
+        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type))
         return GEMM_ERR_CUDA;
     p.out = q.Out;
     p.out_type = q.kernel_out();
@@ -749,7 +772,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     p.batch = static_cast<int>(q.batch);
     p.tiles_x = static_cast<int>((q.M + 255) / 256);
     p.tiles_y = static_cast<int>((q.N + pbn - 1) / pbn);
-    p.num_kb = static_cast<int>((q.K + 63) / 64);
+    p.num_kb = static_cast<int>(q.kblocks());
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
     const int64_t ntiles = tpb * q.batch;
     if (ntiles > INT32_MAX)
@@ -792,7 +815,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     // Out rows 32-byte aligned: the epilogue stores without staging
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
                         q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
-    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, stream) != cudaSuccess)
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.is_f8(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }

@@ -60,14 +60,14 @@ struct TcParams {
 };
 
 struct MmaParams {
-    const uint16_t* A;
-    const uint16_t* B;
+    const void* A;  // 2-byte elements (fp16, bf16) or 1-byte ones (E4M3, E5M2)
+    const void* B;
     void* out;
     int out_type;
     int M, N, K, batch;
     int64_t lda, ldb, ldo;
     int64_t stride_a, stride_b, stride_o;
-    int vec_a;  // A rows and base 16-byte aligned
+    int vec_a;  // A's rows start on 8-element boundaries (vector loads of 8 elements)
     int vec_b;
     int a_mn;   // 1: A is MN-major, A(i, k) at A[k*lda + i]
     int b_mn;   // 1: B is MN-major, B(j, k) at B[k*ldb + j]
@@ -77,7 +77,7 @@ struct MmaParams {
 // epilogue.  Returns the launch status.
 cudaError_t tc05_configure(int bn, bool swap);  // one-time per device
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn,
-                        bool swap, int grid, cudaStream_t stream);
+                        bool swap, int grid, bool f8, cudaStream_t stream);
 
 // CTA-pair tcgen05 kernel: 256 x 256 tiles on clusters of two CTAs.
 // tc05_pair_configure reports how many pairs can be resident at once.
@@ -92,9 +92,10 @@ constexpr size_t pair_workspace_bytes(int pairs)
 // rows).  direct: epilogue without shared-memory staging and a 7-stage ring;
 // needs Out rows 32-byte aligned and no split (p.sk_pairs == 0).
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
-                             bool direct, cudaStream_t stream);
+                             bool direct, bool f8, cudaStream_t stream);
 
-cudaError_t mmasync_launch(const MmaParams& p, bool bf16, cudaStream_t stream);
+// in_type: the A/B element type, a gemm_dtype_t value (fp16, bf16, E4M3, E5M2).
+cudaError_t mmasync_launch(const MmaParams& p, int in_type, cudaStream_t stream);
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
                          cudaStream_t stream);
 

@@ -20,12 +20,17 @@
 // conflict-free ldmatrix).  Out-of-range rows and the K tail are zero-filled
 // while staging, and stores are masked.
 //
+// 8-bit float operands (E4M3, E5M2) are widened to fp16 while staging (exact)
+// and multiplied on the same fp16 MMA.
+//
 // An MN-major operand (A stored as (K, M), B as (K, N)) is staged as it lies,
 // 32 K-rows of 64 elements with a 144-byte pitch, i.e. a column-major shared
 // tile of the operand; "copy -> ldstmatrix" ("Algorithm" step 3) reads such a
 // tile with the .trans form of ldmatrix, whose lane t receives elements
 // (2(t%4), t/4) and (2(t%4)+1, t/4) of each 8x8 block: with K on the block's
 // rows that is exactly the fragment the row-major tile gives.
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,11 +45,56 @@ constexpr int MThreads = 128;
 constexpr int kTileElems = MBM * MPITCH;  // >= MBK * MNPITCH
 static_assert(MBK * MNPITCH <= kTileElems, "MN-major tile fits the slot");
 
-// Stage one (rows x 32) operand tile into shared memory, zero-filling
-// everything outside rows < nrows and k < K.
-__device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, int64_t ld, int row0, int nrows,
+// Element types of A and B (gemm_dtype_t values).  The 16-bit types are staged
+// as they are; the 8-bit floats are widened to fp16 while staging, which is
+// exact (every E4M3 and E5M2 value is an fp16 value), and multiplied on the
+// fp16 MMA.
+constexpr int kInF16 = 0, kInBF16 = 1, kInE4M3 = 3, kInE5M2 = 4;
+
+template <int IN>
+struct Elem {
+    using T = uint16_t;
+    static __device__ __forceinline__ uint16_t get(const T* g) { return *g; }
+    static __device__ __forceinline__ uint4 get8(const T* g) { return *reinterpret_cast<const uint4*>(g); }
+};
+
+template <int IN>
+struct Elem8 {
+    using T = uint8_t;
+    static __device__ __forceinline__ uint16_t get(const T* g)
+    {
+        return __nv_cvt_fp8_to_halfraw(*g, IN == kInE5M2 ? __NV_E5M2 : __NV_E4M3).x;
+    }
+    static __device__ __forceinline__ uint4 get8(const T* g)
+    {
+        const uint2 raw = *reinterpret_cast<const uint2*>(g);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t word = e < 2 ? raw.x : raw.y;
+            const int sh = (e & 1) * 16;
+            const uint16_t lo = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((word >> sh) & 0xff),
+                                                        IN == kInE5M2 ? __NV_E5M2 : __NV_E4M3).x;
+            const uint16_t hi = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((word >> (sh + 8)) & 0xff),
+                                                        IN == kInE5M2 ? __NV_E5M2 : __NV_E4M3).x;
+            w[e] = lo | (static_cast<uint32_t>(hi) << 16);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <>
+struct Elem<kInE4M3> : Elem8<kInE4M3> {};
+template <>
+struct Elem<kInE5M2> : Elem8<kInE5M2> {};
+
+// Stage one (rows x 32) operand tile into shared memory as fp16 (or bf16),
+// zero-filling everything outside rows < nrows and k < K.
+template <int IN>
+__device__ __forceinline__ void stage_tile(uint16_t* sdst, const void* src_v, int64_t ld, int row0, int nrows,
                                            int k0, int K, bool vec)
 {
+    using E = Elem<IN>;
+    const typename E::T* src = static_cast<const typename E::T*>(src_v);
     const int tid = threadIdx.x;
     if (vec) {
         // 64 rows x 4 chunks of 8 fp16 = 256 chunks, two per thread.
@@ -57,14 +107,14 @@ __device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, 
             const int k = k0 + kc;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (row < nrows) {
-                const uint16_t* g = src + static_cast<int64_t>(row) * ld + k;
+                const typename E::T* g = src + static_cast<int64_t>(row) * ld + k;
                 if (k + 8 <= K) {
-                    v = *reinterpret_cast<const uint4*>(g);
+                    v = E::get8(g);
                 } else if (k < K) {
                     uint16_t tmp[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        tmp[e] = (k + e < K) ? g[e] : uint16_t(0);
+                        tmp[e] = (k + e < K) ? E::get(g + e) : uint16_t(0);
                     v = make_uint4(tmp[0] | (uint32_t(tmp[1]) << 16), tmp[2] | (uint32_t(tmp[3]) << 16),
                                    tmp[4] | (uint32_t(tmp[5]) << 16), tmp[6] | (uint32_t(tmp[7]) << 16));
                 }
@@ -82,7 +132,7 @@ __device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, 
             const int k = k0 + kk;
             uint16_t v = 0;
             if (row < nrows && k < K)
-                v = src[static_cast<int64_t>(row) * ld + k];
+                v = E::get(src + static_cast<int64_t>(row) * ld + k);
             sdst[r * MPITCH + kk] = v;
         }
     }
@@ -91,9 +141,12 @@ __device__ __forceinline__ void stage_tile(uint16_t* sdst, const uint16_t* src, 
 // Stage one MN-major operand tile, rows [mn0, mn0 + 64) x k in [k0, k0 + 32),
 // from src (element (r, k) at src[k*ld + r]) into sdst[kk][r - mn0], zero
 // outside r < nmn and k < K.
-__device__ __forceinline__ void stage_tile_mn(uint16_t* sdst, const uint16_t* src, int64_t ld, int mn0, int nmn,
+template <int IN>
+__device__ __forceinline__ void stage_tile_mn(uint16_t* sdst, const void* src_v, int64_t ld, int mn0, int nmn,
                                               int k0, int K, bool vec)
 {
+    using E = Elem<IN>;
+    const typename E::T* src = static_cast<const typename E::T*>(src_v);
     const int tid = threadIdx.x;
     if (vec) {
         // 32 K-rows x 8 chunks of 8 elements, two chunks per thread.
@@ -106,14 +159,14 @@ __device__ __forceinline__ void stage_tile_mn(uint16_t* sdst, const uint16_t* sr
             const int r = mn0 + rc;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (k < K) {
-                const uint16_t* g = src + static_cast<int64_t>(k) * ld + r;
+                const typename E::T* g = src + static_cast<int64_t>(k) * ld + r;
                 if (r + 8 <= nmn) {
-                    v = *reinterpret_cast<const uint4*>(g);
+                    v = E::get8(g);
                 } else if (r < nmn) {
                     uint16_t tmp[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        tmp[e] = (r + e < nmn) ? g[e] : uint16_t(0);
+                        tmp[e] = (r + e < nmn) ? E::get(g + e) : uint16_t(0);
                     v = make_uint4(tmp[0] | (uint32_t(tmp[1]) << 16), tmp[2] | (uint32_t(tmp[3]) << 16),
                                    tmp[4] | (uint32_t(tmp[5]) << 16), tmp[6] | (uint32_t(tmp[7]) << 16));
                 }
@@ -131,7 +184,7 @@ __device__ __forceinline__ void stage_tile_mn(uint16_t* sdst, const uint16_t* sr
             const int r = mn0 + rr;
             uint16_t v = 0;
             if (r < nmn && k < K)
-                v = src[static_cast<int64_t>(k) * ld + r];
+                v = E::get(src + static_cast<int64_t>(k) * ld + r);
             sdst[kk * MNPITCH + rr] = v;
         }
     }
@@ -157,7 +210,7 @@ __device__ __forceinline__ void store_tile(const MmaParams& p, int b, int m0, in
             }
 }
 
-template <bool BF16>
+template <int IN>
 __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams p)
 {
     __shared__ __align__(16) uint16_t As[kTileElems];
@@ -169,8 +222,9 @@ __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams 
     const int m0 = blockIdx.y * MBM, n0 = blockIdx.x * MBN;
 
     for (int b = blockIdx.z; b < p.batch; b += gridDim.z) {
-        const uint16_t* Ab = p.A + static_cast<int64_t>(b) * p.stride_a;
-        const uint16_t* Bb = p.B + static_cast<int64_t>(b) * p.stride_b;
+        using ET = typename Elem<IN>::T;
+        const ET* Ab = static_cast<const ET*>(p.A) + static_cast<int64_t>(b) * p.stride_a;
+        const ET* Bb = static_cast<const ET*>(p.B) + static_cast<int64_t>(b) * p.stride_b;
         float acc[2][4][4];
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -183,13 +237,13 @@ __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams 
         for (int k0 = 0; k0 < p.K; k0 += MBK) {
             __syncthreads();  // previous tile fully consumed
             if (p.a_mn)
-                stage_tile_mn(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
+                stage_tile_mn<IN>(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
             else
-                stage_tile(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
+                stage_tile<IN>(As, Ab, p.lda, m0, p.M, k0, p.K, p.vec_a);
             if (p.b_mn)
-                stage_tile_mn(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
+                stage_tile_mn<IN>(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
             else
-                stage_tile(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
+                stage_tile<IN>(Bs, Bb, p.ldb, n0, p.N, k0, p.K, p.vec_b);
             __syncthreads();
 #pragma unroll
             for (int ks = 0; ks < MBK; ks += 16) {
@@ -231,7 +285,7 @@ __global__ void __launch_bounds__(MThreads) mmasync_gemm_kernel(const MmaParams 
                 for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
                     for (int nb = 0; nb < 4; ++nb)
-                        if (BF16)
+                        if (IN == kInBF16)
                             mma_m16n8k16_bf16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
                         else
                             mma_m16n8k16(acc[mi][nb], af[mi], bfr[nb][0], bfr[nb][1], acc[mi][nb]);
@@ -277,15 +331,18 @@ __global__ void __launch_bounds__(32) probe_kernel(const uint16_t* A, const uint
 
 }  // namespace
 
-cudaError_t mmasync_launch(const MmaParams& p, bool bf16, cudaStream_t stream)
+cudaError_t mmasync_launch(const MmaParams& p, int in_type, cudaStream_t stream)
 {
     dim3 grid((p.N + MBN - 1) / MBN, (p.M + MBM - 1) / MBM, p.batch < 65535 ? p.batch : 65535);
     if (grid.y > 65535)
         return cudaErrorInvalidConfiguration;
-    if (bf16)
-        mmasync_gemm_kernel<true><<<grid, MThreads, 0, stream>>>(p);
-    else
-        mmasync_gemm_kernel<false><<<grid, MThreads, 0, stream>>>(p);
+    switch (in_type) {
+    case kInF16: mmasync_gemm_kernel<kInF16><<<grid, MThreads, 0, stream>>>(p); break;
+    case kInBF16: mmasync_gemm_kernel<kInBF16><<<grid, MThreads, 0, stream>>>(p); break;
+    case kInE4M3: mmasync_gemm_kernel<kInE4M3><<<grid, MThreads, 0, stream>>>(p); break;
+    case kInE5M2: mmasync_gemm_kernel<kInE5M2><<<grid, MThreads, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -54,13 +54,16 @@ struct Cfg {
     static_assert(X_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
 };
 
-template <int BN, bool SWAP, int XR>
+// F8: 8-bit A and B (kind::f8f6f4); a stage slot then holds 128 elements of K
+// in the same 128 bytes per row.
+template <int BN, bool SWAP, int XR, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const TcParams p)
 {
     using C = Cfg<BN, SWAP, XR>;
     constexpr int STAGES = C::STAGES;
+    constexpr int KE = F8 ? 2 * BK : BK;  // elements of K per stage
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -112,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w0.next(s0)) {
             const int n = s0.kb1 - s0.kb0 < STAGES ? s0.kb1 - s0.kb0 : STAGES;
             for (int i = 0; i < n; ++i) {
-                prefetch_operand<XR>(&tmx, p.x_mn, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
-                prefetch_operand<BN>(&tmy, p.y_mn, (s0.kb0 + i) * BK, s0.y0, s0.b * p.y_bmul);
+                prefetch_operand<XR>(&tmx, p.x_mn, (s0.kb0 + i) * KE, s0.x0, s0.b * p.x_bmul);
+                prefetch_operand<BN>(&tmy, p.y_mn, (s0.kb0 + i) * KE, s0.y0, s0.b * p.y_bmul);
             }
         }
     }
@@ -141,9 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
                         mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES);
-                        load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * BK, s.x0,
+                        load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * KE, s.x0,
                                          s.b * p.x_bmul);
-                        load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * BK, s.y0,
+                        load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * KE, s.y0,
                                          s.b * p.y_bmul);
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -199,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    tc_mma_f16_w(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
+                    tc_mma_w<F8>(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
 #pragma unroll
                     for (int k = 1; k < BK / 16; ++k)
-                        tc_mma_f16_w(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi, idesc, 1u);
+                        tc_mma_w<F8>(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi, idesc, 1u);
                     if (!skip_release)
                         tc_commit(ea);
                     skip_release = false;
@@ -277,12 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, bool SWAP, int XR = 128>
 cudaError_t configure_one()
 {
-    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, SWAP, XR>::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg<BN, SWAP, XR>::SMEM);
 }
 
 template <int BN, bool SWAP, int XR = 128>
-cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid,
+cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid, bool f8,
                        cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
@@ -295,7 +302,9 @@ cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR>, tmx, tmy, p);
+    if (f8)
+        return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR, true>, tmx, tmy, p);
+    return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR, false>, tmx, tmy, p);
 }
 
 }  // namespace
@@ -317,19 +326,19 @@ cudaError_t tc05_configure(int bn, bool swap)
 }
 
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn, bool swap,
-                        int grid, cudaStream_t stream)
+                        int grid, bool f8, cudaStream_t stream)
 {
     if (swap) {
         if (bn != 64)
             return cudaErrorInvalidValue;
         if (p.x_box_bytes <= 112 * 128)
-            return launch_one<64, true, 112>(tmx, tmy, p, grid, stream);
-        return launch_one<64, true>(tmx, tmy, p, grid, stream);
+            return launch_one<64, true, 112>(tmx, tmy, p, grid, f8, stream);
+        return launch_one<64, true>(tmx, tmy, p, grid, f8, stream);
     }
     switch (bn) {
-    case 64: return launch_one<64, false>(tmx, tmy, p, grid, stream);
-    case 128: return launch_one<128, false>(tmx, tmy, p, grid, stream);
-    case 256: return launch_one<256, false>(tmx, tmy, p, grid, stream);
+    case 64: return launch_one<64, false>(tmx, tmy, p, grid, f8, stream);
+    case 128: return launch_one<128, false>(tmx, tmy, p, grid, f8, stream);
+    case 256: return launch_one<256, false>(tmx, tmy, p, grid, f8, stream);
     default: return cudaErrorInvalidValue;
     }
 }

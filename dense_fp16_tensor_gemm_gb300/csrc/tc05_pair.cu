@@ -213,13 +213,15 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
     }
 }
 
-template <int PBN, bool DIRECT>
+// F8: 8-bit A and B (kind::f8f6f4, 128 elements of K per 128-byte stage row).
+template <int PBN, bool DIRECT, bool F8>
 __global__ void __launch_bounds__(kPairThreads, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const TcParams p)
 {
     using C = PairCfg<PBN, DIRECT>;
     constexpr int kStages = C::STAGES;
+    constexpr int KE = F8 ? 2 * BK : BK;  // elements of K per stage
     constexpr int B_BYTES = C::B_BYTES;
     constexpr int STAGE_BYTES = C::STAGE_BYTES;
     constexpr int EPI_BYTES = C::EPI_BYTES;
@@ -274,8 +276,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const int n = s0.kb1 - s0.kb0 < kStages ? s0.kb1 - s0.kb0 : kStages;
             const int yb = s0.y0 + static_cast<int>(rank) * (PBN / 2);
             for (int i = 0; i < n; ++i) {
-                prefetch_operand<BM>(&tma, p.x_mn, (s0.kb0 + i) * BK, s0.x0, s0.b * p.x_bmul);
-                prefetch_operand<PBN / 2>(&tmb, p.y_mn, (s0.kb0 + i) * BK, yb, s0.b * p.y_bmul);
+                prefetch_operand<BM>(&tma, p.x_mn, (s0.kb0 + i) * KE, s0.x0, s0.b * p.x_bmul);
+                prefetch_operand<PBN / 2>(&tmb, p.y_mn, (s0.kb0 + i) * KE, yb, s0.b * p.y_bmul);
             }
         }
     }
@@ -308,10 +310,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                             filled |= 1u << stage;
                             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        load_operand<BM, true>(smem_u32(as + stage * A_BYTES), &tma, fb_leader, p.x_mn, kb * BK,
+                        load_operand<BM, true>(smem_u32(as + stage * A_BYTES), &tma, fb_leader, p.x_mn, kb * KE,
                                                s.x0, s.b * p.x_bmul);
                         load_operand<PBN / 2, true>(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, p.y_mn,
-                                                    kb * BK, yb, s.b * p.y_bmul);
+                                                    kb * KE, yb, s.b * p.y_bmul);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -368,10 +370,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    tc_mma_f16_pair_w(d_tmem, alo, da.hi, blo, db.hi, idesc, kb != s.kb0);
+                    tc_mma_pair_w<F8>(d_tmem, alo, da.hi, blo, db.hi, idesc, kb != s.kb0);
 #pragma unroll
                     for (int k = 1; k < BK / 16; ++k)
-                        tc_mma_f16_pair_w(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi, idesc, 1u);
+                        tc_mma_pair_w<F8>(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi, idesc, 1u);
                     if (!skip_release)
                         tc_commit_pair_mc(ea, 0x3);
                     skip_release = false;
@@ -476,18 +478,18 @@ cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaun
     return cfg;
 }
 
-template <int PBN, bool DIRECT>
-cudaError_t configure_one(int* max_pairs)
+template <int PBN, bool DIRECT, bool F8>
+cudaError_t configure_kind(int* max_pairs)
 {
     using C = PairCfg<PBN, DIRECT>;
-    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel<PBN, DIRECT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel<PBN, DIRECT, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT, F8>, &cfg);
     if (e != cudaSuccess)
         return e;
     *max_pairs = std::min(*max_pairs, n);
@@ -495,12 +497,21 @@ cudaError_t configure_one(int* max_pairs)
 }
 
 template <int PBN, bool DIRECT>
-cudaError_t launch_one(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs,
+cudaError_t configure_one(int* max_pairs)
+{
+    cudaError_t e = configure_kind<PBN, DIRECT, false>(max_pairs);
+    return e == cudaSuccess ? configure_kind<PBN, DIRECT, true>(max_pairs) : e;
+}
+
+template <int PBN, bool DIRECT>
+cudaError_t launch_one(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, bool f8,
                        cudaStream_t stream)
 {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT>::SMEM, stream, attr);
-    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT>, tma, tmb, p);
+    if (f8)
+        return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, true>, tma, tmb, p);
+    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, false>, tma, tmb, p);
 }
 
 }  // namespace
@@ -521,20 +532,20 @@ cudaError_t tc05_pair_configure(int* max_pairs)
 }
 
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
-                             bool direct, cudaStream_t stream)
+                             bool direct, bool f8, cudaStream_t stream)
 {
     if (direct) {
         switch (pbn) {
-        case 256: return launch_one<256, true>(tma, tmb, p, pairs, stream);
-        case 224: return launch_one<224, true>(tma, tmb, p, pairs, stream);
-        case 192: return launch_one<192, true>(tma, tmb, p, pairs, stream);
+        case 256: return launch_one<256, true>(tma, tmb, p, pairs, f8, stream);
+        case 224: return launch_one<224, true>(tma, tmb, p, pairs, f8, stream);
+        case 192: return launch_one<192, true>(tma, tmb, p, pairs, f8, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (pbn) {
-    case 256: return launch_one<256, false>(tma, tmb, p, pairs, stream);
-    case 224: return launch_one<224, false>(tma, tmb, p, pairs, stream);
-    case 192: return launch_one<192, false>(tma, tmb, p, pairs, stream);
+    case 256: return launch_one<256, false>(tma, tmb, p, pairs, f8, stream);
+    case 224: return launch_one<224, false>(tma, tmb, p, pairs, f8, stream);
+    case 192: return launch_one<192, false>(tma, tmb, p, pairs, f8, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -63,7 +63,11 @@ typedef enum gemm_status {
 typedef enum gemm_dtype {
     GEMM_DTYPE_F16 = 0,  /* IEEE binary16 */
     GEMM_DTYPE_BF16 = 1, /* bfloat16: the upper half of an IEEE binary32 */
-    GEMM_DTYPE_F32 = 2   /* IEEE binary32 (Out only) */
+    GEMM_DTYPE_F32 = 2,  /* IEEE binary32 (Out only) */
+    GEMM_DTYPE_E4M3 = 3, /* 8-bit float, 4 exponent bits (bias 7), 3 fraction bits, no infinities,
+                            largest value 448 (A and B only) */
+    GEMM_DTYPE_E5M2 = 4  /* 8-bit float, 5 exponent bits (bias 15), 2 fraction bits: the upper byte
+                            of an IEEE binary16 (A and B only) */
 } gemm_dtype_t;
 
 /* Kernel choice.  GEMM_PATH_AUTO lets the library pick (see gemm_nt_select_path). */
@@ -123,8 +127,16 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *
  * gemm_nt_batched_ex(..., GEMM_DTYPE_F16, GEMM_DTYPE_F32, ...).  An fp16 Out
  * overflows to infinity beyond 65504.  Products that would split K across CTAs
  * (few output tiles, long K) run on whole tiles when Out is not fp32, since
- * the partial sums are kept in fp32 only.  Any other dtype value:
- * GEMM_ERR_INVALID_VALUE.
+ * the partial sums are kept in fp32 only.
+ *
+ * A and B may also both be 8-bit floats (E4M3 or E5M2; lda, ldb and the batch
+ * strides then count bytes).  "Blackwell Tensor Cores" names the block-scaled
+ * low-precision forms of the tcgen05 MMA beside kind::f16; these run on its
+ * kind::f8f6f4 form without scale factors (products exact, fp32 accumulation),
+ * at twice the fp16 rate.  The tensor-core kernels want 16-byte aligned bases
+ * and pitches that are multiples of 16; other layouts, and MN-major 8-bit
+ * operands (gemm_nt_batched_major), run on the warp kernel, which widens the
+ * 8-bit values to fp16 (exact).  Any other dtype value: GEMM_ERR_INVALID_VALUE.
  */
 gemm_status_t gemm_nt_batched_ex(const void *A, const void *B, void *Out,
                                  gemm_dtype_t ab_type, gemm_dtype_t out_type,

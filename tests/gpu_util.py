@@ -84,26 +84,33 @@ TORCH_DTYPES = ("f16", "bf16", "f32")
 
 def torch_dtype(name):
     import torch
-    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[name]
 
 
 def dtype_code(name):
-    return {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32}[name]
+    return {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32,
+            "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2}[name]
+
+
+def esize(name):
+    return {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}[name]
 
 
 def to_device(bits, ab, ld=None, offset=0):
-    """(batch, rows, cols) host array of 16-bit values (float16, or uint16
-    bfloat16 patterns) -> device tensor of dtype `ab` with row pitch `ld`;
-    padding and the `offset` elements before the base hold NaN.  Returns
-    (tensor, base pointer)."""
+    """(batch, rows, cols) host array of bit patterns (float16 or uint16 for
+    the 16-bit types, uint8 for the 8-bit floats) -> device tensor of dtype
+    `ab` with row pitch `ld`; padding and the `offset` elements before the base
+    hold NaN.  Returns (tensor, base pointer)."""
     import torch
-    x = np.ascontiguousarray(bits).view(np.int16)
+    es = esize(ab)
+    x = np.ascontiguousarray(bits).view(np.int16 if es == 2 else np.uint8)
     batch, rows, cols = x.shape
     ld = ld or cols
-    t = torch.full((offset + batch * rows * ld,), float("nan"), dtype=torch_dtype(ab))
-    t[offset:].view(batch, rows, ld)[:, :, :cols] = torch.from_numpy(x).view(torch_dtype(ab))
+    t = torch.full((offset + batch * rows * ld,), float("nan"), dtype=torch.float32).to(torch_dtype(ab))
+    t[offset:].view(batch, rows, ld)[:, :, :cols] = torch.from_numpy(x.copy()).view(torch_dtype(ab))
     t = t.cuda()
-    return t, t.data_ptr() + 2 * offset
+    return t, t.data_ptr() + es * offset
 
 
 def run_general(A, B, ab, out, path, a_mn=False, b_mn=False, lda=None, ldb=None, ldo=None, out_offset=0,
