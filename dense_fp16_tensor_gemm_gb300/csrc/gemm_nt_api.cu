@@ -46,7 +46,7 @@ struct DeviceState {
     cudaError_t pipe_err = cudaSuccess;
     std::mutex pipe_mu;
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t ev[2 + 2 * 4];
+    cudaEvent_t ev[2 + 2 * 16];  // start, done, per-chunk input and output events
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -609,10 +609,14 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     return mmasync_launch(p, q.ab_type, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-constexpr int kPipeChunks = 4;
+// The host link carries ~210 GB/s in and ~190 GB/s out (measured on GB300),
+// so a call is bound by its input copies; what follows the last input chunk
+// (that chunk's product and its Out copy) is the part not overlapped, which 16
+// chunks keep short.
+constexpr int kPipeChunks = 16;
 
 // Host buffers in, host buffer out, with the copies overlapped with the
-// products: the problem is cut into up to four chunks (rows of A and Out for a
+// products: the problem is cut into up to sixteen chunks (rows of A and Out for a
 // single product, whole batches otherwise).  One library stream copies inputs
 // to the device, the caller's stream runs each chunk's product once its inputs
 // have arrived, a second library stream copies each chunk's Out back as soon as
@@ -659,6 +663,77 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
     }
 }
 
+// A single large product: Out is needed back in full, and each of its blocks
+// needs a row block of A and one of B, so A and B are both cut into kBlockSplit
+// row blocks and copied A0, B0, A1, B1, ...; Out block (i, j) is computed as
+// soon as A_i and B_j are in and copied back at once (a 2-D copy).  The first
+// result travels back after 2/kBlockSplit of the inputs instead of all of B,
+// so the output copies, the longer half of the traffic, start early.
+constexpr int kBlockSplit = 4;
+
+gemm_status_t from_host_blocks(const void* A_host, const void* B_host, float* Out_host, uint16_t* dA, uint16_t* dB,
+                               float* dOut, int64_t M, int64_t N, int64_t K, DeviceState& d, cudaStream_t stream)
+{
+    const int64_t per_a = (M + kBlockSplit - 1) / kBlockSplit, per_b = (N + kBlockSplit - 1) / kBlockSplit;
+    const int64_t pa = (per_a + 255) / 256 * 256, pb = (per_b + 255) / 256 * 256;
+    const int na = static_cast<int>((M + pa - 1) / pa), nb = static_cast<int>((N + pb - 1) / pb);
+    cudaEvent_t ev_start = d.ev[0], ev_done = d.ev[1];
+    cudaEvent_t* ev_a = d.ev + 2;
+    cudaEvent_t* ev_b = ev_a + kBlockSplit;
+    cudaEvent_t* ev_o = ev_b + kBlockSplit;  // kBlockSplit^2 of them
+    static_assert(2 + 2 * kBlockSplit + kBlockSplit * kBlockSplit <= 2 + 2 * kPipeChunks, "event pool");
+    std::lock_guard<std::mutex> lock(d.pipe_mu);
+    if (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(d.h2d, ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(d.d2h, ev_start, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const uint8_t* ha = static_cast<const uint8_t*>(A_host);
+    const uint8_t* hb = static_cast<const uint8_t*>(B_host);
+    const size_t row = static_cast<size_t>(K) * 2;
+    for (int s = 0; s < std::max(na, nb); ++s) {
+        if (s < na) {
+            const int64_t r0 = s * pa, rows = std::min(pa, M - r0);
+            if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dA) + r0 * row, ha + r0 * row, rows * row,
+                                cudaMemcpyHostToDevice, d.h2d) != cudaSuccess ||
+                cudaEventRecord(ev_a[s], d.h2d) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+        if (s < nb) {
+            const int64_t r0 = s * pb, rows = std::min(pb, N - r0);
+            if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dB) + r0 * row, hb + r0 * row, rows * row,
+                                cudaMemcpyHostToDevice, d.h2d) != cudaSuccess ||
+                cudaEventRecord(ev_b[s], d.h2d) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+    }
+    // blocks in the order their inputs complete: step s brings A_s and B_s
+    int k = 0;
+    for (int s = 0; s < std::max(na, nb); ++s) {
+        for (int t = 0; t < 2 * s + 1; ++t) {
+            // (s, 0..s) then (0..s-1, s)
+            const int i = t <= s ? s : t - s - 1;
+            const int j = t <= s ? t : s;
+            if (i >= na || j >= nb)
+                continue;
+            const int64_t r0 = i * pa, rows = std::min(pa, M - r0), c0 = j * pb, cols = std::min(pb, N - c0);
+            if (cudaStreamWaitEvent(stream, ev_a[i], 0) != cudaSuccess ||
+                cudaStreamWaitEvent(stream, ev_b[j], 0) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            const Problem q{dA + r0 * K, dB + c0 * K, dOut + r0 * N + c0, rows, cols, K, K, K, N, 1, 0, 0, 0};
+            gemm_status_t st = run(q, GEMM_PATH_AUTO, stream);
+            if (st != GEMM_OK)
+                return st;
+            if (cudaEventRecord(ev_o[k], stream) != cudaSuccess || cudaStreamWaitEvent(d.d2h, ev_o[k], 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(Out_host + r0 * N + c0, N * sizeof(float), dOut + r0 * N + c0, N * sizeof(float),
+                                  cols * sizeof(float), rows, cudaMemcpyDeviceToHost, d.d2h) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            ++k;
+        }
+    }
+    if (cudaEventRecord(ev_done, d.d2h) != cudaSuccess || cudaStreamWaitEvent(stream, ev_done, 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
 gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float* Out_host, uint16_t* dA,
                                   uint16_t* dB, float* dOut, int64_t M, int64_t N, int64_t K, int64_t batch,
                                   cudaStream_t stream)
@@ -676,12 +751,14 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
     });
     if (d->pipe_err != cudaSuccess)
         return GEMM_ERR_CUDA;
+    if (batch == 1 && M >= 2048 && N >= 2048 && K > 0)
+        return from_host_blocks(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, *d, stream);
     // chunks: [first, first + count) of batches, or of rows when batch == 1
     const bool by_rows = batch == 1;
     const int64_t units = by_rows ? M : batch;
     int64_t per = units;
     if (by_rows && M >= 1024)
-        per = ((M + kPipeChunks - 1) / kPipeChunks + 255) / 256 * 256;
+        per = std::max<int64_t>(256, ((M + kPipeChunks - 1) / kPipeChunks + 255) / 256 * 256);
     else if (!by_rows)
         per = (batch + kPipeChunks - 1) / kPipeChunks;
     const int nchunks = static_cast<int>((units + per - 1) / per);

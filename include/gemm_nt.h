@@ -192,7 +192,7 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
  * B (packed: lda = ldb = K, strideA = M*K, strideB = N*K) from host to the
  * caller's device buffers dA, dB, runs the batched product into dOut (packed,
  * ldo = N, strideO = M*N) and copies dOut back to host Out.  The work is cut
- * into up to four chunks (row blocks of A and Out when batch == 1, groups of
+ * into up to sixteen chunks (row blocks of A and Out when batch == 1, groups of
  * batches otherwise) so that copies in both directions overlap the products:
  * inputs travel on a library-owned copy stream, each chunk's product runs on
  * `stream` once its inputs have arrived, and its Out travels back on a second

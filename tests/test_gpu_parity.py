@@ -130,9 +130,11 @@ def test_torch_wrapper_and_streams():
 
 
 @pytest.mark.parametrize("batch,M,N,K", [(2, 130, 260, 192), (5, 70, 90, 64), (1, 2000, 300, 136),
-                                         (1, 100, 50, 40)])
+                                         (1, 100, 50, 40), (1, 2500, 2100, 136), (1, 2048, 2048, 64)])
 def test_from_host_pipeline(batch, M, N, K):
-    """Host buffers in and out; chunks of batches or of rows overlap the copies."""
+    """Host buffers in and out; chunks of batches or of rows, or for a large
+    single product 4 x 4 blocks of Out (uneven ones for 2500 x 2100), overlap
+    the copies."""
     import torch
     A, B = workloads.make_inputs(batch, M, N, K, "uniform", seed=10)
     ref, absdot = oracle.gemm_nt(A, B)
