@@ -48,10 +48,10 @@ L2_BYTES = 129 * 1024 * 1024
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1091781888 + 249862912, "c31affbf9a141447"),
-    "square_4096": (91180544 + 35043840, "c31affbf9a141447"),
-    "ragged_batch16_3001x2047x1000": (171515904 + 342115840, "c31affbf9a141447"),
-    "skinny_64x16384x8192": (269560832 + 3447808, "def5b1e2ec4e9763"),
+    "square_8192": (1182796032 + 252719872, "469fcb703cc546f3"),
+    "square_4096": (91348480 + 35164160, "469fcb703cc546f3"),
+    "ragged_batch16_3001x2047x1000": (171542784 + 342095104, "469fcb703cc546f3"),
+    "skinny_64x16384x8192": (269565696 + 3388928, "41efa3320d8a2cb3"),
 }
 
 
