@@ -16,7 +16,11 @@ accurate as any fp32 implementation.
 The same product for bfloat16 inputs ("Warp Matrix Instructions", "Other
 Fragment Shapes and Transfers") is ``gemm_nt(..., dtype="bf16")``, with inputs
 given as uint16 bit patterns; for the 8-bit floats E4M3 and E5M2 it is
-``dtype="e4m3"`` / ``"e5m2"`` with uint8 bit patterns.
+``dtype="e4m3"`` / ``"e5m2"`` with uint8 bit patterns.  The block-scaled form
+(one E8M0 power-of-two scale per 32 consecutive K elements of every row of A
+and of B; "Blackwell Tensor Cores" names block scaling and its tcgen05.cp
+scale operands without a formula, and the plain microscaling reading is taken)
+is ``gemm_nt_mx``.
 
 Parity rule used by the tests (stated once here so every test uses the same):
     |Out - ref| <= 1e-3 * absdot + 1e-6    elementwise, and
@@ -93,6 +97,16 @@ class Oracle:
             lib.oracle_gemm_nt_sampled_f8.argtypes = [u8p, u8p, i64p, i64p, i64p, i64, i64, i64, i64, i64, i64,
                                                       f64p, f64p, ctypes.c_int, ctypes.c_int]
             lib.oracle_gemm_nt_sampled_f8.restype = None
+        self.has_mx = hasattr(lib, "oracle_gemm_nt_mx")
+        if self.has_mx:
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_e8m0_to_double_array.argtypes = [u8p, f64p, i64]
+            lib.oracle_e8m0_to_double_array.restype = None
+            lib.oracle_gemm_nt_mx.argtypes = [u8p, u8p, u8p, u8p, f64p, f64p] + [i64] * 14 + [ctypes.c_int] * 2
+            lib.oracle_gemm_nt_mx.restype = None
+            lib.oracle_gemm_nt_sampled_mx.argtypes = ([u8p] * 4 + [i64p] * 3 + [i64] * 10 + [f64p, f64p]
+                                                      + [ctypes.c_int] * 2)
+            lib.oracle_gemm_nt_sampled_mx.restype = None
         self.lib = lib
         self.path = path
 
@@ -170,6 +184,68 @@ class Oracle:
             ref, absdot = ref[0], absdot[0]
         return ref, absdot
 
+    def e8m0_to_double(self, bits) -> np.ndarray:
+        """Decode E8M0 scales (uint8: 2^(e-127), 255 = NaN) to float64."""
+        b = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.oracle_e8m0_to_double_array(_ptr(b, ctypes.c_uint8), _ptr(out, ctypes.c_double), b.size)
+        return out
+
+    def _mx_operands(self, A, SA, B, SB):
+        if not self.has_mx:
+            raise ValueError("this oracle build has no block-scaled product")
+        a, b, sa, sb = _u8(A), _u8(B), _u8(SA), _u8(SB)
+        if a.ndim == 2:
+            a, b, sa, sb = a[None], b[None], sa[None], sb[None]
+        batch, M, K = a.shape
+        N = b.shape[1]
+        kb = (K + 31) // 32
+        if (b.shape != (batch, N, K) or sa.shape != (batch, M, kb) or sb.shape != (batch, N, kb)):
+            raise ValueError("shape mismatch: A %s, SA %s, B %s, SB %s"
+                             % (np.shape(A), np.shape(SA), np.shape(B), np.shape(SB)))
+        return a, sa, b, sb
+
+    def gemm_nt_mx(self, A, SA, B, SB, nthreads: int = 0, dtype: str = "e4m3"):
+        """Block-scaled product.  A (M,K) or (batch,M,K) and B (N,K) or
+        (batch,N,K): uint8 patterns of dtype "e4m3" or "e5m2"; SA (.., M,
+        ceil(K/32)) and SB (.., N, ceil(K/32)): uint8 E8M0 scales, one per 32
+        consecutive K elements of a row.  Returns (ref, absdot), float64."""
+        squeeze = np.ndim(A) == 2
+        a, sa, b, sb = self._mx_operands(A, SA, B, SB)
+        batch, M, K = a.shape
+        N, kb = b.shape[1], sa.shape[2]
+        ref = np.empty((batch, M, N), dtype=np.float64)
+        absdot = np.empty((batch, M, N), dtype=np.float64)
+        self.lib.oracle_gemm_nt_mx(_ptr(a, ctypes.c_uint8), _ptr(sa, ctypes.c_uint8), _ptr(b, ctypes.c_uint8),
+                                   _ptr(sb, ctypes.c_uint8), _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double),
+                                   batch, M, N, K, K, K, kb, kb, N, M * K, N * K, M * kb, N * kb, M * N,
+                                   int(nthreads), 1 if dtype == "e5m2" else 0)
+        if squeeze:
+            ref, absdot = ref[0], absdot[0]
+        return ref, absdot
+
+    def gemm_nt_sampled_mx(self, A, SA, B, SB, bidx, iidx, jidx, nthreads: int = 0, dtype: str = "e4m3"):
+        """Selected elements of :meth:`gemm_nt_mx` (2-D inputs take bidx = 0)."""
+        a, sa, b, sb = self._mx_operands(A, SA, B, SB)
+        batch, M, K = a.shape
+        N, kb = b.shape[1], sa.shape[2]
+        ii = np.ascontiguousarray(iidx, dtype=np.int64)
+        jj = np.ascontiguousarray(jidx, dtype=np.int64)
+        bb = np.ascontiguousarray(np.broadcast_to(np.asarray(bidx, dtype=np.int64), ii.shape))
+        if ii.shape != jj.shape:
+            raise ValueError("index arrays differ in shape")
+        if ii.size and (ii.min() < 0 or ii.max() >= M or jj.min() < 0 or jj.max() >= N
+                        or bb.min() < 0 or bb.max() >= batch):
+            raise IndexError("sample index out of range")
+        ref = np.empty(ii.shape, dtype=np.float64)
+        absdot = np.empty(ii.shape, dtype=np.float64)
+        self.lib.oracle_gemm_nt_sampled_mx(
+            _ptr(a, ctypes.c_uint8), _ptr(sa, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(sb, ctypes.c_uint8),
+            _ptr(bb, ctypes.c_int64), _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, kb, kb,
+            M * K, N * K, M * kb, N * kb, _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double), int(nthreads),
+            1 if dtype == "e5m2" else 0)
+        return ref, absdot
+
     def _fn(self, name, dtype):
         if dtype == "f16":
             return getattr(self.lib, name)
@@ -242,6 +318,18 @@ def f8_to_double(bits, dtype):
 
 def gemm_nt(A, B, nthreads: int = 0, dtype: str = "f16"):
     return default().gemm_nt(A, B, nthreads, dtype)
+
+
+def e8m0_to_double(bits):
+    return default().e8m0_to_double(bits)
+
+
+def gemm_nt_mx(A, SA, B, SB, nthreads: int = 0, dtype: str = "e4m3"):
+    return default().gemm_nt_mx(A, SA, B, SB, nthreads, dtype)
+
+
+def gemm_nt_sampled_mx(A, SA, B, SB, bidx, iidx, jidx, nthreads: int = 0, dtype: str = "e4m3"):
+    return default().gemm_nt_sampled_mx(A, SA, B, SB, bidx, iidx, jidx, nthreads, dtype)
 
 
 def gemm_nt_sampled(A, B, bidx, iidx, jidx, nthreads: int = 0, dtype: str = "f16"):

@@ -319,6 +319,88 @@ void oracle_gemm_nt_sampled_f8(const uint8_t *A, const uint8_t *B,
                   absdot ? absdot + s : 0);
 }
 
+/* ---------------------------------------------------------------- MX block scaling
+ * Block-scaled 8-bit inputs.  "Blackwell Tensor Cores", section on the other
+ * TMEM operations: tcgen05.cp brings the scale factors of a block-scaled MMA
+ * into Tensor Memory; the pages name block scaling and give no formula for it.
+ * The reading taken here is the plain microscaling one: every run of 32
+ * consecutive K elements of a row of A (of B) shares one scale, an 8-bit
+ * unsigned power of two (E8M0: value 2^(e - 127), e = 255 is NaN), and the
+ * element's value is its 8-bit float value times that scale:
+ *   ref[b,i,j] = sum_k (A[b,i,k] * sa[b,i,k/32]) * (B[b,j,k] * sb[b,j,k/32])
+ * Scaling by a power of two is exact in double, and so is the product of two
+ * scaled 8-bit values, so again only the sequential additions round. */
+double oracle_e8m0_to_double(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    return pow2i((int)e - 127);
+}
+
+void oracle_e8m0_to_double_array(const uint8_t *src, double *dst, int64_t n)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = oracle_e8m0_to_double(src[t]);
+}
+
+static void dot_nt_mx(const uint8_t *a_row, const uint8_t *sa_row, const uint8_t *b_row, const uint8_t *sb_row,
+                      int64_t K, int e5m2, double *ref, double *absdot)
+{
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = (e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k])) *
+                         oracle_e8m0_to_double(sa_row[k / 32]);
+        const double b = (e5m2 ? oracle_e5m2_to_double(b_row[k]) : oracle_e4m3_to_double(b_row[k])) *
+                         oracle_e8m0_to_double(sb_row[k / 32]);
+        const double p = a * b;
+        acc += p;
+        aacc += fabs(p);
+    }
+    *ref = acc;
+    if (absdot)
+        *absdot = aacc;
+}
+
+/* SA: (batch, M, ceil(K/32)) scales with row pitch ldsa and batch stride sSA;
+ * SB likewise for B's N rows. */
+void oracle_gemm_nt_mx(const uint8_t *A, const uint8_t *SA, const uint8_t *B, const uint8_t *SB, double *ref,
+                       double *absdot, int64_t batch, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                       int64_t ldsa, int64_t ldsb, int64_t ldr, int64_t sA, int64_t sB, int64_t sSA, int64_t sSB,
+                       int64_t sR, int nthreads, int e5m2)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bi = 0; bi < batch * M; ++bi) {
+        const int64_t b = bi / M, i = bi % M;
+        const uint8_t *a_row = A + b * sA + i * lda, *sa_row = SA + b * sSA + i * ldsa;
+        for (int64_t j = 0; j < N; ++j) {
+            double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
+            dot_nt_mx(a_row, sa_row, B + b * sB + j * ldb, SB + b * sSB + j * ldsb, K, e5m2,
+                      ref + b * sR + i * ldr + j, ab);
+        }
+    }
+}
+
+void oracle_gemm_nt_sampled_mx(const uint8_t *A, const uint8_t *SA, const uint8_t *B, const uint8_t *SB,
+                               const int64_t *bidx, const int64_t *iidx, const int64_t *jidx, int64_t n,
+                               int64_t K, int64_t lda, int64_t ldb, int64_t ldsa, int64_t ldsb, int64_t sA,
+                               int64_t sB, int64_t sSA, int64_t sSB, double *ref, double *absdot, int nthreads,
+                               int e5m2)
+{
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t s = 0; s < n; ++s)
+        dot_nt_mx(A + bidx[s] * sA + iidx[s] * lda, SA + bidx[s] * sSA + iidx[s] * ldsa,
+                  B + bidx[s] * sB + jidx[s] * ldb, SB + bidx[s] * sSB + jidx[s] * ldsb, K, e5m2, ref + s,
+                  absdot ? absdot + s : 0);
+}
+
 /* Number of threads the OpenMP runtime would use by default. */
 int oracle_max_threads(void)
 {

@@ -354,7 +354,104 @@ def pin_f8_integer_exact(orc, seed=32):
         assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A), np.abs(B)).astype(np.float64))
 
 
+def pin_e8m0_decoder_exhaustive(orc):
+    """All 256 E8M0 scale patterns: 2^(e-127) from math.ldexp, 255 is NaN."""
+    import math
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = orc.e8m0_to_double(bits)
+    want = np.array([math.ldexp(1.0, e - 127) for e in range(255)], dtype=np.float64)
+    assert np.isnan(got[255]), "E8M0 255 is NaN"
+    assert np.array_equal(got[:255], want), "E8M0 decoder mismatch"
+
+
+def _mx_draw(rng, batch, rows, K, dtype, vals, lo=112, hi=142):
+    x = rng.choice(vals, size=(batch, rows, K))
+    s = rng.integers(lo, hi, size=(batch, rows, (K + 31) // 32)).astype(np.uint8)
+    return x, f8_bits(x, dtype), s
+
+
+def pin_mx_exact_tiny(orc, seed=41):
+    """Block-scaled 8-bit products (K over several 32-element blocks and a
+    partial one, random scales) against exact rational sums; sampled = full."""
+    rng = np.random.default_rng(seed)
+    specials = {"e4m3": [0.0, -0.0, 2.0 ** -9, -(2.0 ** -6), 448.0, -448.0, 1.125, 3.5, -0.75],
+                "e5m2": [0.0, 2.0 ** -16, -(2.0 ** -14), 57344.0, -1.25, 0.75, 3.0]}
+    for dtype in ("e4m3", "e5m2"):
+        vals = np.array(specials[dtype])
+        for (batch, M, N, K) in ((1, 3, 4, 40), (2, 2, 3, 97)):
+            a, A, SA = _mx_draw(rng, batch, M, K, dtype, vals)
+            b, B, SB = _mx_draw(rng, batch, N, K, dtype, vals)
+            ref, absdot = orc.gemm_nt_mx(A, SA, B, SB, dtype=dtype)
+            assert np.all(np.isfinite(ref)), "exact sums here are finite"
+            g = gamma(max(K - 1, 0))
+            for bi in range(batch):
+                for i in range(M):
+                    for j in range(N):
+                        terms = [Fraction(float(a[bi, i, k])) * Fraction(2) ** (int(SA[bi, i, k // 32]) - 127)
+                                 * Fraction(float(b[bi, j, k])) * Fraction(2) ** (int(SB[bi, j, k // 32]) - 127)
+                                 for k in range(K)]
+                        ex = sum(terms, Fraction(0))
+                        exa = sum((abs(t) for t in terms), Fraction(0))
+                        assert abs(Fraction(float(ref[bi, i, j])) - ex) <= Fraction(g) * exa * Fraction(1 + 2 * U) \
+                            + Fraction(2 * U) * abs(ex) + Fraction(1, 2 ** 1074), "%s block-scaled product" % dtype
+                        assert abs(Fraction(float(absdot[bi, i, j])) - exa) <= Fraction(g + 2 * U) * exa \
+                            + Fraction(1, 2 ** 1074), "%s block-scaled absdot" % dtype
+            bb = rng.integers(0, batch, size=12)
+            ii = rng.integers(0, M, size=12)
+            jj = rng.integers(0, N, size=12)
+            sref, sabs = orc.gemm_nt_sampled_mx(A, SA, B, SB, bb, ii, jj, dtype=dtype)
+            assert np.array_equal(sref, ref[bb, ii, jj]) and np.array_equal(sabs, absdot[bb, ii, jj])
+
+
+def pin_mx_integer_exact(orc, seed=42):
+    """Integers in [-4, 4] with scales 2^-3..2^3: every product and partial
+    sum is exact, so the result equals numpy's einsum over the operands with
+    each scale repeated over its 32 K elements, bit for bit."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("e4m3", "e5m2"):
+        batch, M, N, K = 2, 9, 7, 150
+        A = rng.integers(-4, 5, size=(batch, M, K))
+        B = rng.integers(-4, 5, size=(batch, N, K))
+        SA = rng.integers(124, 131, size=(batch, M, (K + 31) // 32)).astype(np.uint8)
+        SB = rng.integers(124, 131, size=(batch, N, (K + 31) // 32)).astype(np.uint8)
+        ea = np.exp2(np.repeat(SA.astype(np.float64) - 127, 32, axis=2)[:, :, :K])
+        eb = np.exp2(np.repeat(SB.astype(np.float64) - 127, 32, axis=2)[:, :, :K])
+        want = np.einsum("bik,bjk->bij", A * ea, B * eb)
+        ref, absdot = orc.gemm_nt_mx(f8_bits(A, dtype), SA, f8_bits(B, dtype), SB, dtype=dtype)
+        assert np.array_equal(ref, want), "%s block-scaled integers" % dtype
+        assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A) * ea, np.abs(B) * eb))
+
+
+def pin_mx_unit_scales(orc, seed=43):
+    """Scales of 127 (2^0) reduce the block-scaled product to the unscaled
+    8-bit one, bit for bit; a scale of 128 on one whole row of A doubles that
+    row of the result exactly."""
+    rng = np.random.default_rng(seed)
+    for dtype in ("e4m3", "e5m2"):
+        x = rng.normal(0, 1, size=(3, 5, 70))
+        A = f8_bits(torch_cast(x, dtype), dtype)
+        B = f8_bits(torch_cast(rng.normal(0, 1, size=(3, 6, 70)), dtype), dtype)
+        SA = np.full((3, 5, 3), 127, dtype=np.uint8)
+        SB = np.full((3, 6, 3), 127, dtype=np.uint8)
+        r1, a1 = orc.gemm_nt_mx(A, SA, B, SB, dtype=dtype)
+        r0, a0 = orc.gemm_nt(A, B, dtype=dtype)
+        assert np.array_equal(r1, r0) and np.array_equal(a1, a0), "%s unit scales" % dtype
+        SA[1, 2, :] = 128
+        r2, _ = orc.gemm_nt_mx(A, SA, B, SB, dtype=dtype)
+        want = r0.copy()
+        want[1, 2, :] *= 2
+        assert np.array_equal(r2, want), "%s doubled row" % dtype
+
+
+def torch_cast(x, dtype):
+    """float64 values rounded to the nearest value of the 8-bit format."""
+    import torch
+    tt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(tt).to(torch.float64).numpy()
+
+
 ALL_PINS = [pin_decoder_exhaustive, pin_bruteforce_tiny, pin_k1_exact, pin_worked_examples,
             pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled,
             pin_bf16_decoder_exhaustive, pin_bf16_exact_tiny, pin_bf16_integer_exact,
-            pin_f8_decoders_exhaustive, pin_f8_exact_tiny, pin_f8_integer_exact]
+            pin_f8_decoders_exhaustive, pin_f8_exact_tiny, pin_f8_integer_exact,
+            pin_e8m0_decoder_exhaustive, pin_mx_exact_tiny, pin_mx_integer_exact, pin_mx_unit_scales]

@@ -38,6 +38,12 @@ MUTANTS = [
      "const double a = e5m2 ? oracle_e4m3_to_double(a_row[k]) : oracle_e5m2_to_double(a_row[k]);"),
     ("f8_abs_missing", "        aacc += fabs(p);\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8",
      "        aacc += p;\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8"),
+    ("mx_block_of_16", "sa_row[k / 32]", "sa_row[k / 16]"),
+    ("mx_scale_bias", "return pow2i((int)e - 127);", "return pow2i((int)e - 128);"),
+    ("mx_b_scale_dropped", " *\n                         oracle_e8m0_to_double(sb_row[k / 32]);", ";"),
+    ("mx_nan_pattern", "    if (e == 255)\n        return NAN;", "    if (e == 254)\n        return NAN;"),
+    ("mx_sampled_scale_row", "SA + bidx[s] * sSA + iidx[s] * ldsa", "SA + bidx[s] * sSA + jidx[s] * ldsa"),
+    ("mx_batch_scale_stride", "*sa_row = SA + b * sSA + i * ldsa;", "*sa_row = SA + b * sSB + i * ldsa;"),
     ("bf16_sampled_ij_swapped", "iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, ref + s,\n",
      "jidx[s] * lda, B + bidx[s] * sB + iidx[s] * ldb, K, ref + s,\n"),
 ]
