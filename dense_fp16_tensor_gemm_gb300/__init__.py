@@ -65,6 +65,9 @@ _SIGNATURES = {
                            + [ctypes.c_int, _vp]),
     "gemm_nt_batched_major": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int]
                               + [_i64] * 10 + [ctypes.c_int, _vp]),
+    "gemm_nt_mx": (ctypes.c_int, [_vp] * 5 + [ctypes.c_int, ctypes.c_int] + [_i64] * 10 + [ctypes.c_int, _vp]),
+    "gemm_nt_mx_scale_bytes": (_i64, [_i64, _i64]),
+    "gemm_nt_mx_pack_scales": (ctypes.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _vp]),
     "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
     "gemm_nt_check": (ctypes.c_int, [_vp]),
     "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -129,6 +132,22 @@ def gemm_nt_batched_major(A, a_major, B, b_major, Out, ab_type, out_type, M, N, 
                           strideA, strideB, strideO, path=0, stream=0):
     _check(load().gemm_nt_batched_major(A, int(a_major), B, int(b_major), Out, int(ab_type), int(out_type), M, N,
                                         K, lda, ldb, ldo, batch, strideA, strideB, strideO, int(path), stream))
+
+
+def gemm_nt_mx(A, SA, B, SB, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO,
+               path=0, stream=0):
+    """Block-scaled 8-bit product; SA / SB in the packed atom layout (see
+    include/gemm_nt.h)."""
+    _check(load().gemm_nt_mx(A, SA, B, SB, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo, batch,
+                             strideA, strideB, strideO, int(path), stream))
+
+
+def gemm_nt_mx_scale_bytes(rows, K):
+    return int(load().gemm_nt_mx_scale_bytes(rows, K))
+
+
+def gemm_nt_mx_pack_scales(plain, ld, stride, packed, rows, K, batch=1, stream=0):
+    _check(load().gemm_nt_mx_pack_scales(plain, ld, stride, packed, rows, K, batch, stream))
 
 
 def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
@@ -214,6 +233,48 @@ def gemm_nt(A, B, out=None, path=Path.AUTO, stream=None, out_dtype=None):
     gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
                        _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
                        1, 0, 0, 0, path, _stream_handle(stream))
+    return out
+
+
+def pack_mx_scales(S, K, stream=None):
+    """Plain block scales -> the packed atom layout, on the device: S a uint8
+    CUDA tensor (rows, ceil(K/32)) or (batch, rows, ceil(K/32)) of E8M0
+    bytes, last dimension contiguous.  Returns a new uint8 tensor."""
+    import torch
+    if S.dtype != torch.uint8 or S.dim() not in (2, 3) or S.stride(-1) != 1:
+        raise ValueError("S: uint8 (rows, ceil(K/32)) or (batch, rows, ceil(K/32)), last dimension contiguous")
+    S3 = S if S.dim() == 3 else S[None]
+    batch, rows, kb = S3.shape
+    if kb != (K + 31) // 32:
+        raise ValueError("S has %d scale columns, K=%d needs %d" % (kb, K, (K + 31) // 32))
+    packed = torch.empty(batch * gemm_nt_mx_scale_bytes(rows, K), dtype=torch.uint8, device=S.device)
+    gemm_nt_mx_pack_scales(S3.data_ptr(), S3.stride(1), S3.stride(0), packed.data_ptr(), rows, K, batch,
+                           _stream_handle(stream))
+    return packed
+
+
+def gemm_nt_mx_tensors(A, SA, B, SB, out=None, path=Path.AUTO, stream=None, out_dtype=None):
+    """Block-scaled Out = (A * sa) @ (B * sb).T for torch CUDA tensors: A (M,K)
+    and B (N,K) both float8_e4m3fn or both float8_e5m2; SA (M, ceil(K/32))
+    and SB (N, ceil(K/32)) uint8 E8M0 scales (2^(e-127)), one per 32
+    consecutive K elements of a row, in the plain layout (packed here).
+    ``out``/``out_dtype`` as in :func:`gemm_nt`."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("shapes: A (M,K), B (N,K)")
+    ab, ot, dt = _dtypes(A, B, out, out_dtype)
+    if ab not in (DType.E4M3, DType.E5M2):
+        raise TypeError("block-scaled inputs are float8_e4m3fn or float8_e5m2")
+    M, K = A.shape
+    N = B.shape[0]
+    pa, pb = pack_mx_scales(SA, K, stream), pack_mx_scales(SB, K, stream)
+    if out is None:
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must have shape (M,N)")
+    gemm_nt_mx(A.data_ptr(), pa.data_ptr(), B.data_ptr(), pb.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
+               _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"), 1, 0, 0, 0, path,
+               _stream_handle(stream))
     return out
 
 

@@ -162,6 +162,12 @@ struct Problem {
     int out_type = GEMM_DTYPE_F32;  // element type of Out
     int a_major = GEMM_MAJOR_K;     // A(i,k) at A[i*lda + k] (K) or A[k*lda + i] (MN)
     int b_major = GEMM_MAJOR_K;
+    // block scales of A and B in the packed atom layout (8-bit inputs only);
+    // null for unscaled products
+    const void* SA = nullptr;
+    const void* SB = nullptr;
+
+    bool mx() const { return SA != nullptr || SB != nullptr; }
 
     bool a_mn() const { return a_major == GEMM_MAJOR_MN; }
     bool b_mn() const { return b_major == GEMM_MAJOR_MN; }
@@ -173,6 +179,8 @@ struct Problem {
 
     int64_t out_esize() const { return out_type == GEMM_DTYPE_F32 ? 4 : 2; }
     bool is_f8() const { return ab_type == GEMM_DTYPE_E4M3 || ab_type == GEMM_DTYPE_E5M2; }
+    // kernel kind of tc05_launch: 0 16-bit, 1 8-bit, 2 8-bit block-scaled
+    int kind() const { return mx() ? 2 : (is_f8() ? 1 : 0); }
     int64_t ab_esize() const { return is_f8() ? 1 : 2; }
     // k-blocks of one 128-byte stage row: 64 elements of 16 bits, 128 of 8
     int64_t kblocks() const { return (K + 127 / ab_esize()) / (128 / ab_esize()); }
@@ -186,6 +194,13 @@ struct Problem {
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Bytes of one packed block-scale matrix: 512-byte atoms for every 128 rows
+// and every 128 elements of K.
+int64_t mx_scale_bytes(int64_t rows, int64_t K)
+{
+    return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
 
 // Byte span [lo, hi) touched by a strided batch of row-major matrices.
 void span(const void* base, int64_t esize, int64_t batch, int64_t stride, int64_t rows, int64_t ld,
@@ -233,6 +248,12 @@ gemm_status_t validate(const Problem& q)
         return GEMM_ERR_INVALID_VALUE;
     if (q.batch > 1 && q.sO < (q.M - 1) * q.ldo + q.N)
         return GEMM_ERR_OVERLAP;
+    if (q.mx() && q.K > 0) {
+        if (!q.SA || !q.SB || !q.is_f8() || q.a_mn() || q.b_mn())
+            return GEMM_ERR_INVALID_VALUE;
+        if (!aligned(q.SA, 16) || !aligned(q.SB, 16))
+            return GEMM_ERR_INVALID_VALUE;
+    }
     if (q.K > 0) {
         uintptr_t olo, ohi, alo, ahi, blo, bhi;
         span(q.Out, q.out_esize(), q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
@@ -240,6 +261,13 @@ gemm_status_t validate(const Problem& q)
         span(q.B, q.ab_esize(), q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
         if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
             return GEMM_ERR_OVERLAP;
+        if (q.mx()) {
+            const uintptr_t sa = reinterpret_cast<uintptr_t>(q.SA), sb = reinterpret_cast<uintptr_t>(q.SB);
+            const uintptr_t na = static_cast<uintptr_t>(mx_scale_bytes(q.M, q.K)) * (q.sA == 0 ? 1 : q.batch);
+            const uintptr_t nb = static_cast<uintptr_t>(mx_scale_bytes(q.N, q.K)) * (q.sB == 0 ? 1 : q.batch);
+            if ((olo < sa + na && sa < ohi) || (olo < sb + nb && sb < ohi))
+                return GEMM_ERR_OVERLAP;
+        }
     }
     return GEMM_OK;
 }
@@ -269,6 +297,8 @@ bool tma_ok(const Problem& q)
 
 gemm_path_t select_path(const Problem& q)
 {
+    if (q.mx())  // block-scaled: the one-CTA tcgen05 kernel, swapped for small M
+        return q.M <= 64 && q.N >= 1024 ? GEMM_PATH_SKINNY : GEMM_PATH_TC05;
     if (!tma_ok(q))
         return GEMM_PATH_MMASYNC;
     if (q.M <= 64 && q.N >= 1024)
@@ -393,6 +423,8 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         if (yrows > 64)
             return GEMM_ERR_NOT_SUPPORTED;
         bn = 64;
+    } else if (q.mx()) {
+        bn = yrows <= 64 ? 64 : 128;  // two accumulators and the scale slots fit TMEM
     } else {
         bn = yrows <= 64 ? 64 : (yrows <= 128 ? 128 : 256);
     }
@@ -401,7 +433,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     // X per CTA): every CTA takes an even share of the rows over all of K, with
     // an X box just tall enough for that share (a multiple of 8 rows).
     // (K-major X only: an MN-major box is whole 64-row chunks.)
-    const bool rowsplit = swap && !x_mn && q.batch == 1 && yrows <= bn &&
+    const bool rowsplit = swap && !x_mn && !q.mx() && q.batch == 1 && yrows <= bn &&
                           xrows >= 64 * static_cast<int64_t>(d.num_sms) && xrows <= 128 * static_cast<int64_t>(d.num_sms);
     int xbox = 128;
     if (rowsplit) {
@@ -460,7 +492,16 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         p.mode = kModeTiles;
         grid = static_cast<int>(std::min<int64_t>(ntiles, d.num_sms));
     }
-    if (tc05_launch(tmx, tmy, p, bn, swap, grid, q.is_f8(), stream) != cudaSuccess)
+    if (q.mx()) {
+        // scale atoms follow the operands: X = B when swapped
+        const void* sx = swap ? q.SB : q.SA;
+        const void* sy = swap ? q.SA : q.SB;
+        p.sf_x = static_cast<const uint8_t*>(sx);
+        p.sf_y = static_cast<const uint8_t*>(sy);
+        p.sf_x_bstride = xs == 0 ? 0 : mx_scale_bytes(xrows, q.K);
+        p.sf_y_bstride = ys == 0 ? 0 : mx_scale_bytes(yrows, q.K);
+    }
+    if (tc05_launch(tmx, tmy, p, bn, swap, grid, q.kind(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -643,6 +684,8 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         return zero_out(q, stream);
     if (path == GEMM_PATH_AUTO)
         path = select_path(q);
+    if (q.mx() && path != GEMM_PATH_TC05 && path != GEMM_PATH_SKINNY)
+        return GEMM_ERR_NOT_SUPPORTED;
     switch (path) {
     case GEMM_PATH_MMASYNC:
         return run_mmasync(q, stream);
@@ -949,6 +992,52 @@ gemm_status_t gemm_nt_batched_major(const void* A, gemm_major_t a_major, const v
     q.a_major = static_cast<int>(a_major);
     q.b_major = static_cast<int>(b_major);
     return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_nt_mx(const void* A, const void* SA, const void* B, const void* SB, void* Out,
+                         gemm_dtype_t ab_type, gemm_dtype_t out_type, int64_t M, int64_t N, int64_t K, int64_t lda,
+                         int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
+                         gemm_path_t path, gemm_stream_t stream)
+{
+    if (K > 0 && M > 0 && N > 0 && batch > 0 && (!SA || !SB))
+        return GEMM_ERR_INVALID_VALUE;
+    Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
+    q.ab_type = static_cast<int>(ab_type);
+    q.out_type = static_cast<int>(out_type);
+    q.SA = SA;
+    q.SB = SB;
+    if (!q.is_f8())
+        return GEMM_ERR_INVALID_VALUE;
+    return gnt::run(q, path, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t gemm_nt_mx_scale_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0)
+        return -1;
+    return gnt::mx_scale_bytes(rows, K);
+}
+
+gemm_status_t gemm_nt_mx_pack_scales(const void* plain, int64_t ld, int64_t stride, void* packed, int64_t rows,
+                                     int64_t K, int64_t batch, gemm_stream_t stream)
+{
+    if (rows < 0 || K < 0 || batch < 0 || ld < 0 || stride < 0)
+        return GEMM_ERR_INVALID_VALUE;
+    if (rows == 0 || K == 0 || batch == 0)
+        return GEMM_OK;
+    const int64_t kb = (K + 31) / 32;
+    if (!plain || !packed || ld < kb || (batch > 1 && stride != 0 && stride < (rows - 1) * ld + kb))
+        return GEMM_ERR_INVALID_VALUE;
+    if (rows > INT32_MAX || K > INT32_MAX || batch > INT32_MAX)
+        return GEMM_ERR_INVALID_VALUE;
+    gnt::DeviceState* d = nullptr;
+    gemm_status_t st = gnt::device_state(&d);
+    if (st != GEMM_OK)
+        return st;
+    return gnt::mx_pack_launch(static_cast<const uint8_t*>(plain), ld, stride, static_cast<uint8_t*>(packed), rows, K,
+                               batch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_nt_f16_f32_from_host(const void* A_host, const void* B_host, float* Out_host, void* dA,

@@ -57,6 +57,13 @@ struct TcParams {
     uint32_t* status;     // device status word
     unsigned long long wait_limit;  // bounded-wait limit, SM clock cycles
     int fault;            // test hook: 0 none, 1 drop a producer stage, 2 skip a release
+    // Block-scaled 8-bit inputs (kind 2 of tc05_launch): the scale atoms of X
+    // and Y, 512 bytes per (128-row block, 128-element K block), row block-major
+    // (atom (r, k) at offset (r * num_kb + k) * 512), one set per batch.
+    const uint8_t* sf_x;
+    const uint8_t* sf_y;
+    long long sf_x_bstride;  // bytes between batches (0: shared)
+    long long sf_y_bstride;
 };
 
 struct MmaParams {
@@ -74,10 +81,17 @@ struct MmaParams {
 };
 
 // tcgen05 kernel family.  bn in {64, 128, 256}; swap selects the transposed
-// epilogue.  Returns the launch status.
+// epilogue; kind 0: 16-bit inputs, 1: 8-bit inputs, 2: 8-bit inputs with block
+// scales (bn 64 or 128, 128-row X tiles).  Returns the launch status.
 cudaError_t tc05_configure(int bn, bool swap);  // one-time per device
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn,
-                        bool swap, int grid, bool f8, cudaStream_t stream);
+                        bool swap, int grid, int kind, cudaStream_t stream);
+
+// Block scales: plain (rows, ceil(K/32)) E8M0 bytes, row pitch ld, batch
+// stride `stride` -> the atom layout of TcParams::sf_x (missing rows and K
+// blocks filled with 127, a scale of one).
+cudaError_t mx_pack_launch(const uint8_t* plain, int64_t ld, int64_t stride, uint8_t* packed, int64_t rows,
+                           int64_t K, int64_t batch, cudaStream_t stream);
 
 // CTA-pair tcgen05 kernel: 256 x 256 tiles on clusters of two CTAs.
 // tc05_pair_configure reports how many pairs can be resident at once.

@@ -24,6 +24,7 @@
 // Every mbarrier wait is bounded (wait_limit cycles); on expiry the kernel sets
 // the device status word and an abort flag, all roles leave their loops, loads
 // still in flight are waited for, TMEM is freed and the kernel returns.
+#include "ptx_mx.cuh"
 #include "tc05_common.cuh"
 
 namespace gnt {
@@ -38,30 +39,51 @@ constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // swapped path (shares of at most 112 rows), which packs 10 stages instead of
 // 9.  The MMA still reads 128 rows: rows XR..127 come from the next slot and
 // only feed accumulator rows that are never stored.
-template <int BN, bool SWAP, int XR = 128>
+// KIND: 0 16-bit inputs (kind::f16), 1 8-bit inputs (kind::f8f6f4), 2 8-bit
+// inputs with block scales (kind::mxf8f6f4): each stage then also holds one
+// 512-byte scale atom for X and one for Y, and TMEM holds, after the two
+// accumulators, 8 columns of scales per stage (X atom, then Y atom).
+constexpr int kKind16 = 0, kKind8 = 1, kKindMx = 2;
+
+constexpr int pow2_at_least(int v)
+{
+    int r = 32;
+    while (r < v)
+        r *= 2;
+    return r;
+}
+
+template <int BN, bool SWAP, int XR = 128, int KIND = kKind16>
 struct Cfg {
-    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? (XR <= 112 ? 10 : 9) : 8));
     static constexpr int X_BYTES = XR * BK * 2;
     static constexpr int Y_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
+    static constexpr int SF_BYTES = KIND == kKindMx ? 1024 : 0;
+    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES + SF_BYTES;
     static constexpr int EPI_BYTES = SWAP ? 0 : 8 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
-    static constexpr int TMEM_COLS = 2 * BN;                      // power of two, >= 32
     static constexpr int BAR_BYTES = 256;
+    static constexpr int BASE_STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? (XR <= 112 ? 10 : 9) : 8));
+    static constexpr int FIT_STAGES = (232448 - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = BASE_STAGES < FIT_STAGES ? BASE_STAGES : FIT_STAGES;
+    static constexpr int SF_COL = 2 * BN;  // first TMEM column of the scale slots
+    static constexpr int TMEM_COLS = pow2_at_least(2 * BN + (KIND == kKindMx ? 8 * STAGES : 0));
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(X_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
+    static_assert(TMEM_COLS <= 512, "Tensor Memory columns");
 };
 
-// F8: 8-bit A and B (kind::f8f6f4); a stage slot then holds 128 elements of K
-// in the same 128 bytes per row.
-template <int BN, bool SWAP, int XR, bool F8>
+// 8-bit A and B (KIND 1, 2): a stage slot holds 128 elements of K in the same
+// 128 bytes per row.
+template <int BN, bool SWAP, int XR, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const TcParams p)
 {
-    using C = Cfg<BN, SWAP, XR>;
+    using C = Cfg<BN, SWAP, XR, KIND>;
+    constexpr bool F8 = KIND != kKind16;
+    constexpr bool MX = KIND == kKindMx;
     constexpr int STAGES = C::STAGES;
     constexpr int KE = F8 ? 2 * BK : BK;  // elements of K per stage
 
@@ -69,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xs = smem;
     uint8_t* ys = smem + STAGES * C::X_BYTES;
+    uint8_t* sfs = ys + STAGES * C::Y_BYTES;  // MX: per stage the X atom, then the Y atom
     float* epi = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES);
     uint64_t* full = bars;
@@ -143,11 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
-                        mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES);
+                        mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES + C::SF_BYTES);
                         load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * KE, s.x0,
                                          s.b * p.x_bmul);
                         load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * KE, s.y0,
                                          s.b * p.y_bmul);
+                        if constexpr (MX) {
+                            // the stage's scale atoms: rows [128*(x0/128), +128) of X and
+                            // [128*(y0/128), +128) of Y, K blocks 4*kb .. 4*kb+3
+                            const uint32_t sfd = smem_u32(sfs + stage * C::SF_BYTES);
+                            bulk_load(sfd, p.sf_x + s.b * p.sf_x_bstride + (static_cast<int64_t>(s.x0 / BM) * p.num_kb + kb) * 512,
+                                      512, fb);
+                            bulk_load(sfd + 512,
+                                      p.sf_y + s.b * p.sf_y_bstride + (static_cast<int64_t>(s.y0 / BM) * p.num_kb + kb) * 512,
+                                      512, fb);
+                        }
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -174,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ahead of the one executing, so the work between k-blocks is kept to
         // additions (stage addresses, descriptor words) and the waits' fast path.
         if (lane == 0) {
-            const uint32_t idesc = C::IDESC | p.idesc_bits;
+            const uint32_t idesc = (MX ? idesc_mx(BM, BN) : C::IDESC) | p.idesc_bits;
+            const uint32_t sf_smem0 = smem_u32(sfs);
             const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
             const DescWords dx = desc_words(smem_u32(xs), p.x_mn != 0);
             const DescWords dy = desc_words(smem_u32(ys), p.y_mn != 0);
@@ -195,6 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                // MX: a Y tile that starts half-way into its 128-row atom reads
+                // the atom's upper columns
+                const uint32_t y_sf_off = static_cast<uint32_t>((s.y0 % BM) / 32);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (!wait_bounded(fa, phase, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
@@ -202,10 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    tc_mma_w<F8>(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
+                    if constexpr (MX) {
+                        // The scale slot of a stage is refilled only after the
+                        // stage's previous MMAs completed (its release), and the
+                        // copy is ordered before the MMAs that follow it.
+                        const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + 8 * stage);
+                        const uint32_t sfd = sf_smem0 + static_cast<uint32_t>(stage * C::SF_BYTES);
+                        tc_cp_atom(sft, atom_desc(sfd));
+                        tc_cp_atom(sft + 4, atom_desc(sfd + 512));
 #pragma unroll
-                    for (int k = 1; k < BK / 16; ++k)
-                        tc_mma_w<F8>(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi, idesc, 1u);
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma_mx(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi,
+                                      idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4), sft,
+                                      sft + 4 + y_sf_off, (k > 0 || kb != s.kb0) ? 1u : 0u);
+                    } else {
+                        tc_mma_w<F8>(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
+#pragma unroll
+                        for (int k = 1; k < BK / 16; ++k)
+                            tc_mma_w<F8>(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi, idesc, 1u);
+                    }
                     if (!skip_release)
                         tc_commit(ea);
                     skip_release = false;
@@ -277,34 +329,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, bool SWAP, int XR = 128>
-cudaError_t configure_one()
+template <int BN, bool SWAP, int XR = 128, int KIND = kKind16>
+cudaError_t configure_kind()
 {
-    cudaError_t e = cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, SWAP, XR>::SMEM);
-    if (e != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<BN, SWAP, XR>::SMEM);
+    return cudaFuncSetAttribute(tc05_gemm_kernel<BN, SWAP, XR, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<BN, SWAP, XR, KIND>::SMEM);
 }
 
 template <int BN, bool SWAP, int XR = 128>
-cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid, bool f8,
-                       cudaStream_t stream)
+cudaError_t configure_one()
+{
+    cudaError_t e = configure_kind<BN, SWAP, XR, kKind16>();
+    return e == cudaSuccess ? configure_kind<BN, SWAP, XR, kKind8>() : e;
+}
+
+template <int BN, bool SWAP, int XR = 128, int KIND = kKind16>
+cudaError_t launch_kind(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid,
+                        cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<BN, SWAP, XR>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, SWAP, XR, KIND>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (f8)
-        return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR, true>, tmx, tmy, p);
-    return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR, false>, tmx, tmy, p);
+    return cudaLaunchKernelEx(&cfg, tc05_gemm_kernel<BN, SWAP, XR, KIND>, tmx, tmy, p);
+}
+
+template <int BN, bool SWAP, int XR = 128>
+cudaError_t launch_one(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int grid, int kind,
+                       cudaStream_t stream)
+{
+    if (kind == kKind8)
+        return launch_kind<BN, SWAP, XR, kKind8>(tmx, tmy, p, grid, stream);
+    return launch_kind<BN, SWAP, XR, kKind16>(tmx, tmy, p, grid, stream);
 }
 
 }  // namespace
@@ -315,30 +377,47 @@ cudaError_t tc05_configure(int bn, bool swap)
         if (bn != 64)
             return cudaErrorInvalidValue;
         cudaError_t e = configure_one<64, true>();
-        return e == cudaSuccess ? configure_one<64, true, 112>() : e;
+        if (e == cudaSuccess)
+            e = configure_one<64, true, 112>();
+        return e == cudaSuccess ? configure_kind<64, true, 128, kKindMx>() : e;
     }
+    cudaError_t e;
     switch (bn) {
-    case 64: return configure_one<64, false>();
-    case 128: return configure_one<128, false>();
+    case 64:
+        e = configure_one<64, false>();
+        return e == cudaSuccess ? configure_kind<64, false, 128, kKindMx>() : e;
+    case 128:
+        e = configure_one<128, false>();
+        return e == cudaSuccess ? configure_kind<128, false, 128, kKindMx>() : e;
     case 256: return configure_one<256, false>();
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn, bool swap,
-                        int grid, bool f8, cudaStream_t stream)
+                        int grid, int kind, cudaStream_t stream)
 {
+    if (kind == kKindMx) {
+        // block-scaled: 128-row X tiles (no row split), Y tiles of 64 or 128
+        if (swap)
+            return bn == 64 ? launch_kind<64, true, 128, kKindMx>(tmx, tmy, p, grid, stream) : cudaErrorInvalidValue;
+        if (bn == 64)
+            return launch_kind<64, false, 128, kKindMx>(tmx, tmy, p, grid, stream);
+        if (bn == 128)
+            return launch_kind<128, false, 128, kKindMx>(tmx, tmy, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
     if (swap) {
         if (bn != 64)
             return cudaErrorInvalidValue;
         if (p.x_box_bytes <= 112 * 128)
-            return launch_one<64, true, 112>(tmx, tmy, p, grid, f8, stream);
-        return launch_one<64, true>(tmx, tmy, p, grid, f8, stream);
+            return launch_one<64, true, 112>(tmx, tmy, p, grid, kind, stream);
+        return launch_one<64, true>(tmx, tmy, p, grid, kind, stream);
     }
     switch (bn) {
-    case 64: return launch_one<64, false>(tmx, tmy, p, grid, f8, stream);
-    case 128: return launch_one<128, false>(tmx, tmy, p, grid, f8, stream);
-    case 256: return launch_one<256, false>(tmx, tmy, p, grid, f8, stream);
+    case 64: return launch_one<64, false>(tmx, tmy, p, grid, kind, stream);
+    case 128: return launch_one<128, false>(tmx, tmy, p, grid, kind, stream);
+    case 256: return launch_one<256, false>(tmx, tmy, p, grid, kind, stream);
     default: return cudaErrorInvalidValue;
     }
 }

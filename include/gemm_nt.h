@@ -188,6 +188,58 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
                                     int64_t strideO, gemm_path_t path, gemm_stream_t stream);
 
 /*
+ * Block-scaled 8-bit product ("Blackwell Tensor Cores", on the other TMEM
+ * operations: tcgen05.cp brings the scale factors of a block-scaled MMA into
+ * Tensor Memory; the MMA reference it points to lists block scaling).  A and B
+ * are E4M3 or E5M2 (both the same), K-major, as in gemm_nt_batched_ex; every
+ * run of 32 consecutive K elements of a row of A (of B) shares one scale, an
+ * E8M0 byte e standing for 2^(e-127) (255 is NaN), and
+ *   Out[b,i,j] = sum_k (A[b,i,k] * 2^(sa[b,i,k/32]-127)) * (B[b,j,k] * 2^(sb[b,j,k/32]-127))
+ * accumulated in fp32 on the tcgen05 kind::mxf8f6f4 MMA, Out fp32, fp16 or
+ * bf16.
+ *
+ * SA and SB hold the scales in the packed atom layout (device memory, 16-byte
+ * aligned): for each 128 rows and each 128 elements of K one 512-byte atom
+ * whose byte 16*r + 4*q + s is the scale of row 32*q + r of the row block, K
+ * block s of the K block group; atoms stored row block-major, so atom
+ * (rb, kg) is at byte (rb * ceil(K/128) + kg) * 512; rows and K blocks past
+ * the matrix are ignored (any value but 255).  One matrix of scales takes
+ * gemm_nt_mx_scale_bytes(rows, K) bytes; the matrices of a batch follow one
+ * another, except that an operand with batch stride 0 (shared by every batch)
+ * has one matrix of scales.  gemm_nt_mx_pack_scales makes this layout from
+ * the plain one.
+ *
+ * path: GEMM_PATH_AUTO, GEMM_PATH_TC05 (128 x 64 or 128 x 128 tiles) or
+ * GEMM_PATH_SKINNY (M <= 64; chosen by AUTO for M <= 64 and N >= 1024).  The
+ * CTA-pair and warp kernels take no scales (GEMM_ERR_NOT_SUPPORTED), nor does
+ * a layout the tensor-core kernels cannot read (unaligned bases, pitches not
+ * multiples of 16 bytes).  Null SA / SB with K > 0, a 16-bit ab_type, or
+ * unaligned SA / SB: GEMM_ERR_INVALID_VALUE; Out overlapping A, B, SA or SB:
+ * GEMM_ERR_OVERLAP.  Other arguments and errors as gemm_nt_batched_ex.
+ */
+gemm_status_t gemm_nt_mx(const void *A, const void *SA, const void *B, const void *SB, void *Out,
+                         gemm_dtype_t ab_type, gemm_dtype_t out_type,
+                         int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldo,
+                         int64_t batch, int64_t strideA, int64_t strideB,
+                         int64_t strideO, gemm_path_t path, gemm_stream_t stream);
+
+/* Bytes of one packed scale matrix for `rows` rows and K elements of K:
+ * ceil(rows/128) * ceil(K/128) * 512; -1 for negative arguments. */
+int64_t gemm_nt_mx_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * Packs block scales on the device: `plain` holds, for each of `batch`
+ * matrices (batch stride `stride` bytes, 0 = one shared matrix), `rows` rows of
+ * ceil(K/32) E8M0 bytes with row pitch `ld` bytes (ld >= ceil(K/32));
+ * `packed` receives batch * gemm_nt_mx_scale_bytes(rows, K) bytes in the
+ * layout gemm_nt_mx reads (padding atoms filled with 127).  Stream-ordered;
+ * GEMM_ERR_INVALID_VALUE for null pointers or pitches too small.
+ */
+gemm_status_t gemm_nt_mx_pack_scales(const void *plain, int64_t ld, int64_t stride, void *packed,
+                                     int64_t rows, int64_t K, int64_t batch, gemm_stream_t stream);
+
+/*
  * Host-side pipeline for callers whose data lives in host memory: copies A and
  * B (packed: lda = ldb = K, strideA = M*K, strideB = N*K) from host to the
  * caller's device buffers dA, dB, runs the batched product into dOut (packed,

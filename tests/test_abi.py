@@ -151,3 +151,27 @@ def test_major_validation(lib):
     # an empty product returns before any pointer check
     assert f(FAKE_A, Mj.MN, FAKE_B, Mj.K, FAKE_A + 256, D.F16, D.F32, 0, N, K, 16, 8, N, 1, 0, 0, 0, 0,
              None) == 0
+
+
+def test_mx_validation(lib):
+    """Block-scaled entry: rejected on the host before any CUDA call."""
+    D = gnt.DType
+    f = lib.gemm_nt_mx
+    tail = (64, 256, 256, 256, 256, 256, 1, 0, 0, 0, 0, None)  # M N K lda ldb ldo batch sA sB sO path stream
+    SA, SB = FAKE_A + (1 << 20), FAKE_B + (1 << 20)
+    assert f(FAKE_A, 0, FAKE_B, SB, FAKE_O, D.E4M3, D.F32, *tail) == gnt.Status.INVALID_VALUE  # null SA
+    assert f(FAKE_A, SA, FAKE_B, 0, FAKE_O, D.E4M3, D.F32, *tail) == gnt.Status.INVALID_VALUE  # null SB
+    assert f(FAKE_A, SA, FAKE_B, SB, FAKE_O, D.F16, D.F32, *tail) == gnt.Status.INVALID_VALUE  # 16-bit inputs
+    assert f(FAKE_A, SA + 8, FAKE_B, SB, FAKE_O, D.E5M2, D.F32, *tail) == gnt.Status.INVALID_VALUE  # SA unaligned
+    # Out on top of the scales of B
+    assert f(FAKE_A, SA, FAKE_B, FAKE_O, FAKE_O, D.E4M3, D.F32, *tail) == gnt.Status.OVERLAP
+    # empty problems launch nothing
+    assert f(FAKE_A, 0, FAKE_B, 0, FAKE_O, D.E4M3, D.F32, 0, *tail[1:]) == gnt.Status.OK
+    assert lib.gemm_nt_mx_scale_bytes(1, 1) == 512
+    assert lib.gemm_nt_mx_scale_bytes(129, 257) == 2 * 3 * 512
+    assert lib.gemm_nt_mx_scale_bytes(-1, 5) == -1
+    p = lib.gemm_nt_mx_pack_scales
+    assert p(0, 8, 0, FAKE_O, 10, 256, 1, None) == gnt.Status.INVALID_VALUE   # null plain
+    assert p(FAKE_A, 7, 0, FAKE_O, 10, 256, 1, None) == gnt.Status.INVALID_VALUE  # ld < ceil(K/32)
+    assert p(FAKE_A, 8, 8, FAKE_O, 10, 256, 2, None) == gnt.Status.INVALID_VALUE  # batch stride too small
+    assert p(FAKE_A, 8, 0, FAKE_O, 0, 256, 1, None) == gnt.Status.OK          # nothing to pack
