@@ -164,20 +164,30 @@ def dist_init():
     return world, rank, local
 
 
-def oracle_cpu_sample(w, A, B, target_s, dtype="f16"):
+def oracle_cpu_sample(w, A, B, target_s, dtype="f16", scales=None):
     """Time the CPU oracle on whole rows of the workload (batch 0), sized to
-    about target_s seconds.  Returns (tflops, seconds, rows, threads)."""
+    about target_s seconds; `scales` (SA, SB) selects the block-scaled oracle.
+    Returns (tflops, seconds, rows, threads)."""
     import oracle
     A0 = A if A.ndim == 2 else A[0]
     B0 = B if B.ndim == 2 else B[0]
+    if scales is None:
+        def run(rows):
+            oracle.gemm_nt(A0[:rows], B0, dtype=dtype)
+    else:
+        SA0 = scales[0] if scales[0].ndim == 2 else scales[0][0]
+        SB0 = scales[1] if scales[1].ndim == 2 else scales[1][0]
+
+        def run(rows):
+            oracle.gemm_nt_mx(A0[:rows], SA0[:rows], B0, SB0, dtype=dtype)
     probe = min(8, A0.shape[0])
-    oracle.gemm_nt(A0[:1], B0, dtype=dtype)  # thread pool start-up
+    run(1)  # thread pool start-up
     t0 = time.perf_counter()
-    oracle.gemm_nt(A0[:probe], B0, dtype=dtype)
+    run(probe)
     per_row = max(time.perf_counter() - t0, 1e-4) / probe
     rows = int(max(1, min(A0.shape[0], target_s / per_row)))
     t0 = time.perf_counter()
-    oracle.gemm_nt(A0[:rows], B0, dtype=dtype)
+    run(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * B0.shape[0] * A0.shape[1]
     return flops / dt / 1e12, dt, rows, oracle.max_threads()
@@ -189,11 +199,12 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     A, B = workloads.workload_inputs(w.name, args.ab_dtype)
+    scales = mx_scales(w) if args.mx else None
     per_step = max(1.0, args.cpu_seconds / 5)
     vals = []
     rows_used = None
     for i in range(args.warmup + args.steps):
-        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, per_step, args.ab_dtype)
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, per_step, args.ab_dtype, scales)
         if i >= args.warmup:
             vals.append((tf, dt))
             rows_used = rows
@@ -205,7 +216,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, None, args.ab_dtype, args.out_dtype),
+        "config": workload_config(w, None, args.ab_dtype, args.out_dtype, mx=args.mx),
         "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -214,7 +225,20 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K"):
+def mx_scales(w):
+    """Seeded block scales of the workload: (batch, rows, ceil(K/32)) E8M0
+    bytes uniform in 120..134 (2^-7..2^7), A's then B's."""
+    import numpy as np
+    rng = np.random.default_rng(w.seed + 7)
+    kb = (w.K + 31) // 32
+    sa = rng.integers(120, 135, size=(w.batch, w.M, kb)).astype(np.uint8)
+    sb = rng.integers(120, 135, size=(w.batch, w.N, kb)).astype(np.uint8)
+    if w.batch == 1:
+        sa, sb = sa[0], sb[0]
+    return sa, sb
+
+
+def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K", mx=False):
     cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) %s row-major, "
                        "fp32 accumulate, %s Out" % (
                            w.name, w.description, "%d," % w.batch if w.batch > 1 else "", w.M, w.K,
@@ -230,6 +254,9 @@ def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", 
     if flush is not None:
         cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (alg_bytes / 2 ** 20)
                      if not flush else "L2 flushed between timed steps (256 MiB write)")
+    if mx:
+        cfg["block_scales"] = ("one E8M0 scale per 32 K elements of each row of A and B, uniform 2^-7..2^7 "
+                               "(seed + 7), packed into the atom layout once before timing")
     return cfg
 
 
@@ -253,7 +280,14 @@ def main():
                     help="element type of A and B (bf16, e4m3, e5m2: the same draws rounded to that type)")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of Out (16-bit: fp32 accumulator rounded to nearest even)")
+    ap.add_argument("--mx", action="store_true",
+                    help="block-scaled 8-bit product (needs --ab-dtype e4m3 or e5m2): one E8M0 scale per 32 K "
+                         "elements of each row, drawn uniformly from 2^-7..2^7 and packed once before timing")
     args = ap.parse_args()
+    if args.mx and args.ab_dtype not in ("e4m3", "e5m2"):
+        ap.error("--mx needs --ab-dtype e4m3 or e5m2")
+    if args.mx and (args.a_major != "K" or args.b_major != "K"):
+        ap.error("--mx takes K-major operands only")
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     w = workloads.WORKLOADS[args.workload]
@@ -303,8 +337,19 @@ def main():
     sA, sB, sO = (w.M * w.K, w.N * w.K, w.M * w.N) if batched else (0, 0, 0)
     majors = {"K": gnt.Major.K, "MN": gnt.Major.MN}
 
+    scales = mx_scales(w) if args.mx else None
+    if args.mx:
+        sa_plain = torch.from_numpy(scales[0]).cuda()
+        sb_plain = torch.from_numpy(scales[1]).cuda()
+        sa_packed = gnt.pack_mx_scales(sa_plain, w.K)
+        sb_packed = gnt.pack_mx_scales(sb_plain, w.K)
+
     def step():
-        if not default_layout:
+        if args.mx:
+            gnt.gemm_nt_mx(a.data_ptr(), sa_packed.data_ptr(), b.data_ptr(), sb_packed.data_ptr(), out.data_ptr(),
+                           codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB,
+                           sO, path, sh)
+        elif not default_layout:
             gnt.gemm_nt_batched_major(a.data_ptr(), majors[args.a_major], b.data_ptr(), majors[args.b_major],
                                       out.data_ptr(), codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K,
                                       lda, ldb, w.N, nb, sA, sB, sO, path, sh)
@@ -316,8 +361,10 @@ def main():
                                    codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB, sO,
                                    path, sh)
 
-    # algorithmic bytes: A and B read once, Out written once
+    # algorithmic bytes: A and B (and their block scales) read once, Out written once
     alg_bytes = float(w.batch) * (ab_es * w.M * w.K + ab_es * w.N * w.K + out.element_size() * w.M * w.N)
+    if args.mx:
+        alg_bytes += float(w.batch) * (w.M + w.N) * ((w.K + 31) // 32)
     flush = alg_bytes <= 2 * L2_BYTES
     scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
 
@@ -413,7 +460,19 @@ def main():
         bt = b if b_mn else b.transpose(-1, -2)
         mm = torch.bmm if batched else torch.mm
         cub_fn = None
-        if f8:
+        if args.mx:
+            # cuBLAS's block-scaled path: its 128 x 4 blocked scale layout is
+            # the library's atom layout
+            if not batched:
+                try:
+                    e8 = torch.float8_e8m0fnu
+                    csa, csb = sa_packed.view(e8), sb_packed.view(e8)
+                    torch._scaled_mm(al, bt, scale_a=csa, scale_b=csb, out_dtype=torch.float32)
+                    cub_fn, cub_out = (lambda: torch._scaled_mm(al, bt, scale_a=csa, scale_b=csb,
+                                                                out_dtype=torch.float32)), "f32"
+                except (TypeError, RuntimeError, NotImplementedError, AttributeError):
+                    cub_fn = None
+        elif f8:
             # cuBLAS's 8-bit path: scaled matmul with unit scales (2-D only;
             # it wants the second operand column-major, which B^T of a
             # row-major B is)
@@ -434,7 +493,8 @@ def main():
         if cub_fn is not None:
             cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
             cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
-                      "call": ("torch._scaled_mm(A, B^T, unit scales) -> f32 Out" if f8 else
+                      "call": ("torch._scaled_mm(A, B^T, E8M0 block scales) -> f32 Out" if args.mx else
+                               "torch._scaled_mm(A, B^T, unit scales) -> f32 Out" if f8 else
                                "torch.%s(A, B^T%s) -> %s Out" % ("bmm" if batched else "mm",
                                                                 ", out_dtype=float32" if cub_out == "f32" else "",
                                                                 cub_out)),
@@ -446,8 +506,20 @@ def main():
     hb = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
     ho = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
 
+    if args.mx:
+        hsa = torch.from_numpy(scales[0]).pin_memory()
+        hsb = torch.from_numpy(scales[1]).pin_memory()
+
     def e2e_step():
-        if default_types and default_layout:
+        if args.mx:
+            # the call a user with host data makes: plain scales in, packed on the device
+            a.copy_(ha, non_blocking=True)
+            b.copy_(hb, non_blocking=True)
+            sa_plain.copy_(hsa, non_blocking=True)
+            sb_plain.copy_(hsb, non_blocking=True)
+            gnt.gemm_nt_mx_tensors(a, sa_plain, b, sb_plain, out=out, path=path, stream=stream)
+            ho.copy_(out, non_blocking=True)
+        elif default_types and default_layout:
             gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
                                           b.data_ptr(), out.data_ptr(), w.M, w.N, w.K, w.batch, sh)
         else:
@@ -500,7 +572,7 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, args.cpu_seconds, args.ab_dtype)
+        tf, dt, rows, threads = oracle_cpu_sample(w, A, B, args.cpu_seconds, args.ab_dtype, scales)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": "%d full rows of batch 0 (%d x %d outputs, K=%d), %.1f s" % (
                    rows, rows, w.N, w.K, dt)}
@@ -509,14 +581,17 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.ab_dtype, "data": "synthetic",
-        "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes, args.a_major, args.b_major),
+        "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes, args.a_major, args.b_major,
+                                  args.mx),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+                "h2d_bytes_per_step": int(A.nbytes + B.nbytes + (scales[0].nbytes + scales[1].nbytes
+                                                                  if args.mx else 0)),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "clocks": clocks,
         "gpu_launches": args.steps,
+        "block_scaled": bool(args.mx),
         "host_us_per_step": host_us,
         "path": args.path,
         "ms_per_step_median": step_ms_median,

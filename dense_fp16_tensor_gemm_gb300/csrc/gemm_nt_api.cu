@@ -297,8 +297,11 @@ bool tma_ok(const Problem& q)
 
 gemm_path_t select_path(const Problem& q)
 {
-    if (q.mx())  // block-scaled: the one-CTA tcgen05 kernel, swapped for small M
-        return q.M <= 64 && q.N >= 1024 ? GEMM_PATH_SKINNY : GEMM_PATH_TC05;
+    if (q.mx()) {  // block-scaled: no warp kernel; swapped for small M, pairs for large tiles
+        if (q.M <= 64 && q.N >= 1024)
+            return GEMM_PATH_SKINNY;
+        return q.M > 128 && q.N > 128 ? GEMM_PATH_TC05_PAIR : GEMM_PATH_TC05;
+    }
     if (!tma_ok(q))
         return GEMM_PATH_MMASYNC;
     if (q.M <= 64 && q.N >= 1024)
@@ -362,6 +365,23 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Block scales as a tensor of `atoms` 512-byte atoms, each 4 rows of 128
+// bytes: a box {128, 4} at row 4*i is atom i (unswizzled, so shared memory
+// receives the atom's bytes in order).
+bool encode_scale_map(CUtensorMap* map, const void* base, int64_t atoms)
+{
+    auto enc = encode_fn();
+    if (!enc || atoms <= 0 || atoms > (int64_t(1) << 29))
+        return false;
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(4 * atoms), 1};
+    cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(4 * atoms * 128)};
+    cuuint32_t box[3] = {128, 4, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
@@ -538,6 +558,8 @@ bool pair_split(int64_t ntiles, int num_kb, int pairs, int out_type)
 
 int pair_plan_width(const Problem& q, const DeviceState& d)
 {
+    if (q.mx())
+        return 192;  // two 192-column accumulators leave TMEM room for the scale slots
     if (q.b_mn())
         return 256;  // each CTA's half of B must be whole 64-row chunks
     const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
@@ -618,7 +640,21 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     // Out rows 32-byte aligned: the epilogue stores without staging
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
                         q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
-    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.is_f8(), stream) != cudaSuccess)
+    if (q.mx()) {
+        // each CTA stages its A rows' atom and all of the tile's B atoms through
+        // tensor maps over the packed scales (atoms as rows of 128 bytes)
+        CUtensorMap tmsa, tmsb;
+        const int64_t na = (q.sA == 0 ? 1 : q.batch) * mx_scale_bytes(q.M, q.K) / 512;
+        const int64_t nb = (q.sB == 0 ? 1 : q.batch) * mx_scale_bytes(q.N, q.K) / 512;
+        if (!encode_scale_map(&tmsa, q.SA, na) || !encode_scale_map(&tmsb, q.SB, nb))
+            return GEMM_ERR_CUDA;
+        p.sf_x_bstride = q.sA == 0 ? 0 : mx_scale_bytes(q.M, q.K);
+        p.sf_y_bstride = q.sB == 0 ? 0 : mx_scale_bytes(q.N, q.K);
+        if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream, &tmsa, &tmsb) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_OK;
+    }
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -684,7 +720,7 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         return zero_out(q, stream);
     if (path == GEMM_PATH_AUTO)
         path = select_path(q);
-    if (q.mx() && path != GEMM_PATH_TC05 && path != GEMM_PATH_SKINNY)
+    if (q.mx() && path == GEMM_PATH_MMASYNC)
         return GEMM_ERR_NOT_SUPPORTED;
     switch (path) {
     case GEMM_PATH_MMASYNC:
@@ -935,7 +971,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     // Out rows 32-byte aligned: the epilogue stores without staging
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
                         q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
-    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.is_f8(), stream) != cudaSuccess)
+    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }

@@ -106,7 +106,8 @@ constexpr size_t pair_workspace_bytes(int pairs)
 // rows).  direct: epilogue without shared-memory staging and a 7-stage ring;
 // needs Out rows 32-byte aligned and no split (p.sk_pairs == 0).
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
-                             bool direct, bool f8, cudaStream_t stream);
+                             bool direct, int kind, cudaStream_t stream, const CUtensorMap* tmsa = nullptr,
+                             const CUtensorMap* tmsb = nullptr);
 
 // in_type: the A/B element type, a gemm_dtype_t value (fp16, bf16, E4M3, E5M2).
 cudaError_t mmasync_launch(const MmaParams& p, int in_type, cudaStream_t stream);

@@ -71,4 +71,28 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint32_t alo, uint32_
         : "memory");
 }
 
+// The pair forms (cta_group::2), issued by the leader CTA of a pair: the copy
+// moves each CTA's atom at this shared offset into its own TMEM; each half of
+// the MMA reads the scales of its 128 rows of A, and of all N rows of B, from
+// its own CTA's TMEM.
+__device__ __forceinline__ void tc_cp_atom_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair_mx(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo,
+                                               uint32_t bhi, uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %8, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %5, [%6], [%7], p;\n\t}" ::"r"(
+            d_tmem),
+        "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 }  // namespace gnt

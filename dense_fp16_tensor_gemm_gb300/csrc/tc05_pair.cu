@@ -20,6 +20,7 @@
 // Every wait is bounded as in the single-CTA kernel.
 #include <algorithm>
 
+#include "ptx_mx.cuh"
 #include "tc05_common.cuh"
 
 namespace gnt {
@@ -30,8 +31,7 @@ using namespace tc;
 
 constexpr int kPairThreads = 320;
 constexpr int A_BYTES = BM * BK * 2;           // this CTA's 128 rows of A
-constexpr int TMEM_COLS = 512;                 // two accumulators, 256 columns apart
-constexpr int kAccStride = 256;
+constexpr int TMEM_COLS = 512;                 // two accumulators (and, block-scaled, the scale slots)
 constexpr int BAR_BYTES = 256;
 constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CTAs
 
@@ -40,11 +40,25 @@ constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CT
 // number of rounds over the pairs.  DIRECT: the epilogue stores straight from
 // TMEM-loaded registers (Out rows 32-byte aligned), which frees the 32 KB of
 // staging for a seventh pipeline stage.
-template <int PBN, bool DIRECT>
+// KIND: 0 16-bit inputs, 1 8-bit, 2 8-bit block-scaled.  Block-scaled, each
+// CTA's stage also holds the scale atom of its 128 rows of A and the atoms of
+// all of the tile's B rows (each half of the pair MMA reads B's scales from its
+// own CTA's TMEM): up to 3 atoms for a window of PBN <= 256 rows that starts on
+// a 32-row boundary.  TMEM then holds the accumulators PBN columns apart and,
+// from column 2*PBN, 16 scale columns per stage (A atom, then the B atoms).
+constexpr int kSfAtomsB = 3;
+
+template <int PBN, bool DIRECT, int KIND = 0>
 struct PairCfg {
+    static constexpr bool MX = KIND == 2;
     static constexpr int STAGES = DIRECT ? 7 : 6;
     static constexpr int B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SF_BYTES = MX ? 512 * (1 + kSfAtomsB) : 0;
+    static constexpr int DATA_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+    static constexpr int ACC_STRIDE = MX ? PBN : 256;
+    static constexpr int SF_COL = 2 * PBN;
+    static constexpr int SF_COLS = 16;
     static constexpr int EPI_BYTES = DIRECT ? 0 : 8 * 32 * 32 * 4;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(2 * BM, PBN);
@@ -54,6 +68,7 @@ struct PairCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(B_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
+    static_assert(!MX || SF_COL + SF_COLS * STAGES <= TMEM_COLS, "scale slots fit in TMEM");
 };
 
 // Pair tiles (256 rows x PBN columns): tiles [0, sk_first) whole and round-robin
@@ -214,14 +229,18 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
 }
 
 // F8: 8-bit A and B (kind::f8f6f4, 128 elements of K per 128-byte stage row).
-template <int PBN, bool DIRECT, bool F8>
+template <int PBN, bool DIRECT, int KIND>
 __global__ void __launch_bounds__(kPairThreads, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                     const __grid_constant__ CUtensorMap tmsa, const __grid_constant__ CUtensorMap tmsb,
                      const TcParams p)
 {
-    using C = PairCfg<PBN, DIRECT>;
+    using C = PairCfg<PBN, DIRECT, KIND>;
+    constexpr bool F8 = KIND != 0;
+    constexpr bool MX = C::MX;
     constexpr int kStages = C::STAGES;
     constexpr int KE = F8 ? 2 * BK : BK;  // elements of K per stage
+    constexpr int kAccStride = C::ACC_STRIDE;
     constexpr int B_BYTES = C::B_BYTES;
     constexpr int STAGE_BYTES = C::STAGE_BYTES;
     constexpr int EPI_BYTES = C::EPI_BYTES;
@@ -229,6 +248,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* as = smem;
     uint8_t* bs = smem + kStages * A_BYTES;
+    uint8_t* sfs = bs + kStages * B_BYTES;  // block-scaled: per stage the A atom, then the B atoms
     float* epi = reinterpret_cast<float*>(smem + kStages * STAGE_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES + EPI_BYTES);
     uint64_t* full = bars;
@@ -305,8 +325,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     if (!drop) {
                         const uint32_t fb_local = smem_u32(&full[stage]);
                         const uint32_t fb_leader = mapa_shared(fb_local, 0);
+                        // block-scaled: B atoms [y0/128, (y0+PBN-1)/128] of the tile
+                        const int nb_atoms = MX ? (s.y0 + PBN - 1) / BM - s.y0 / BM + 1 : 0;
                         if (leader) {
-                            mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+                            mbar_arrive_expect_tx(fb_local, 2 * (C::DATA_BYTES + (MX ? 512 * (1 + nb_atoms) : 0)));
                             filled |= 1u << stage;
                             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         }
@@ -314,6 +336,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                                s.x0, s.b * p.x_bmul);
                         load_operand<PBN / 2, true>(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, p.y_mn,
                                                     kb * KE, yb, s.b * p.y_bmul);
+                        if constexpr (MX) {
+                            // atoms as 4 rows of 128 bytes in the scale maps; an atom
+                            // past the packed array reads as zeros (rows past N only)
+                            const uint32_t sfd = smem_u32(sfs + stage * C::SF_BYTES);
+                            const long long ia = (s.b * p.sf_x_bstride) / 512 +
+                                                 static_cast<long long>(s.x0 / BM) * p.num_kb + kb;
+                            tma_load_3d_pair(sfd, &tmsa, fb_leader, 0, static_cast<int>(4 * ia), 0);
+                            const long long ib0 = (s.b * p.sf_y_bstride) / 512 + kb;
+                            for (int a = 0; a < nb_atoms; ++a)
+                                tma_load_3d_pair(sfd + 512 * (1 + a), &tmsb, fb_leader, 0,
+                                                 static_cast<int>(4 * (ib0 + static_cast<long long>(s.y0 / BM + a) *
+                                                                                  p.num_kb)),
+                                                 0);
+                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -342,7 +378,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // first must fit in one MMA's time (~128 cycles at N = 256).  The
             // loop therefore steps stage addresses and descriptor words by
             // additions, and leaves the line only when a wait has to sleep.
-            const uint32_t idesc = C::IDESC | p.idesc_bits;
+            const uint32_t idesc = (MX ? idesc_mx(2 * BM, PBN) : C::IDESC) | p.idesc_bits;
+            const uint32_t sf_smem0 = smem_u32(sfs);
             const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
             const DescWords da = desc_words(smem_u32(as), p.x_mn != 0);
             const DescWords db = desc_words(smem_u32(bs), p.y_mn != 0);
@@ -363,6 +400,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccStride);
+                const int nb_atoms = MX ? (s.y0 + PBN - 1) / BM - s.y0 / BM + 1 : 0;
+                const uint32_t y_sf_off = static_cast<uint32_t>((s.y0 % BM) / 32);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (!wait_bounded(fa, phase, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
@@ -370,10 +409,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    tc_mma_pair_w<F8>(d_tmem, alo, da.hi, blo, db.hi, idesc, kb != s.kb0);
+                    if constexpr (MX) {
+                        // scale slot of the stage: refilled only after the stage's
+                        // previous MMAs completed; copies are ordered before the MMAs
+                        const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + C::SF_COLS * stage);
+                        const uint32_t sfd = sf_smem0 + static_cast<uint32_t>(stage * C::SF_BYTES);
+                        tc_cp_atom_pair(sft, atom_desc(sfd));
+                        for (int a = 0; a < nb_atoms; ++a)
+                            tc_cp_atom_pair(sft + 4 + 4 * a, atom_desc(sfd + 512 * (1 + a)));
 #pragma unroll
-                    for (int k = 1; k < BK / 16; ++k)
-                        tc_mma_pair_w<F8>(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi, idesc, 1u);
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma_pair_mx(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi,
+                                           idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4),
+                                           sft, sft + 4 + y_sf_off, (k > 0 || kb != s.kb0) ? 1u : 0u);
+                    } else {
+                        tc_mma_pair_w<F8>(d_tmem, alo, da.hi, blo, db.hi, idesc, kb != s.kb0);
+#pragma unroll
+                        for (int k = 1; k < BK / 16; ++k)
+                            tc_mma_pair_w<F8>(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi, idesc,
+                                              1u);
+                    }
                     if (!skip_release)
                         tc_commit_pair_mc(ea, 0x3);
                     skip_release = false;
@@ -478,18 +533,18 @@ cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaun
     return cfg;
 }
 
-template <int PBN, bool DIRECT, bool F8>
+template <int PBN, bool DIRECT, int KIND>
 cudaError_t configure_kind(int* max_pairs)
 {
-    using C = PairCfg<PBN, DIRECT>;
-    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel<PBN, DIRECT, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    using C = PairCfg<PBN, DIRECT, KIND>;
+    cudaError_t e = cudaFuncSetAttribute(tc05_pair_kernel<PBN, DIRECT, KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT, F8>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT, KIND>, &cfg);
     if (e != cudaSuccess)
         return e;
     *max_pairs = std::min(*max_pairs, n);
@@ -499,19 +554,27 @@ cudaError_t configure_kind(int* max_pairs)
 template <int PBN, bool DIRECT>
 cudaError_t configure_one(int* max_pairs)
 {
-    cudaError_t e = configure_kind<PBN, DIRECT, false>(max_pairs);
-    return e == cudaSuccess ? configure_kind<PBN, DIRECT, true>(max_pairs) : e;
+    cudaError_t e = configure_kind<PBN, DIRECT, 0>(max_pairs);
+    return e == cudaSuccess ? configure_kind<PBN, DIRECT, 1>(max_pairs) : e;
+}
+
+template <int PBN, bool DIRECT, int KIND>
+cudaError_t launch_kind(const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmsa,
+                        const CUtensorMap& tmsb, const TcParams& p, int pairs, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT, KIND>::SMEM, stream, attr);
+    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, KIND>, tma, tmb, tmsa, tmsb, p);
 }
 
 template <int PBN, bool DIRECT>
-cudaError_t launch_one(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, bool f8,
+cudaError_t launch_one(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int kind,
                        cudaStream_t stream)
 {
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT>::SMEM, stream, attr);
-    if (f8)
-        return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, true>, tma, tmb, p);
-    return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, false>, tma, tmb, p);
+    // the scale maps are not read unless kind is 2
+    if (kind == 1)
+        return launch_kind<PBN, DIRECT, 1>(tma, tmb, tma, tmb, p, pairs, stream);
+    return launch_kind<PBN, DIRECT, 0>(tma, tmb, tma, tmb, p, pairs, stream);
 }
 
 }  // namespace
@@ -525,6 +588,8 @@ cudaError_t tc05_pair_configure(int* max_pairs)
     if (e == cudaSuccess) e = configure_one<256, true>(&n);
     if (e == cudaSuccess) e = configure_one<224, true>(&n);
     if (e == cudaSuccess) e = configure_one<192, true>(&n);
+    if (e == cudaSuccess) e = configure_kind<192, true, 2>(&n);
+    if (e == cudaSuccess) e = configure_kind<192, false, 2>(&n);
     if (e != cudaSuccess)
         return e;
     *max_pairs = n;
@@ -532,20 +597,29 @@ cudaError_t tc05_pair_configure(int* max_pairs)
 }
 
 cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, const TcParams& p, int pairs, int pbn,
-                             bool direct, bool f8, cudaStream_t stream)
+                             bool direct, int kind, cudaStream_t stream, const CUtensorMap* tmsa,
+                             const CUtensorMap* tmsb)
 {
+    if (kind == 2) {
+        // block-scaled: 192-wide tiles leave TMEM room for the scale slots
+        if (pbn != 192 || !tmsa || !tmsb)
+            return cudaErrorInvalidValue;
+        if (direct)
+            return launch_kind<192, true, 2>(tma, tmb, *tmsa, *tmsb, p, pairs, stream);
+        return launch_kind<192, false, 2>(tma, tmb, *tmsa, *tmsb, p, pairs, stream);
+    }
     if (direct) {
         switch (pbn) {
-        case 256: return launch_one<256, true>(tma, tmb, p, pairs, f8, stream);
-        case 224: return launch_one<224, true>(tma, tmb, p, pairs, f8, stream);
-        case 192: return launch_one<192, true>(tma, tmb, p, pairs, f8, stream);
+        case 256: return launch_one<256, true>(tma, tmb, p, pairs, kind, stream);
+        case 224: return launch_one<224, true>(tma, tmb, p, pairs, kind, stream);
+        case 192: return launch_one<192, true>(tma, tmb, p, pairs, kind, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (pbn) {
-    case 256: return launch_one<256, false>(tma, tmb, p, pairs, f8, stream);
-    case 224: return launch_one<224, false>(tma, tmb, p, pairs, f8, stream);
-    case 192: return launch_one<192, false>(tma, tmb, p, pairs, f8, stream);
+    case 256: return launch_one<256, false>(tma, tmb, p, pairs, kind, stream);
+    case 224: return launch_one<224, false>(tma, tmb, p, pairs, kind, stream);
+    case 192: return launch_one<192, false>(tma, tmb, p, pairs, kind, stream);
     default: return cudaErrorInvalidValue;
     }
 }

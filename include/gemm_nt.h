@@ -209,11 +209,12 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
  * has one matrix of scales.  gemm_nt_mx_pack_scales makes this layout from
  * the plain one.
  *
- * path: GEMM_PATH_AUTO, GEMM_PATH_TC05 (128 x 64 or 128 x 128 tiles) or
- * GEMM_PATH_SKINNY (M <= 64; chosen by AUTO for M <= 64 and N >= 1024).  The
- * CTA-pair and warp kernels take no scales (GEMM_ERR_NOT_SUPPORTED), nor does
- * a layout the tensor-core kernels cannot read (unaligned bases, pitches not
- * multiples of 16 bytes).  Null SA / SB with K > 0, a 16-bit ab_type, or
+ * path: GEMM_PATH_AUTO, GEMM_PATH_TC05 (128 x 64 or 128 x 128 tiles),
+ * GEMM_PATH_SKINNY (M <= 64) or GEMM_PATH_TC05_PAIR (256 x 192 tiles on CTA
+ * pairs); AUTO takes SKINNY for M <= 64 and N >= 1024, the pairs for M and N
+ * above 128, else TC05.  The warp kernel takes no scales
+ * (GEMM_ERR_NOT_SUPPORTED), nor does any kernel a layout the tensor-core
+ * kernels cannot read (unaligned bases, pitches not multiples of 16 bytes).  Null SA / SB with K > 0, a 16-bit ab_type, or
  * unaligned SA / SB: GEMM_ERR_INVALID_VALUE; Out overlapping A, B, SA or SB:
  * GEMM_ERR_OVERLAP.  Other arguments and errors as gemm_nt_batched_ex.
  */

@@ -76,7 +76,7 @@ def test_pack_matches_the_layout():
 
 @pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("ab", F8)
-@pytest.mark.parametrize("path", [P.AUTO, P.TC05], ids=lambda p: p.name)
+@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR], ids=lambda p: p.name)
 def test_ragged_batched(path, ab, out):
     """Several tiles each way, ragged M and N, K = 400 (three 128-element
     stages, a 16-element tail, a partial 32-element scale block), batch 2."""
@@ -89,7 +89,7 @@ def test_ragged_batched(path, ab, out):
 
 
 @pytest.mark.parametrize("ab", F8)
-@pytest.mark.parametrize("path", [P.TC05, P.SKINNY], ids=lambda p: p.name)
+@pytest.mark.parametrize("path", [P.TC05, P.SKINNY, P.TC05_PAIR], ids=lambda p: p.name)
 def test_integer_inputs_exact(path, ab):
     """Integers in [-4, 4] and scales 2^-3..2^3: every partial sum is exact."""
     M = 48 if path == P.SKINNY else 200
@@ -124,11 +124,23 @@ def test_shared_operand_and_padded_pitch():
     check_tol(run_mx(A, SA, B, SB, "e5m2", "f32", P.AUTO, shared_b=True, lda=544), ref, absdot, "f32", "shared B")
 
 
-def test_long_k_few_tiles():
-    """Few tiles and K = 16384: the one-CTA kernel splits K (stream-K)."""
+@pytest.mark.parametrize("path", [P.TC05, P.TC05_PAIR], ids=lambda p: p.name)
+def test_long_k_few_tiles(path):
+    """Few tiles and K = 16384: both kernels split K (stream-K; the pair
+    kernel through its workspace slices)."""
     A, SA, B, SB = draw(1, 256, 256, 16384, "e4m3", seed=506, sigma=0.25)
     ref, absdot = oracle.gemm_nt_mx(A, SA, B, SB, dtype="e4m3")
-    check_tol(run_mx(A, SA, B, SB, "e4m3", "f32", P.TC05), ref, absdot, "f32", "stream-K")
+    check_tol(run_mx(A, SA, B, SB, "e4m3", "f32", path), ref, absdot, "f32", "stream-K")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 192, 128), (640, 1000, 384), (1000, 576, 256), (130, 1300, 640)])
+def test_pair_tile_windows(M, N, K):
+    """256 x 192 pair tiles whose B rows start at every offset within a
+    128-row scale atom (0, 64; 192 = 64 mod 128) and span two or three atoms,
+    ragged M and N."""
+    A, SA, B, SB = draw(1, M, N, K, "e5m2", seed=M + N + K)
+    ref, absdot = oracle.gemm_nt_mx(A, SA, B, SB, dtype="e5m2")
+    check_tol(run_mx(A, SA, B, SB, "e5m2", "f32", P.TC05_PAIR), ref, absdot, "f32", "pair %dx%dx%d" % (M, N, K))
 
 
 def test_unit_scales_equal_the_unscaled_product():
@@ -152,7 +164,7 @@ def test_torch_wrapper_and_unsupported_paths():
     check_tol(out16.double().cpu().numpy(), ref, absdot, "bf16", "wrapper bf16")
     pa, pb = gnt.pack_mx_scales(sa, 320), gnt.pack_mx_scales(sb, 320)
     o = torch.empty((192, 256), dtype=torch.float32, device="cuda")
-    for path in (P.TC05_PAIR, P.MMASYNC):
+    for path in (P.MMASYNC,):
         with pytest.raises(gnt.GemmError) as e:
             gnt.gemm_nt_mx(a.data_ptr(), pa.data_ptr(), b.data_ptr(), pb.data_ptr(), o.data_ptr(), gnt.DType.E4M3,
                            gnt.DType.F32, 192, 256, 320, 320, 320, 256, 1, 0, 0, 0, path,
