@@ -367,19 +367,24 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
     return r == CUDA_SUCCESS;
 }
 
-// Block scales as a tensor of `atoms` 512-byte atoms, each 4 rows of 128
-// bytes: a box {128, 4} at row 4*i is atom i (unswizzled, so shared memory
-// receives the atom's bytes in order).
-bool encode_scale_map(CUtensorMap* map, const void* base, int64_t atoms)
+// Block scales of `mats` matrices (rows row blocks of 128, K of K) as a 4-D
+// tensor {128 bytes, 4 rows, K block group, row block}: one atom is {128, 4},
+// and a box takes box_kg consecutive K block groups of box_rb consecutive row
+// blocks (unswizzled, so shared memory receives the atoms in that order).
+bool encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t mats, int box_rb,
+                      int box_kg)
 {
     auto enc = encode_fn();
-    if (!enc || atoms <= 0 || atoms > (int64_t(1) << 29))
+    const int64_t kg = (K + 127) / 128, rb = (rows + 127) / 128 * mats;
+    if (!enc || kg <= 0 || rb <= 0 || kg > (int64_t(1) << 31) || rb > (int64_t(1) << 31))
         return false;
-    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(4 * atoms), 1};
-    cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(4 * atoms * 128)};
-    cuuint32_t box[3] = {128, 4, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[4] = {128, 4, static_cast<cuuint64_t>(kg), static_cast<cuuint64_t>(rb)};
+    cuuint64_t strides[3] = {128, 512, static_cast<cuuint64_t>(kg * 512)};
+    if (box_kg < 1 || box_kg > kg || box_rb < 1 || box_rb > rb)
+        return false;
+    cuuint32_t box[4] = {128, 4, static_cast<cuuint32_t>(box_kg), static_cast<cuuint32_t>(box_rb)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -641,12 +646,16 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
                         q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
     if (q.mx()) {
-        // each CTA stages its A rows' atom and all of the tile's B atoms through
-        // tensor maps over the packed scales (atoms as rows of 128 bytes)
+        // each CTA stages its A rows' atom and the tile's two B atoms through
+        // tensor maps over the packed scales
+        // boxes of up to 8 K block groups and 2 B row blocks, never larger than
+        // the scale tensors themselves
         CUtensorMap tmsa, tmsb;
-        const int64_t na = (q.sA == 0 ? 1 : q.batch) * mx_scale_bytes(q.M, q.K) / 512;
-        const int64_t nb = (q.sB == 0 ? 1 : q.batch) * mx_scale_bytes(q.N, q.K) / 512;
-        if (!encode_scale_map(&tmsa, q.SA, na) || !encode_scale_map(&tmsb, q.SB, nb))
+        const int64_t mats_b = q.sB == 0 ? 1 : q.batch;
+        p.sf_box_kg = static_cast<int>(std::min<int64_t>(8, (q.K + 127) / 128));
+        p.sf_box_rb = static_cast<int>(std::min<int64_t>(2, (q.N + 127) / 128 * mats_b));
+        if (!encode_scale_map(&tmsa, q.SA, q.M, q.K, q.sA == 0 ? 1 : q.batch, 1, p.sf_box_kg) ||
+            !encode_scale_map(&tmsb, q.SB, q.N, q.K, mats_b, p.sf_box_rb, p.sf_box_kg))
             return GEMM_ERR_CUDA;
         p.sf_x_bstride = q.sA == 0 ? 0 : mx_scale_bytes(q.M, q.K);
         p.sf_y_bstride = q.sB == 0 ? 0 : mx_scale_bytes(q.N, q.K);

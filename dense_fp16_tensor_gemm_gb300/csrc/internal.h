@@ -64,6 +64,8 @@ struct TcParams {
     const uint8_t* sf_y;
     long long sf_x_bstride;  // bytes between batches (0: shared)
     long long sf_y_bstride;
+    int sf_box_kg;           // CTA-pair kernel: K block groups per scale box (<= 8, <= the tensor's)
+    int sf_box_rb;           // CTA-pair kernel: row blocks per B scale box (1 or 2)
 };
 
 struct MmaParams {

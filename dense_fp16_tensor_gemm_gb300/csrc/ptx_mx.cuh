@@ -17,6 +17,7 @@
 // is the same for either operand.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 
 namespace gnt {
 
@@ -68,6 +69,18 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint32_t alo, uint32_
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], da, db, %5, [%6], [%7], p;\n\t}" ::"r"(
             d_tmem),
         "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 4-D tiled load of scale atoms into this CTA's shared memory, completing on a
+// barrier in either CTA of the pair (the pair kernel's stage barrier).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 

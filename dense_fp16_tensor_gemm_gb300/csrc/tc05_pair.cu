@@ -40,35 +40,43 @@ constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CT
 // number of rounds over the pairs.  DIRECT: the epilogue stores straight from
 // TMEM-loaded registers (Out rows 32-byte aligned), which frees the 32 KB of
 // staging for a seventh pipeline stage.
-// KIND: 0 16-bit inputs, 1 8-bit, 2 8-bit block-scaled.  Block-scaled, each
-// CTA's stage also holds the scale atom of its 128 rows of A and the atoms of
-// all of the tile's B rows (each half of the pair MMA reads B's scales from its
-// own CTA's TMEM): up to 3 atoms for a window of PBN <= 256 rows that starts on
-// a 32-row boundary.  TMEM then holds the accumulators PBN columns apart and,
-// from column 2*PBN, 16 scale columns per stage (A atom, then the B atoms).
-constexpr int kSfAtomsB = 3;
+// KIND: 0 16-bit inputs, 1 8-bit, 2 8-bit block-scaled (PBN = 192 only).
+// Block-scaled, each CTA needs the scale atoms of its 128 rows of A and those
+// of all of the tile's B rows (each half of the pair MMA reads B's scales from
+// its own CTA's TMEM; a 192-row window starts 0 or 64 rows into a 128-row block
+// and so spans exactly two atoms).  They come through a ring of two scale
+// stages, each holding the atoms of kScaleKb consecutive k-blocks (A: 4 KB in
+// one box, B: 8 KB in one box): small per-k-block scale loads beside the data
+// loads slowed the stream down by a third.  TMEM holds the accumulators PBN
+// columns apart and, from column 2*PBN, 16 scale columns per data stage (A
+// atom, then the B atoms), filled by tcgen05.cp before the stage's MMAs.
+constexpr int kSfAtomsB = 2;
+constexpr int kScaleKb = 8;
+constexpr int kScaleStages = 2;
 
 template <int PBN, bool DIRECT, int KIND = 0>
 struct PairCfg {
     static constexpr bool MX = KIND == 2;
     static constexpr int STAGES = DIRECT ? 7 : 6;
     static constexpr int B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
-    static constexpr int SF_BYTES = MX ? 512 * (1 + kSfAtomsB) : 0;
     static constexpr int DATA_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SC_STAGE_BYTES = (1 + kSfAtomsB) * kScaleKb * 512;  // one scale stage
+    static constexpr int SC_BYTES = MX ? kScaleStages * SC_STAGE_BYTES : 0;
     static constexpr int ACC_STRIDE = MX ? PBN : 256;
     static constexpr int SF_COL = 2 * PBN;
     static constexpr int SF_COLS = 16;
     static constexpr int EPI_BYTES = DIRECT ? 0 : 8 * 32 * 32 * 4;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SC_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(2 * BM, PBN);
     // epilogue warps 2-5 store columns [0, SPLIT), warps 6-9 [SPLIT, PBN)
     static constexpr int SPLIT = ((PBN / 32 + 1) / 2) * 32;
     static_assert(PBN % 32 == 0 && PBN <= 256 && PBN >= 128, "tile width");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert((3 * STAGES + 6 + 2 * kScaleStages) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(B_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
     static_assert(!MX || SF_COL + SF_COLS * STAGES <= TMEM_COLS, "scale slots fit in TMEM");
+    static_assert(!MX || PBN == 192, "block-scaled tiles are 192 wide (two B atoms per stage)");
 };
 
 // Pair tiles (256 rows x PBN columns): tiles [0, sk_first) whole and round-robin
@@ -229,8 +237,9 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
 }
 
 // F8: 8-bit A and B (kind::f8f6f4, 128 elements of K per 128-byte stage row).
+// Block-scaled kernels add warp 10, which copies the scale atoms into TMEM.
 template <int PBN, bool DIRECT, int KIND>
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const __grid_constant__ CUtensorMap tmsa, const __grid_constant__ CUtensorMap tmsb,
                      const TcParams p)
@@ -248,9 +257,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* as = smem;
     uint8_t* bs = smem + kStages * A_BYTES;
-    uint8_t* sfs = bs + kStages * B_BYTES;  // block-scaled: per stage the A atom, then the B atoms
-    float* epi = reinterpret_cast<float*>(smem + kStages * STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES + EPI_BYTES);
+    // block-scaled: scale stage t holds A's atoms [t][k] then B's [t][rb][k]
+    uint8_t* sfs = smem + kStages * STAGE_BYTES;
+    float* epi = reinterpret_cast<float*>(sfs + C::SC_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sfs + C::SC_BYTES + EPI_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* tfull = bars + 2 * kStages;
@@ -258,6 +268,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* sc_full = drain + 2;  // leader: both CTAs' scale bytes of scale stage t
+    uint64_t* sc_empty = sc_full + kScaleStages;  // each CTA: the copies that read stage t are done
+    uint64_t* sf_ready = sc_empty + kScaleStages;  // leader: data stage s's scales are in TMEM
+    uint64_t* cdrain = sf_ready + kStages;         // leader: the copier's last copies are done
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -274,10 +288,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             mbar_init(smem_u32(&tempty[b]), kTemptyArrivals);
         }
         mbar_init(smem_u32(drain), 1);
+        for (int t = 0; t < kScaleStages; ++t) {
+            mbar_init(smem_u32(&sc_full[t]), 1);
+            mbar_init(smem_u32(&sc_empty[t]), 1);
+        }
+        for (int st = 0; st < kStages; ++st)
+            mbar_init(smem_u32(&sf_ready[st]), 1);
+        mbar_init(smem_u32(cdrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tma);
         tma_prefetch_map(&tmb);
+        if (MX) {
+            tma_prefetch_map(&tmsa);
+            tma_prefetch_map(&tmsb);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));
@@ -309,12 +334,40 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
+            int sst = 0;  // scale stage ring
+            uint32_t sphase = 0, sc_filled = 0, sc_parity = 0;
             bool first = true, ok = true;
             PairIter<PBN> w(p, static_cast<int>(rank));
             Seg s;
             while (ok && w.next(s)) {
                 const int yb = s.y0 + static_cast<int>(rank) * (PBN / 2);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (MX && (kb == s.kb0 || kb % kScaleKb == 0)) {
+                        // the next scale stage: atoms of k-blocks [kb - kb % 8, +8)
+                        if (!wait_bounded(smem_u32(&sc_empty[sst]), sphase ^ 1, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sb_local = smem_u32(&sc_full[sst]);
+                        if (leader) {
+                            // both CTAs' boxes: A's p.sf_box_kg atoms, B's p.sf_box_rb times as many
+                            mbar_arrive_expect_tx(sb_local, 2 * 512 * p.sf_box_kg * (1 + p.sf_box_rb));
+                            sc_filled |= 1u << sst;
+                            sc_parity = (sc_parity & ~(1u << sst)) | (sphase << sst);
+                        }
+                        const uint32_t sb_leader = mapa_shared(sb_local, 0);
+                        const uint32_t sd = smem_u32(sfs + sst * C::SC_STAGE_BYTES);
+                        const int kg0 = kb - kb % kScaleKb;
+                        const int rbx = static_cast<int>((s.b * p.sf_x_bstride) / (512LL * p.num_kb)) + s.x0 / BM;
+                        const int rby = static_cast<int>((s.b * p.sf_y_bstride) / (512LL * p.num_kb)) + s.y0 / BM;
+                        tma_load_4d_pair(sd, &tmsa, sb_leader, 0, 0, kg0, rbx);
+                        tma_load_4d_pair(sd + kScaleKb * 512, &tmsb, sb_leader, 0, 0, kg0, rby);
+                        if (++sst == kScaleStages) {
+                            sst = 0;
+                            sphase ^= 1;
+                        }
+                    }
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
@@ -325,10 +378,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     if (!drop) {
                         const uint32_t fb_local = smem_u32(&full[stage]);
                         const uint32_t fb_leader = mapa_shared(fb_local, 0);
-                        // block-scaled: B atoms [y0/128, (y0+PBN-1)/128] of the tile
-                        const int nb_atoms = MX ? (s.y0 + PBN - 1) / BM - s.y0 / BM + 1 : 0;
                         if (leader) {
-                            mbar_arrive_expect_tx(fb_local, 2 * (C::DATA_BYTES + (MX ? 512 * (1 + nb_atoms) : 0)));
+                            mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
                             filled |= 1u << stage;
                             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         }
@@ -336,20 +387,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                                s.x0, s.b * p.x_bmul);
                         load_operand<PBN / 2, true>(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, p.y_mn,
                                                     kb * KE, yb, s.b * p.y_bmul);
-                        if constexpr (MX) {
-                            // atoms as 4 rows of 128 bytes in the scale maps; an atom
-                            // past the packed array reads as zeros (rows past N only)
-                            const uint32_t sfd = smem_u32(sfs + stage * C::SF_BYTES);
-                            const long long ia = (s.b * p.sf_x_bstride) / 512 +
-                                                 static_cast<long long>(s.x0 / BM) * p.num_kb + kb;
-                            tma_load_3d_pair(sfd, &tmsa, fb_leader, 0, static_cast<int>(4 * ia), 0);
-                            const long long ib0 = (s.b * p.sf_y_bstride) / 512 + kb;
-                            for (int a = 0; a < nb_atoms; ++a)
-                                tma_load_3d_pair(sfd + 512 * (1 + a), &tmsb, fb_leader, 0,
-                                                 static_cast<int>(4 * (ib0 + static_cast<long long>(s.y0 / BM + a) *
-                                                                                  p.num_kb)),
-                                                 0);
-                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -359,6 +396,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             // The leader's full barriers count both CTAs' bytes: waiting for the
             // last fills lets every load of the pair land before either exits.
+            for (int st = 0; st < kScaleStages; ++st) {
+                if (sc_filled & (1u << st)) {
+                    const uint32_t par = (sc_parity >> st) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(smem_u32(&sc_full[st]), par) &&
+                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                    }
+                }
+            }
             for (int st = 0; st < kStages; ++st) {
                 if (filled & (1u << st)) {
                     const uint32_t par = (fill_parity >> st) & 1u;
@@ -379,7 +425,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // loop therefore steps stage addresses and descriptor words by
             // additions, and leaves the line only when a wait has to sleep.
             const uint32_t idesc = (MX ? idesc_mx(2 * BM, PBN) : C::IDESC) | p.idesc_bits;
-            const uint32_t sf_smem0 = smem_u32(sfs);
             const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
             const DescWords da = desc_words(smem_u32(as), p.x_mn != 0);
             const DescWords db = desc_words(smem_u32(bs), p.y_mn != 0);
@@ -400,7 +445,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccStride);
-                const int nb_atoms = MX ? (s.y0 + PBN - 1) / BM - s.y0 / BM + 1 : 0;
                 const uint32_t y_sf_off = static_cast<uint32_t>((s.y0 % BM) / 32);
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (!wait_bounded(fa, phase, abort_flag, p.wait_limit)) {
@@ -410,13 +454,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     }
                     tc_fence_after();
                     if constexpr (MX) {
-                        // scale slot of the stage: refilled only after the stage's
-                        // previous MMAs completed; copies are ordered before the MMAs
+                        // the copier has put this stage's scales into its TMEM slot
+                        if (!wait_bounded(smem_u32(&sf_ready[stage]), phase, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                         const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + C::SF_COLS * stage);
-                        const uint32_t sfd = sf_smem0 + static_cast<uint32_t>(stage * C::SF_BYTES);
-                        tc_cp_atom_pair(sft, atom_desc(sfd));
-                        for (int a = 0; a < nb_atoms; ++a)
-                            tc_cp_atom_pair(sft + 4 + 4 * a, atom_desc(sfd + 512 * (1 + a)));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             tc_mma_pair_mx(d_tmem, alo + k * da.kstep, da.hi, blo + k * db.kstep, db.hi,
@@ -455,6 +500,71 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const long long t0 = clock64();
             while (!mbar_try_wait(smem_u32(drain), 0) &&
                    static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+            }
+        }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ scale copier (leader, block-scaled)
+        // Copies each data stage's scale atoms from the scale ring into the
+        // stage's TMEM slot (tcgen05.cp.cta_group::2: each CTA's atoms into its
+        // own TMEM) and signals sf_ready[stage] when the copies are done, so the
+        // MMA thread issues nothing but MMAs.  The slot is rewritten only after
+        // the stage's new data has landed, which follows the release of its
+        // previous MMAs.
+        if (MX && lane == 0 && leader) {
+            const uint32_t sf_smem0 = smem_u32(sfs);
+            int stage = 0, sst = 0;
+            uint32_t phase = 0, sphase = 0, sc_cur = 0;
+            bool issued = false;
+            PairIter<PBN> w(p, 0);
+            Seg s;
+            bool ok = true;
+            while (ok && w.next(s)) {
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    if (kb == s.kb0 || kb % kScaleKb == 0) {
+                        if (!wait_bounded(smem_u32(&sc_full[sst]), sphase, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        sc_cur = sf_smem0 + static_cast<uint32_t>(sst * C::SC_STAGE_BYTES);
+                    }
+                    tc_fence_after();
+                    const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + C::SF_COLS * stage);
+                    const uint32_t j = static_cast<uint32_t>(kb % kScaleKb);
+                    tc_cp_atom_pair(sft, atom_desc(sc_cur + j * 512));
+                    // B's box: row block a, K block group j at (a * box_kg + j); a B
+                    // row block past the tensor (box of one) holds only rows past N
+#pragma unroll
+                    for (int a = 0; a < kSfAtomsB; ++a)
+                        tc_cp_atom_pair(sft + 4 + 4 * a, atom_desc(sc_cur + (kScaleKb + a * p.sf_box_kg + j) * 512));
+                    tc_commit_pair(smem_u32(&sf_ready[stage]));
+                    issued = true;
+                    if (kb % kScaleKb == kScaleKb - 1 || kb == s.kb1 - 1) {
+                        // the scale stage's last copies: release it in both CTAs
+                        tc_commit_pair_mc(smem_u32(&sc_empty[sst]), 0x3);
+                        if (++sst == kScaleStages) {
+                            sst = 0;
+                            sphase ^= 1;
+                        }
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (issued) {
+                // no copy may still be running when TMEM is released
+                tc_commit_pair(smem_u32(cdrain));
+                const long long t0 = clock64();
+                while (!mbar_try_wait(smem_u32(cdrain), 0) &&
+                       static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                }
             }
         }
     } else {
@@ -515,11 +625,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
-cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaunchAttribute* attr)
+cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaunchAttribute* attr, int threads)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -542,7 +652,7 @@ cudaError_t configure_kind(int* max_pairs)
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr);
+    cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr, KIND == 2 ? kPairThreads + 32 : kPairThreads);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT, KIND>, &cfg);
     if (e != cudaSuccess)
@@ -563,7 +673,8 @@ cudaError_t launch_kind(const CUtensorMap& tma, const CUtensorMap& tmb, const CU
                         const CUtensorMap& tmsb, const TcParams& p, int pairs, cudaStream_t stream)
 {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT, KIND>::SMEM, stream, attr);
+    cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT, KIND>::SMEM, stream, attr,
+                                         KIND == 2 ? kPairThreads + 32 : kPairThreads);
     return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, KIND>, tma, tmb, tmsa, tmsb, p);
 }
 
