@@ -48,19 +48,21 @@ L2_BYTES = 129 * 1024 * 1024
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1182796032 + 252719872, "469fcb703cc546f3"),
-    "square_4096": (91348480 + 35164160, "469fcb703cc546f3"),
-    "ragged_batch16_3001x2047x1000": (171542784 + 342095104, "469fcb703cc546f3"),
-    "skinny_64x16384x8192": (269565696 + 3388928, "41efa3320d8a2cb3"),
+    "square_8192": (1084634368 + 248275456, "31005f3dea441fb4"),
+    "square_4096": (91346688 + 35053568, "31005f3dea441fb4"),
+    "ragged_batch16_3001x2047x1000": (171426816 + 342086400, "31005f3dea441fb4"),
+    "skinny_64x16384x8192": (269561856 + 3363072, "6b8cc54f64f26f7a"),
+    # block-scaled E4M3 inputs (--ab-dtype e4m3 --mx)
+    "square_8192/mx-e4m3": (347736320 + 238664960, "31005f3dea441fb4"),
 }
 
 
 KERNEL_SOURCES = {
-    "square_8192": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh"],
-    "square_4096": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh"],
-    "ragged_batch16_3001x2047x1000": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh"],
-    "skinny_64x16384x8192": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh"],
-    "tile_128x64x64": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh"],
+    "square_8192": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
+    "square_4096": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
+    "ragged_batch16_3001x2047x1000": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
+    "skinny_64x16384x8192": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
+    "tile_128x64x64": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
 }
 
 
@@ -555,8 +557,9 @@ def main():
     # bf16 one times that nominal ratio (4.5 / 2.25 PFLOP/s dense)
     tpeak = peaks["tflops"] * (2.0 if f8 else 1.0)
     tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > tpeak * 1e12
-    tr = TRAFFIC.get(w.name)
-    traffic = tr[0] if default_types and default_layout and tr and tr[1] == kernel_source_sha(w.name) else None
+    tr = TRAFFIC.get(w.name + ("/mx-" + args.ab_dtype if args.mx else ""))
+    traffic = (tr[0] if (default_types or args.mx) and default_layout and tr and tr[1] == kernel_source_sha(w.name)
+               else None)
     if tensor_bound:
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
