@@ -16,7 +16,9 @@ accurate as any fp32 implementation.
 The same product for bfloat16 inputs ("Warp Matrix Instructions", "Other
 Fragment Shapes and Transfers") is ``gemm_nt(..., dtype="bf16")``, with inputs
 given as uint16 bit patterns; for the 8-bit floats E4M3 and E5M2 it is
-``dtype="e4m3"`` / ``"e5m2"`` with uint8 bit patterns.  The block-scaled form
+``dtype="e4m3"`` / ``"e5m2"`` with uint8 bit patterns, and for the 6- and
+4-bit floats E2M3, E3M2 and E2M1 (one per byte, in its low bits)
+``dtype="e2m3"`` / ``"e3m2"`` / ``"e2m1"``.  The block-scaled form
 (one E8M0 power-of-two scale per 32 consecutive K elements of every row of A
 and of B; "Blackwell Tensor Cores" names block scaling and its tcgen05.cp
 scale operands without a formula, and the plain microscaling reading is taken)
@@ -45,7 +47,11 @@ def _u16(x):
     return np.ascontiguousarray(x)
 
 
-F8_TYPES = ("e4m3", "e5m2")
+F8_TYPES = ("e4m3", "e5m2", "e2m3", "e3m2", "e2m1")
+# 8-bit container formats: codes of the oracle's dec8 (those of the MMA's
+# instruction descriptor); E2M3 / E3M2 sit in the low 6 bits of a byte, E2M1 in
+# the low 4
+FMT8 = {"e4m3": 0, "e5m2": 1, "e2m3": 3, "e3m2": 4, "e2m1": 5}
 
 
 def _u8(x):
@@ -130,11 +136,11 @@ class Oracle:
         return out
 
     def f8_to_double(self, bits, dtype: str) -> np.ndarray:
-        """Decode 8-bit float patterns (uint8; dtype "e4m3" or "e5m2") to float64."""
+        """Decode 8-bit container patterns (uint8; dtype one of F8_TYPES) to float64."""
         b = np.ascontiguousarray(bits, dtype=np.uint8)
         out = np.empty(b.shape, dtype=np.float64)
         self.lib.oracle_f8_to_double_array(_ptr(b, ctypes.c_uint8), _ptr(out, ctypes.c_double), b.size,
-                                           1 if dtype == "e5m2" else 0)
+                                           FMT8[dtype])
         return out
 
     def gemm_nt(self, A, B, nthreads: int = 0, dtype: str = "f16"):
@@ -179,7 +185,7 @@ class Oracle:
         absdot = np.empty((batch, M, N), dtype=np.float64)
         self.lib.oracle_gemm_nt_f8(_ptr(a, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(ref, ctypes.c_double),
                                    _ptr(absdot, ctypes.c_double), batch, M, N, K, K, K, N, M * K, N * K, M * N,
-                                   int(nthreads), 1 if dtype == "e5m2" else 0)
+                                   int(nthreads), FMT8[dtype])
         if squeeze:
             ref, absdot = ref[0], absdot[0]
         return ref, absdot
@@ -219,7 +225,7 @@ class Oracle:
         self.lib.oracle_gemm_nt_mx(_ptr(a, ctypes.c_uint8), _ptr(sa, ctypes.c_uint8), _ptr(b, ctypes.c_uint8),
                                    _ptr(sb, ctypes.c_uint8), _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double),
                                    batch, M, N, K, K, K, kb, kb, N, M * K, N * K, M * kb, N * kb, M * N,
-                                   int(nthreads), 1 if dtype == "e5m2" else 0)
+                                   int(nthreads), FMT8[dtype])
         if squeeze:
             ref, absdot = ref[0], absdot[0]
         return ref, absdot
@@ -243,7 +249,7 @@ class Oracle:
             _ptr(a, ctypes.c_uint8), _ptr(sa, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(sb, ctypes.c_uint8),
             _ptr(bb, ctypes.c_int64), _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, kb, kb,
             M * K, N * K, M * kb, N * kb, _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double), int(nthreads),
-            1 if dtype == "e5m2" else 0)
+            FMT8[dtype])
         return ref, absdot
 
     def _fn(self, name, dtype):
@@ -280,7 +286,7 @@ class Oracle:
                 _ptr(a, ctypes.c_uint8), _ptr(b, ctypes.c_uint8), _ptr(bb, ctypes.c_int64),
                 _ptr(ii, ctypes.c_int64), _ptr(jj, ctypes.c_int64), ii.size, K, K, K, M * K, N * K,
                 _ptr(ref, ctypes.c_double), _ptr(absdot, ctypes.c_double), int(nthreads),
-                1 if dtype == "e5m2" else 0)
+                FMT8[dtype])
             return ref, absdot
         self._fn("oracle_gemm_nt_sampled", dtype)(
             _ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), _ptr(bb, ctypes.c_int64),

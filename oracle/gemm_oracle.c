@@ -129,10 +129,62 @@ double oracle_e5m2_to_double(uint8_t h)
     return sign ? -v : v;
 }
 
-void oracle_f8_to_double_array(const uint8_t *src, double *dst, int64_t n, int e5m2)
+/* The 6- and 4-bit floats of the tcgen05 kind::f8f6f4 MMA, one per byte in its
+ * low bits (the higher bits are not part of the value).  The pages name only
+ * the block-scaled low-precision MMA forms; these are the plain microscaling
+ * element types, read from their field widths:
+ *   E2M3: sign bit 5, exponent bits 3-4 (bias 1), fraction bits 0-2;
+ *   E3M2: sign bit 5, exponent bits 2-4 (bias 3), fraction bits 0-1;
+ *   E2M1: sign bit 3, exponent bits 1-2 (bias 1), fraction bit 0;
+ * no infinities or NaN; exponent 0 encodes zero and subnormals,
+ * fraction * 2^(1 - bias - fraction bits). */
+double oracle_e2m3_to_double(uint8_t h)
+{
+    const unsigned sign = (h >> 5) & 1u;
+    const unsigned expo = (h >> 3) & 0x3u;
+    const unsigned frac = h & 0x7u;
+    /* (1 + frac/8) * 2^(expo-1) = (8 + frac) * 2^(expo-4) */
+    const double v = expo == 0 ? (double)frac * pow2i(-3) : (double)(8u + frac) * pow2i((int)expo - 4);
+    return sign ? -v : v;
+}
+
+double oracle_e3m2_to_double(uint8_t h)
+{
+    const unsigned sign = (h >> 5) & 1u;
+    const unsigned expo = (h >> 2) & 0x7u;
+    const unsigned frac = h & 0x3u;
+    /* (1 + frac/4) * 2^(expo-3) = (4 + frac) * 2^(expo-5) */
+    const double v = expo == 0 ? (double)frac * pow2i(-4) : (double)(4u + frac) * pow2i((int)expo - 5);
+    return sign ? -v : v;
+}
+
+double oracle_e2m1_to_double(uint8_t h)
+{
+    const unsigned sign = (h >> 3) & 1u;
+    const unsigned expo = (h >> 1) & 0x3u;
+    const unsigned frac = h & 0x1u;
+    /* (1 + frac/2) * 2^(expo-1) = (2 + frac) * 2^(expo-2) */
+    const double v = expo == 0 ? (double)frac * pow2i(-1) : (double)(2u + frac) * pow2i((int)expo - 2);
+    return sign ? -v : v;
+}
+
+/* One element of an 8-bit container in format `fmt`: 0 E4M3, 1 E5M2, 3 E2M3,
+ * 4 E3M2, 5 E2M1 (the codes of the MMA's instruction descriptor). */
+static double dec8(uint8_t h, int fmt)
+{
+    switch (fmt) {
+    case 1: return oracle_e5m2_to_double(h);
+    case 3: return oracle_e2m3_to_double(h);
+    case 4: return oracle_e3m2_to_double(h);
+    case 5: return oracle_e2m1_to_double(h);
+    default: return oracle_e4m3_to_double(h);
+    }
+}
+
+void oracle_f8_to_double_array(const uint8_t *src, double *dst, int64_t n, int fmt)
 {
     for (int64_t t = 0; t < n; ++t)
-        dst[t] = e5m2 ? oracle_e5m2_to_double(src[t]) : oracle_e4m3_to_double(src[t]);
+        dst[t] = dec8(src[t], fmt);
 }
 
 void oracle_bf16_to_double_array(const uint16_t *src, double *dst, int64_t n)
@@ -265,16 +317,16 @@ void oracle_gemm_nt_sampled_bf16(const uint16_t *A, const uint16_t *B,
                     absdot ? absdot + s : 0);
 }
 
-/* The same product for 8-bit inputs (e5m2 != 0: E5M2, else E4M3): element
- * (i, j) is the sequential-k double sum of exact products (4 x 4 or 3 x 3
+/* The same product for 8-bit containers in format `fmt` (see dec8): element
+ * (i, j) is the sequential-k double sum of exact products (at most 4 x 4
  * significant bits). */
-static void dot_nt_f8(const uint8_t *a_row, const uint8_t *b_row, int64_t K, int e5m2, double *ref,
+static void dot_nt_f8(const uint8_t *a_row, const uint8_t *b_row, int64_t K, int fmt, double *ref,
                       double *absdot)
 {
     double acc = 0.0, aacc = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        const double a = e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k]);
-        const double b = e5m2 ? oracle_e5m2_to_double(b_row[k]) : oracle_e4m3_to_double(b_row[k]);
+        const double a = dec8(a_row[k], fmt);
+        const double b = dec8(b_row[k], fmt);
         const double p = a * b;
         acc += p;
         aacc += fabs(p);
@@ -287,7 +339,7 @@ static void dot_nt_f8(const uint8_t *a_row, const uint8_t *b_row, int64_t K, int
 void oracle_gemm_nt_f8(const uint8_t *A, const uint8_t *B, double *ref, double *absdot,
                        int64_t batch, int64_t M, int64_t N, int64_t K,
                        int64_t lda, int64_t ldb, int64_t ldr,
-                       int64_t sA, int64_t sB, int64_t sR, int nthreads, int e5m2)
+                       int64_t sA, int64_t sB, int64_t sR, int nthreads, int fmt)
 {
 #ifdef _OPENMP
     if (nthreads <= 0)
@@ -299,7 +351,7 @@ void oracle_gemm_nt_f8(const uint8_t *A, const uint8_t *B, double *ref, double *
         const uint8_t *a_row = A + b * sA + i * lda;
         for (int64_t j = 0; j < N; ++j) {
             double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
-            dot_nt_f8(a_row, B + b * sB + j * ldb, K, e5m2, ref + b * sR + i * ldr + j, ab);
+            dot_nt_f8(a_row, B + b * sB + j * ldb, K, fmt, ref + b * sR + i * ldr + j, ab);
         }
     }
 }
@@ -307,7 +359,7 @@ void oracle_gemm_nt_f8(const uint8_t *A, const uint8_t *B, double *ref, double *
 void oracle_gemm_nt_sampled_f8(const uint8_t *A, const uint8_t *B,
                                const int64_t *bidx, const int64_t *iidx, const int64_t *jidx,
                                int64_t n, int64_t K, int64_t lda, int64_t ldb,
-                               int64_t sA, int64_t sB, double *ref, double *absdot, int nthreads, int e5m2)
+                               int64_t sA, int64_t sB, double *ref, double *absdot, int nthreads, int fmt)
 {
 #ifdef _OPENMP
     if (nthreads <= 0)
@@ -315,7 +367,7 @@ void oracle_gemm_nt_sampled_f8(const uint8_t *A, const uint8_t *B,
 #pragma omp parallel for schedule(static) num_threads(nthreads)
 #endif
     for (int64_t s = 0; s < n; ++s)
-        dot_nt_f8(A + bidx[s] * sA + iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, e5m2, ref + s,
+        dot_nt_f8(A + bidx[s] * sA + iidx[s] * lda, B + bidx[s] * sB + jidx[s] * ldb, K, fmt, ref + s,
                   absdot ? absdot + s : 0);
 }
 
@@ -344,13 +396,13 @@ void oracle_e8m0_to_double_array(const uint8_t *src, double *dst, int64_t n)
 }
 
 static void dot_nt_mx(const uint8_t *a_row, const uint8_t *sa_row, const uint8_t *b_row, const uint8_t *sb_row,
-                      int64_t K, int e5m2, double *ref, double *absdot)
+                      int64_t K, int fmt, double *ref, double *absdot)
 {
     double acc = 0.0, aacc = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        const double a = (e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k])) *
+        const double a = dec8(a_row[k], fmt) *
                          oracle_e8m0_to_double(sa_row[k / 32]);
-        const double b = (e5m2 ? oracle_e5m2_to_double(b_row[k]) : oracle_e4m3_to_double(b_row[k])) *
+        const double b = dec8(b_row[k], fmt) *
                          oracle_e8m0_to_double(sb_row[k / 32]);
         const double p = a * b;
         acc += p;
@@ -366,7 +418,7 @@ static void dot_nt_mx(const uint8_t *a_row, const uint8_t *sa_row, const uint8_t
 void oracle_gemm_nt_mx(const uint8_t *A, const uint8_t *SA, const uint8_t *B, const uint8_t *SB, double *ref,
                        double *absdot, int64_t batch, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                        int64_t ldsa, int64_t ldsb, int64_t ldr, int64_t sA, int64_t sB, int64_t sSA, int64_t sSB,
-                       int64_t sR, int nthreads, int e5m2)
+                       int64_t sR, int nthreads, int fmt)
 {
 #ifdef _OPENMP
     if (nthreads <= 0)
@@ -378,7 +430,7 @@ void oracle_gemm_nt_mx(const uint8_t *A, const uint8_t *SA, const uint8_t *B, co
         const uint8_t *a_row = A + b * sA + i * lda, *sa_row = SA + b * sSA + i * ldsa;
         for (int64_t j = 0; j < N; ++j) {
             double *ab = absdot ? absdot + b * sR + i * ldr + j : 0;
-            dot_nt_mx(a_row, sa_row, B + b * sB + j * ldb, SB + b * sSB + j * ldsb, K, e5m2,
+            dot_nt_mx(a_row, sa_row, B + b * sB + j * ldb, SB + b * sSB + j * ldsb, K, fmt,
                       ref + b * sR + i * ldr + j, ab);
         }
     }
@@ -388,7 +440,7 @@ void oracle_gemm_nt_sampled_mx(const uint8_t *A, const uint8_t *SA, const uint8_
                                const int64_t *bidx, const int64_t *iidx, const int64_t *jidx, int64_t n,
                                int64_t K, int64_t lda, int64_t ldb, int64_t ldsa, int64_t ldsb, int64_t sA,
                                int64_t sB, int64_t sSA, int64_t sSB, double *ref, double *absdot, int nthreads,
-                               int e5m2)
+                               int fmt)
 {
 #ifdef _OPENMP
     if (nthreads <= 0)
@@ -397,7 +449,7 @@ void oracle_gemm_nt_sampled_mx(const uint8_t *A, const uint8_t *SA, const uint8_
 #endif
     for (int64_t s = 0; s < n; ++s)
         dot_nt_mx(A + bidx[s] * sA + iidx[s] * lda, SA + bidx[s] * sSA + iidx[s] * ldsa,
-                  B + bidx[s] * sB + jidx[s] * ldb, SB + bidx[s] * sSB + jidx[s] * ldsb, K, e5m2, ref + s,
+                  B + bidx[s] * sB + jidx[s] * ldb, SB + bidx[s] * sSB + jidx[s] * ldsb, K, fmt, ref + s,
                   absdot ? absdot + s : 0);
 }
 

@@ -443,6 +443,103 @@ def pin_mx_unit_scales(orc, seed=43):
         assert np.array_equal(r2, want), "%s doubled row" % dtype
 
 
+# 6- and 4-bit floats: (exponent bits, fraction bits, bias, total bits)
+MINIFLOATS = {"e2m3": (2, 3, 1, 6), "e3m2": (3, 2, 3, 6), "e2m1": (2, 1, 1, 4)}
+
+
+def minifloat_code(x, dtype):
+    """Code of the value x in a 6- or 4-bit format, built from the format's
+    field widths (exponent 0: subnormal fraction * 2^(1-bias-m)); x must be
+    exactly representable."""
+    e, m, b, n = MINIFLOATS[dtype]
+    x = Fraction(x)
+    sign = 1 if x < 0 else 0
+    x = abs(x)
+    for expo in range(2 ** e):
+        for frac in range(2 ** m):
+            v = (Fraction(frac, 2 ** m) * Fraction(2) ** (1 - b) if expo == 0
+                 else (1 + Fraction(frac, 2 ** m)) * Fraction(2) ** (expo - b))
+            if v == x:
+                return (sign << (n - 1)) | (expo << m) | frac
+    raise ValueError("%s is not an %s value" % (x, dtype))
+
+
+def pin_f6f4_decoders(orc):
+    """E2M3, E3M2 and E2M1, one per byte in its low bits: normal codes equal
+    the binary16 of the same sign, fraction and unbiased exponent (numpy);
+    the exponent-0 codes are equally spaced by 2^(1-bias-m) from 0; values
+    increase with the code; the sign bit negates; the bits above the format
+    are ignored; every value is an E4M3 value (torch's cast)."""
+    import torch
+    for dtype, (e, m, b, n) in MINIFLOATS.items():
+        codes = np.arange(2 ** (n - 1), dtype=np.uint16).astype(np.uint8)
+        v = orc.f8_to_double(codes, dtype)
+        expo, frac = codes.astype(np.uint16) >> m, codes.astype(np.uint16) & (2 ** m - 1)
+        normal = expo > 0
+        h = (((expo.astype(np.int64) - b + 15) << 10) | (frac.astype(np.int64) << (10 - m))).astype(np.uint16)
+        assert np.array_equal(v[normal], h[normal].view(np.float16).astype(np.float64)), "%s normal codes" % dtype
+        sub = v[~normal]
+        assert np.array_equal(sub, np.arange(2 ** m) * 2.0 ** (1 - b - m)), "%s subnormal codes" % dtype
+        assert np.all(np.diff(v) > 0), "%s monotonic" % dtype
+        neg = orc.f8_to_double(codes | np.uint8(1 << (n - 1)), dtype)
+        assert np.array_equal(neg, -v) and np.all(np.signbit(neg)), "%s sign bit" % dtype
+        hi = orc.f8_to_double(codes | np.uint8((0xff << n) & 0xff), dtype)
+        assert np.array_equal(hi, v), "%s bits above the format" % dtype
+        t = torch.from_numpy(v)
+        assert torch.equal(t.to(torch.float8_e4m3fn).to(torch.float64), t), "%s values are E4M3 values" % dtype
+
+
+def pin_f6f4_exact_tiny(orc, seed=51):
+    """Products of random 6- and 4-bit codes (high bits set at random too)
+    against exact rational sums of the decoded values, plain and
+    block-scaled; sampled = full."""
+    rng = np.random.default_rng(seed)
+    for dtype in MINIFLOATS:
+        for (batch, M, N, K) in ((1, 3, 4, 9), (2, 4, 3, 70)):
+            A = rng.integers(0, 256, size=(batch, M, K)).astype(np.uint8)
+            B = rng.integers(0, 256, size=(batch, N, K)).astype(np.uint8)
+            a, b = orc.f8_to_double(A, dtype), orc.f8_to_double(B, dtype)
+            SA = rng.integers(120, 135, size=(batch, M, (K + 31) // 32)).astype(np.uint8)
+            SB = rng.integers(120, 135, size=(batch, N, (K + 31) // 32)).astype(np.uint8)
+            for scaled in (False, True):
+                ref, absdot = (orc.gemm_nt_mx(A, SA, B, SB, dtype=dtype) if scaled else orc.gemm_nt(A, B, dtype=dtype))
+                g = gamma(max(K - 1, 0))
+                for bi in range(batch):
+                    for i in range(M):
+                        for j in range(N):
+                            terms = []
+                            for k in range(K):
+                                t = Fraction(float(a[bi, i, k])) * Fraction(float(b[bi, j, k]))
+                                if scaled:
+                                    t *= Fraction(2) ** (int(SA[bi, i, k // 32]) + int(SB[bi, j, k // 32]) - 254)
+                                terms.append(t)
+                            ex = sum(terms, Fraction(0))
+                            exa = sum((abs(t) for t in terms), Fraction(0))
+                            assert abs(Fraction(float(ref[bi, i, j])) - ex) <= Fraction(g) * exa * Fraction(1 + 2 * U) \
+                                + Fraction(2 * U) * abs(ex) + Fraction(1, 2 ** 1074), "%s product" % dtype
+                            assert abs(Fraction(float(absdot[bi, i, j])) - exa) <= Fraction(g + 2 * U) * exa \
+                                + Fraction(1, 2 ** 1074), "%s absdot" % dtype
+            bb = rng.integers(0, batch, size=12)
+            ii = rng.integers(0, M, size=12)
+            jj = rng.integers(0, N, size=12)
+            sref, sabs = orc.gemm_nt_sampled(A, B, bb, ii, jj, dtype=dtype)
+            ref, absdot = orc.gemm_nt(A, B, dtype=dtype)
+            assert np.array_equal(sref, ref[bb, ii, jj]) and np.array_equal(sabs, absdot[bb, ii, jj])
+
+
+def pin_f6f4_integer_exact(orc, seed=52):
+    """Integers in [-4, 4], encoded from the field widths, give numpy's
+    einsum exactly."""
+    rng = np.random.default_rng(seed)
+    for dtype in MINIFLOATS:
+        A = rng.integers(-4, 5, size=(2, 7, 75))
+        B = rng.integers(-4, 5, size=(2, 5, 75))
+        enc = np.vectorize(lambda x: minifloat_code(int(x), dtype))
+        ref, absdot = orc.gemm_nt(enc(A).astype(np.uint8), enc(B).astype(np.uint8), dtype=dtype)
+        assert np.array_equal(ref, np.einsum("bik,bjk->bij", A, B).astype(np.float64)), "%s integers" % dtype
+        assert np.array_equal(absdot, np.einsum("bik,bjk->bij", np.abs(A), np.abs(B)).astype(np.float64))
+
+
 def torch_cast(x, dtype):
     """float64 values rounded to the nearest value of the 8-bit format."""
     import torch
@@ -454,4 +551,5 @@ ALL_PINS = [pin_decoder_exhaustive, pin_bruteforce_tiny, pin_k1_exact, pin_worke
             pin_closed_forms, pin_integer_exact, pin_numpy_crosscheck, pin_batched_and_sampled,
             pin_bf16_decoder_exhaustive, pin_bf16_exact_tiny, pin_bf16_integer_exact,
             pin_f8_decoders_exhaustive, pin_f8_exact_tiny, pin_f8_integer_exact,
-            pin_e8m0_decoder_exhaustive, pin_mx_exact_tiny, pin_mx_integer_exact, pin_mx_unit_scales]
+            pin_e8m0_decoder_exhaustive, pin_mx_exact_tiny, pin_mx_integer_exact, pin_mx_unit_scales,
+            pin_f6f4_decoders, pin_f6f4_exact_tiny, pin_f6f4_integer_exact]

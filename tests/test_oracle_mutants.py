@@ -34,8 +34,12 @@ MUTANTS = [
     ("e4m3_subnormal_scale", "v = (double)frac * pow2i(-9);", "v = (double)frac * pow2i(-10);"),
     ("e4m3_nan_as_value", "if (expo == 15 && frac == 7) {", "if (expo == 15 && frac == 8) {"),
     ("e5m2_exponent_bias", "(int)expo - 17", "(int)expo - 16"),
-    ("f8_formats_swapped", "const double a = e5m2 ? oracle_e5m2_to_double(a_row[k]) : oracle_e4m3_to_double(a_row[k]);",
-     "const double a = e5m2 ? oracle_e4m3_to_double(a_row[k]) : oracle_e5m2_to_double(a_row[k]);"),
+    ("f8_formats_swapped", "    case 1: return oracle_e5m2_to_double(h);", "    case 1: return oracle_e4m3_to_double(h);"),
+    ("e2m3_exponent_bias", "(double)(8u + frac) * pow2i((int)expo - 4)", "(double)(8u + frac) * pow2i((int)expo - 3)"),
+    ("e3m2_fraction_bits", "    const unsigned frac = h & 0x3u;\n    /* (1 + frac/4) * 2^(expo-3)", "    const unsigned frac = h & 0x1u;\n    /* (1 + frac/4) * 2^(expo-3)"),
+    ("e2m1_sign_bit", "    const unsigned sign = (h >> 3) & 1u;\n    const unsigned expo = (h >> 1) & 0x3u;", "    const unsigned sign = (h >> 4) & 1u;\n    const unsigned expo = (h >> 1) & 0x3u;"),
+    ("e2m1_subnormal", "(double)frac * pow2i(-1) : (double)(2u + frac)", "(double)frac * pow2i(-2) : (double)(2u + frac)"),
+    ("f6_codes_swapped", "    case 3: return oracle_e2m3_to_double(h);", "    case 3: return oracle_e3m2_to_double(h);"),
     ("f8_abs_missing", "        aacc += fabs(p);\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8",
      "        aacc += p;\n    }\n    *ref = acc;\n    if (absdot)\n        *absdot = aacc;\n}\n\nvoid oracle_gemm_nt_f8"),
     ("mx_block_of_16", "sa_row[k / 32]", "sa_row[k / 16]"),
