@@ -32,6 +32,9 @@ class DType(enum.IntEnum):
     F32 = 2
     E4M3 = 3  # 8-bit floats (A and B only)
     E5M2 = 4
+    E2M3 = 5  # 6- and 4-bit floats, one per byte in its low bits (A and B only)
+    E3M2 = 6
+    E2M1 = 7
 
 
 class Major(enum.IntEnum):

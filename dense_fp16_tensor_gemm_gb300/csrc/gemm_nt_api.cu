@@ -178,7 +178,16 @@ struct Problem {
     int64_t b_cols() const { return b_mn() ? N : K; }
 
     int64_t out_esize() const { return out_type == GEMM_DTYPE_F32 ? 4 : 2; }
-    bool is_f8() const { return ab_type == GEMM_DTYPE_E4M3 || ab_type == GEMM_DTYPE_E5M2; }
+    // the 8-bit MMA kinds: 8-bit floats, and the 6- and 4-bit ones (stored packed)
+    bool is_f8() const { return ab_type >= GEMM_DTYPE_E4M3 && ab_type <= GEMM_DTYPE_E2M1; }
+    // 6- and 4-bit floats, packed along K (two per byte, or four per three bytes)
+    bool is_packed() const { return ab_type >= GEMM_DTYPE_E2M3 && ab_type <= GEMM_DTYPE_E2M1; }
+    int ab_bits() const
+    {
+        return ab_type == GEMM_DTYPE_E2M1 ? 4 : (is_packed() ? 6 : (is_f8() ? 8 : 16));
+    }
+    // bytes of n elements of A or B (n a multiple of the packing group)
+    int64_t ab_bytes(int64_t n) const { return n * ab_bits() / 8; }
     // kernel kind of tc05_launch: 0 16-bit, 1 8-bit, 2 8-bit block-scaled
     int kind() const { return mx() ? 2 : (is_f8() ? 1 : 0); }
     int64_t ab_esize() const { return is_f8() ? 1 : 2; }
@@ -189,7 +198,17 @@ struct Problem {
     // bf16 for kind::f16 and E5M2 for kind::f8f6f4; 0 is fp16 or E4M3.
     uint32_t ab_fmt() const
     {
-        return (ab_type == GEMM_DTYPE_BF16 || ab_type == GEMM_DTYPE_E5M2) ? ((1u << 7) | (1u << 10)) : 0u;
+        // kind::f8f6f4 codes: E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5
+        uint32_t f = 0;
+        switch (ab_type) {
+        case GEMM_DTYPE_BF16: f = 1; break;
+        case GEMM_DTYPE_E5M2: f = 1; break;
+        case GEMM_DTYPE_E2M3: f = 3; break;
+        case GEMM_DTYPE_E3M2: f = 4; break;
+        case GEMM_DTYPE_E2M1: f = 5; break;
+        default: f = 0;
+        }
+        return (f << 7) | (f << 10);
     }
 };
 
@@ -209,6 +228,15 @@ void span(const void* base, int64_t esize, int64_t batch, int64_t stride, int64_
     const int64_t last = (batch - 1) * stride + (rows - 1) * ld + cols;
     lo = reinterpret_cast<uintptr_t>(base);
     hi = lo + static_cast<uintptr_t>(last * esize);
+}
+
+// The same for elements of `bits` bits (the end rounded up to a byte).
+void span_bits(const void* base, int bits, int64_t batch, int64_t stride, int64_t rows, int64_t ld, int64_t cols,
+               uintptr_t& lo, uintptr_t& hi)
+{
+    const int64_t last = (batch - 1) * stride + (rows - 1) * ld + cols;
+    lo = reinterpret_cast<uintptr_t>(base);
+    hi = lo + static_cast<uintptr_t>((last * bits + 7) / 8);
 }
 
 gemm_status_t validate(const Problem& q)
@@ -237,8 +265,7 @@ gemm_status_t validate(const Problem& q)
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sA, q.lda * q.a_rows())) * 2.0 > lim ||
         static_cast<double>(q.batch) * static_cast<double>(std::max(q.sB, q.ldb * q.b_rows())) * 2.0 > lim)
         return GEMM_ERR_INVALID_VALUE;
-    if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16 && q.ab_type != GEMM_DTYPE_E4M3 &&
-        q.ab_type != GEMM_DTYPE_E5M2)
+    if (q.ab_type != GEMM_DTYPE_F16 && q.ab_type != GEMM_DTYPE_BF16 && !q.is_f8())
         return GEMM_ERR_INVALID_VALUE;
     if (q.out_type != GEMM_DTYPE_F32 && q.out_type != GEMM_DTYPE_F16 && q.out_type != GEMM_DTYPE_BF16)
         return GEMM_ERR_INVALID_VALUE;
@@ -248,6 +275,12 @@ gemm_status_t validate(const Problem& q)
         return GEMM_ERR_INVALID_VALUE;
     if (q.batch > 1 && q.sO < (q.M - 1) * q.ldo + q.N)
         return GEMM_ERR_OVERLAP;
+    if (q.is_packed() && q.K > 0) {
+        // rows and batches start on whole bytes (fp4: even pitches; fp6: multiples of 4), K-major
+        const int64_t g = q.ab_bits() == 4 ? 2 : 4;
+        if (q.a_mn() || q.b_mn() || q.lda % g || q.ldb % g || q.sA % g || q.sB % g)
+            return GEMM_ERR_INVALID_VALUE;
+    }
     if (q.mx() && q.K > 0) {
         if (!q.SA || !q.SB || !q.is_f8() || q.a_mn() || q.b_mn())
             return GEMM_ERR_INVALID_VALUE;
@@ -257,8 +290,8 @@ gemm_status_t validate(const Problem& q)
     if (q.K > 0) {
         uintptr_t olo, ohi, alo, ahi, blo, bhi;
         span(q.Out, q.out_esize(), q.batch, q.sO, q.M, q.ldo, q.N, olo, ohi);
-        span(q.A, q.ab_esize(), q.batch, q.sA, q.a_rows(), q.lda, q.a_cols(), alo, ahi);
-        span(q.B, q.ab_esize(), q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
+        span_bits(q.A, q.ab_bits(), q.batch, q.sA, q.a_rows(), q.lda, q.a_cols(), alo, ahi);
+        span_bits(q.B, q.ab_bits(), q.batch, q.sB, q.b_rows(), q.ldb, q.b_cols(), blo, bhi);
         if ((olo < ahi && alo < ohi) || (olo < bhi && blo < ohi))
             return GEMM_ERR_OVERLAP;
         if (q.mx()) {
@@ -276,6 +309,20 @@ gemm_status_t validate(const Problem& q)
 // row / batch strides that are multiples of 16 bytes and below 2^40 bytes.
 bool tma_ok(const Problem& q)
 {
+    if (q.is_packed()) {
+        // the unpacking tensor-map types: 32-byte aligned bases, pitches and batch
+        // strides in multiples of 32 bytes, K a multiple of 128, below 2^40 bytes
+        if (!aligned(q.A, 32) || !aligned(q.B, 32) || q.K % 128)
+            return false;
+        if (q.ab_bytes(q.lda) % 32 || q.ab_bytes(q.ldb) % 32)
+            return false;
+        if (q.batch > 1 && (q.ab_bytes(q.sA) % 32 || q.ab_bytes(q.sB) % 32))
+            return false;
+        if (q.batch > 1 && ((q.sA != 0 && q.sA < q.a_rows() * q.lda) || (q.sB != 0 && q.sB < q.b_rows() * q.ldb)))
+            return false;
+        const int64_t lim = int64_t(1) << 40;
+        return q.ab_bytes(q.lda) < lim && q.ab_bytes(q.ldb) < lim && q.ab_bytes(q.sA) < lim && q.ab_bytes(q.sB) < lim;
+    }
     if (!aligned(q.A, 16) || !aligned(q.B, 16))
         return false;
     const int64_t v = 16 / q.ab_esize();  // elements in 16 bytes
@@ -297,6 +344,9 @@ bool tma_ok(const Problem& q)
 
 gemm_path_t select_path(const Problem& q)
 {
+    if (q.is_packed() && !q.mx())  // no warp kernel for packed 6- and 4-bit inputs
+        return q.M <= 64 && q.N >= 1024 ? GEMM_PATH_SKINNY
+                                        : (q.M > 128 && q.N > 128 ? GEMM_PATH_TC05_PAIR : GEMM_PATH_TC05);
     if (q.mx()) {  // block-scaled: no warp kernel; swapped for small M, pairs for large tiles
         if (q.M <= 64 && q.N >= 1024)
             return GEMM_PATH_SKINNY;
@@ -345,7 +395,8 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
                 int64_t stride, int box_rows, int* bmul, int dtype, bool mn)
 {
     const bool f8 = dtype == GEMM_DTYPE_E4M3 || dtype == GEMM_DTYPE_E5M2;
-    const int64_t es = f8 ? 1 : 2;
+    const bool packed = dtype >= GEMM_DTYPE_E2M3 && dtype <= GEMM_DTYPE_E2M1;
+    const int bits = dtype == GEMM_DTYPE_E2M1 ? 4 : (packed ? 6 : (f8 ? 8 : 16));
     auto enc = encode_fn();
     if (!enc)
         return false;
@@ -353,14 +404,18 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int
     const int64_t inner = mn ? rows : K, outer = mn ? K : rows;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
                           static_cast<cuuint64_t>(batched ? batch : 1)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es),
-                             static_cast<cuuint64_t>((batched ? stride : outer * ld) * es)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(mn ? 64 : box_rows), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * bits / 8),
+                             static_cast<cuuint64_t>((batched ? stride : outer * ld) * bits / 8)};
+    // one 128-byte shared row per box row: 64 elements of 16 bits, 128 of 8 bits,
+    // or 128 packed 6- or 4-bit elements, which the unpacking types spread to 16
+    // elements per 16-byte chunk (the layout the 8-bit MMA kind reads them in)
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(bits == 16 ? 64 : 128), static_cast<cuuint32_t>(mn ? 64 : box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     *bmul = batched ? 1 : 0;
-    const CUtensorMapDataType ty = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                      : (dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const CUtensorMapDataType ty =
+        packed ? (bits == 4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B)
+               : (f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                     : (dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16));
     CUresult r = enc(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -454,6 +509,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         bn = yrows <= 64 ? 64 : (yrows <= 128 ? 128 : 256);
     }
     TcParams p{};
+    p.ab_packed_bits = q.is_packed() ? q.ab_bits() : 0;
     // Row split (swapped operands, one batch, one column tile, 64..128 rows of
     // X per CTA): every CTA takes an even share of the rows over all of K, with
     // an X box just tall enough for that share (a multiple of 8 rows).
@@ -580,6 +636,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     if (d.max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
     TcParams p{};
+    p.ab_packed_bits = q.is_packed() ? q.ab_bits() : 0;
     const int pbn = pair_plan_width(q, d);
     CUtensorMap tma, tmb;
     if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type,
@@ -729,7 +786,7 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         return zero_out(q, stream);
     if (path == GEMM_PATH_AUTO)
         path = select_path(q);
-    if (q.mx() && path == GEMM_PATH_MMASYNC)
+    if ((q.mx() || q.is_packed()) && path == GEMM_PATH_MMASYNC)
         return GEMM_ERR_NOT_SUPPORTED;
     switch (path) {
     case GEMM_PATH_MMASYNC:
@@ -922,6 +979,7 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     if (!tma_ok(q) || d->max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
     TcParams p{};
+    p.ab_packed_bits = q.is_packed() ? q.ab_bits() : 0;
     const int pbn = pair_plan_width(q, *d);
     CUtensorMap tma, tmb;
     if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type) ||

@@ -45,6 +45,10 @@ struct TcParams {
     int y_bmul;
     int vec4;             // Out base and ldo allow 4-element vector stores
     int x_box_bytes;      // bytes of one X box (its height x 128 B; at most 16 KB)
+    // 0, or the width (6 or 4 bits) of packed A/B elements: their loads spread 16
+    // packed elements over each 16-byte chunk of shared memory but credit the
+    // stage barrier with the packed global bytes, width / 8 of the shared ones
+    int ab_packed_bits;
     // Stream-K on the pair kernel: tiles [sk_first, num_tiles) are cut into
     // even k-block ranges, one per pair.  Each partial piece leaves its slice in
     // ws; per-(tile, CTA, epilogue warp) counters in ws_flags pick the warp that

@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t filled = 0;       // bit s: stage s has a load this thread issued
             uint32_t fill_parity = 0;  // bit s: parity of that fill
+            // bytes the two data loads credit: packed 6- and 4-bit elements count
+            // their global bytes, width / 8 of the shared ones
+            const uint32_t data_tx = (p.x_box_bytes + C::Y_BYTES) * (p.ab_packed_bits ? p.ab_packed_bits : 8) / 8;
             bool first = true, ok = true;
             WorkIter<BN> w(p);
             Seg s;
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
-                        mbar_arrive_expect_tx(fb, p.x_box_bytes + C::Y_BYTES + C::SF_BYTES);
+                        mbar_arrive_expect_tx(fb, data_tx + C::SF_BYTES);
                         load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * KE, s.x0,
                                          s.b * p.x_bmul);
                         load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * KE, s.y0,

@@ -334,6 +334,8 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
+            // both CTAs' data loads of a stage, as credited (packed elements: global bytes)
+            const uint32_t data_tx = 2 * STAGE_BYTES * (p.ab_packed_bits ? p.ab_packed_bits : 8) / 8;
             int sst = 0;  // scale stage ring
             uint32_t sphase = 0, sc_filled = 0, sc_parity = 0;
             bool first = true, ok = true;
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
                         const uint32_t fb_local = smem_u32(&full[stage]);
                         const uint32_t fb_leader = mapa_shared(fb_local, 0);
                         if (leader) {
-                            mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+                            mbar_arrive_expect_tx(fb_local, data_tx);
                             filled |= 1u << stage;
                             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         }

@@ -66,8 +66,15 @@ typedef enum gemm_dtype {
     GEMM_DTYPE_F32 = 2,  /* IEEE binary32 (Out only) */
     GEMM_DTYPE_E4M3 = 3, /* 8-bit float, 4 exponent bits (bias 7), 3 fraction bits, no infinities,
                             largest value 448 (A and B only) */
-    GEMM_DTYPE_E5M2 = 4  /* 8-bit float, 5 exponent bits (bias 15), 2 fraction bits: the upper byte
+    GEMM_DTYPE_E5M2 = 4, /* 8-bit float, 5 exponent bits (bias 15), 2 fraction bits: the upper byte
                             of an IEEE binary16 (A and B only) */
+    /* 6- and 4-bit floats (A and B only), no infinities or NaN, packed along K with
+       little-endian bit order: element k of a row occupies bits [b*k, b*k + b) of the
+       row's bit string (b = 6 or 4; byte i holds bits [8i, 8i + 8)), so fp4 holds
+       element 2t in the low nibble of byte t and element 2t+1 in its high nibble: */
+    GEMM_DTYPE_E2M3 = 5, /* sign bit 5, 2 exponent bits (bias 1), 3 fraction bits; largest 7.5 */
+    GEMM_DTYPE_E3M2 = 6, /* sign bit 5, 3 exponent bits (bias 3), 2 fraction bits; largest 28 */
+    GEMM_DTYPE_E2M1 = 7  /* sign bit 3, 2 exponent bits (bias 1), 1 fraction bit; largest 6 */
 } gemm_dtype_t;
 
 /* Kernel choice.  GEMM_PATH_AUTO lets the library pick (see gemm_nt_select_path). */
@@ -130,7 +137,15 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *
  * the partial sums are kept in fp32 only.
  *
  * A and B may also both be 8-bit floats (E4M3 or E5M2; lda, ldb and the batch
- * strides then count bytes).  "Blackwell Tensor Cores" names the block-scaled
+ * strides then count bytes), or both one of the 6- and 4-bit floats E2M3,
+ * E3M2, E2M1, packed along K (lda, ldb and the batch strides count elements
+ * and must start every row on a byte: multiples of 2 for E2M1, of 4 for the
+ * 6-bit types; K-major only, else GEMM_ERR_INVALID_VALUE).  The packed types run
+ * on the tcgen05 kernels only (kind::f8f6f4, whose tensor maps spread every 16
+ * packed elements to a 16-byte chunk of shared memory), which need K a
+ * multiple of 128, A and B 32-byte aligned, and pitches and batch strides of
+ * whole multiples of 32 bytes; other layouts, and the warp kernel path, give
+ * GEMM_ERR_NOT_SUPPORTED.  "Blackwell Tensor Cores" names the block-scaled
  * low-precision forms of the tcgen05 MMA beside kind::f16; these run on its
  * kind::f8f6f4 form without scale factors (products exact, fp32 accumulation),
  * at twice the fp16 rate.  The tensor-core kernels want 16-byte aligned bases
@@ -191,7 +206,8 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
  * Block-scaled 8-bit product ("Blackwell Tensor Cores", on the other TMEM
  * operations: tcgen05.cp brings the scale factors of a block-scaled MMA into
  * Tensor Memory; the MMA reference it points to lists block scaling).  A and B
- * are E4M3 or E5M2 (both the same), K-major, as in gemm_nt_batched_ex; every
+ * are E4M3, E5M2, E2M3, E3M2 or E2M1 (both the same), K-major, as in
+ * gemm_nt_batched_ex; every
  * run of 32 consecutive K elements of a row of A (of B) shares one scale, an
  * E8M0 byte e standing for 2^(e-127) (255 is NaN), and
  *   Out[b,i,j] = sum_k (A[b,i,k] * 2^(sa[b,i,k/32]-127)) * (B[b,j,k] * 2^(sb[b,j,k/32]-127))

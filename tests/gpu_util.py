@@ -85,16 +85,18 @@ TORCH_DTYPES = ("f16", "bf16", "f32")
 def torch_dtype(name):
     import torch
     return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
-            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[name]
+            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2,
+            "e2m3": torch.uint8, "e3m2": torch.uint8, "e2m1": torch.uint8}[name]
 
 
 def dtype_code(name):
     return {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32,
-            "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2}[name]
+            "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2, "e2m3": gnt.DType.E2M3, "e3m2": gnt.DType.E3M2,
+            "e2m1": gnt.DType.E2M1}[name]
 
 
 def esize(name):
-    return {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}[name]
+    return {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e2m3": 1, "e3m2": 1, "e2m1": 1}[name]
 
 
 def to_device(bits, ab, ld=None, offset=0):
@@ -111,6 +113,25 @@ def to_device(bits, ab, ld=None, offset=0):
     t[offset:].view(batch, rows, ld)[:, :, :cols] = torch.from_numpy(x.copy()).view(torch_dtype(ab))
     t = t.cuda()
     return t, t.data_ptr() + es * offset
+
+
+PACKED = {"e2m3": 6, "e3m2": 6, "e2m1": 4}  # bits per element of the packed types
+
+
+def to_device_packed(codes, ab, ld):
+    """(batch, rows, K) codes of a packed 6- or 4-bit type -> device bytes in
+    the packed storage with a row pitch of `ld` elements (padding zero).
+    Returns (tensor, base pointer)."""
+    import torch
+    import workloads
+    bits = PACKED[ab]
+    batch, rows, K = codes.shape
+    packed = workloads.pack_subbyte(codes, ab)
+    pitch = ld * bits // 8
+    t = torch.zeros(batch * rows * pitch, dtype=torch.uint8)
+    t.view(batch, rows, pitch)[:, :, :packed.shape[2]] = torch.from_numpy(packed)
+    t = t.cuda()
+    return t, t.data_ptr()
 
 
 def run_general(A, B, ab, out, path, a_mn=False, b_mn=False, lda=None, ldb=None, ldo=None, out_offset=0,
@@ -131,8 +152,12 @@ def run_general(A, B, ab, out, path, a_mn=False, b_mn=False, lda=None, ldb=None,
     lda = lda or ((As.shape[2] + 7) // 8 * 8 if a_mn else As.shape[2])
     ldb = ldb or ((Bs.shape[2] + 7) // 8 * 8 if b_mn else Bs.shape[2])
     ldo = ldo or N
-    a, pa = to_device(As, ab, lda, a_offset)
-    b, pb = to_device(Bs, ab, ldb)
+    if ab in PACKED:
+        a, pa = to_device_packed(As, ab, lda)
+        b, pb = to_device_packed(Bs, ab, ldb)
+    else:
+        a, pa = to_device(As, ab, lda, a_offset)
+        b, pb = to_device(Bs, ab, ldb)
     o = torch.full((out_offset + batch * M * ldo,), float("nan"), dtype=torch_dtype(out), device="cuda")
     esize = o.element_size()
     stream = torch.cuda.current_stream().cuda_stream

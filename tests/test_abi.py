@@ -122,7 +122,7 @@ def test_dtype_validation(lib):
     D = gnt.DType
     base = (8, 8, 8, 8, 8, 8, 1, 64, 64, 64, 0, None)
     assert f(FAKE_A, FAKE_B, FAKE_O, D.F32, D.F32, *base) == gnt.Status.INVALID_VALUE  # fp32 inputs
-    assert f(FAKE_A, FAKE_B, FAKE_O, 7, D.F32, *base) == gnt.Status.INVALID_VALUE
+    assert f(FAKE_A, FAKE_B, FAKE_O, 8, D.F32, *base) == gnt.Status.INVALID_VALUE
     assert f(FAKE_A, FAKE_B, FAKE_O, D.BF16, 9, *base) == gnt.Status.INVALID_VALUE
     assert f(FAKE_A, FAKE_B, FAKE_O + 1, D.F16, D.BF16, *base) == gnt.Status.INVALID_VALUE
     assert f(FAKE_A, FAKE_B, FAKE_O + 2, D.F16, D.F32, *base) == gnt.Status.INVALID_VALUE

@@ -46,8 +46,12 @@ def run_mx(A, SA, B, SB, ab, out, path, shared_b=False, lda=None, pack_on_host=F
     batch, M, K = A.shape
     N = B.shape[1]
     lda = lda or K
-    a, pa = gpu_util.to_device(A, ab, lda)
-    b, pb = gpu_util.to_device(B[:1] if shared_b else B, ab)
+    if ab in gpu_util.PACKED:
+        a, pa = gpu_util.to_device_packed(A, ab, lda)
+        b, pb = gpu_util.to_device_packed(B[:1] if shared_b else B, ab, K)
+    else:
+        a, pa = gpu_util.to_device(A, ab, lda)
+        b, pb = gpu_util.to_device(B[:1] if shared_b else B, ab)
     SBu = SB[:1] if shared_b else SB
     if pack_on_host:
         sa = torch.from_numpy(pack_ref(SA, K)).cuda()

@@ -138,14 +138,88 @@ def _draw_f8(dtype):
     return draw
 
 
+# 6- and 4-bit floats, one per byte in its low bits: (exponent bits, fraction
+# bits, bias).  Inputs are drawn as values and rounded to the nearest value of
+# the format (ties to the even code), which needs the format's value grid.
+F6F4 = {"e2m3": (2, 3, 1), "e3m2": (3, 2, 3), "e2m1": (2, 1, 1)}
+
+
+def _f6f4_grid(dtype):
+    """(values, codes) of the non-negative codes of a 6- or 4-bit format,
+    ascending."""
+    e, m, b = F6F4[dtype]
+    vals, codes = [], []
+    for expo in range(2 ** e):
+        for frac in range(2 ** m):
+            vals.append(frac / 2 ** m * 2.0 ** (1 - b) if expo == 0 else (1 + frac / 2 ** m) * 2.0 ** (expo - b))
+            codes.append((expo << m) | frac)
+    return np.array(vals), np.array(codes, dtype=np.uint8)
+
+
+def _draw_f6f4(dtype):
+    vals, codes = _f6f4_grid(dtype)
+    e, m, b = F6F4[dtype]
+    sign_bit = np.uint8(1 << (e + m))
+
+    def quantize(v):
+        a = np.minimum(np.abs(v), vals[-1])
+        hi = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
+        lo = hi - 1
+        d_lo, d_hi = a - vals[lo], vals[hi] - a
+        pick = np.where((d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0)), hi, lo)
+        return codes[pick] | np.where(v < 0, sign_bit, np.uint8(0))
+
+    def draw(rng, n, dist, sigma):
+        out = np.empty(n, dtype=np.uint8)
+        if dist == "int4":
+            out[:] = quantize(rng.integers(-4, 5, size=n, dtype=np.int8).astype(np.float64))
+            return out
+        for s in range(0, n, _CHUNK):
+            m_ = min(_CHUNK, n - s)
+            if dist == "uniform":
+                v = rng.uniform(-1.0, 1.0, size=m_)
+            elif dist == "normal":
+                v = sigma * rng.standard_normal(size=m_)
+            else:
+                raise ValueError("unknown distribution %r" % dist)
+            out[s:s + m_] = quantize(v)
+        return out
+    return draw
+
+
+def pack_subbyte(codes, dtype):
+    """Codes of a 6- or 4-bit format (uint8, one per element, (..., K) with K a
+    multiple of 4 or 2) -> the packed storage along the last axis: element k
+    at bits [b*k, b*k + b) of the row's little-endian bit string (b = 6 or 4)."""
+    e, m, _ = F6F4[dtype]
+    b = 1 + e + m
+    c = np.asarray(codes, dtype=np.uint8) & np.uint8((1 << b) - 1)
+    K = c.shape[-1]
+    if b == 4:
+        if K % 2:
+            raise ValueError("fp4 rows need an even number of elements")
+        return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    if K % 4:
+        raise ValueError("fp6 rows need a multiple of 4 elements")
+    g = c.reshape(c.shape[:-1] + (K // 4, 4)).astype(np.uint32)
+    word = g[..., 0] | (g[..., 1] << 6) | (g[..., 2] << 12) | (g[..., 3] << 18)
+    out = np.stack([word & 0xff, (word >> 8) & 0xff, (word >> 16) & 0xff], axis=-1).astype(np.uint8)
+    return out.reshape(c.shape[:-1] + (K // 4 * 3,))
+
+
 def make_inputs(batch, M, N, K, dist="uniform", sigma=1.0, seed=0, dtype="f16"):
     """Return (A, B) of shape (batch,M,K), (batch,N,K) (or (M,K), (N,K) when
     batch == 0 is passed to mean "unbatched"): float16 arrays for dtype "f16",
     uint16 bfloat16 bit patterns for dtype "bf16", uint8 patterns for "e4m3"
-    and "e5m2"."""
+    and "e5m2", and for the 6- and 4-bit floats "e2m3", "e3m2", "e2m1" (values
+    rounded to the nearest code, one code per byte; pack_subbyte gives the
+    packed storage the library takes)."""
     rng = np.random.default_rng(seed)
     nb = max(batch, 1)
-    draw = {"f16": _draw, "bf16": _draw_bf16}[dtype] if dtype in ("f16", "bf16") else _draw_f8(dtype)
+    if dtype in ("f16", "bf16"):
+        draw = {"f16": _draw, "bf16": _draw_bf16}[dtype]
+    else:
+        draw = _draw_f6f4(dtype) if dtype in F6F4 else _draw_f8(dtype)
     A = draw(rng, nb * M * K, dist, sigma).reshape(nb, M, K)
     B = draw(rng, nb * N * K, dist, sigma).reshape(nb, N, K)
     if batch == 0:
