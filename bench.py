@@ -42,6 +42,8 @@ import workloads  # noqa: E402
 
 METRIC = "TFLOP/s fp16→fp32 Out=A·Bᵀ at 8192³; % of dense fp16 peak / HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
+# element widths of the 6- and 4-bit floats, stored packed along K
+PACKED_BITS = {"e2m3": 6, "e3m2": 6, "e2m1": 4}
 
 # DRAM traffic per launch of the dominant kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
@@ -57,19 +59,36 @@ TRAFFIC = {
 }
 
 
+_PAIR_SRC = ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"]
+_ONE_SRC = ["tc05_gemm.cu", "tc05_kernel.cuh", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"]
+_SMALL_SRC = ["tc05_small.cu", "tc05_kernel.cuh", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"]
 KERNEL_SOURCES = {
-    "square_8192": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
-    "square_4096": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
-    "ragged_batch16_3001x2047x1000": ["tc05_pair.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
-    "skinny_64x16384x8192": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
-    "tile_128x64x64": ["tc05_gemm.cu", "tc05_common.cuh", "ptx.cuh", "ptx_mx.cuh"],
+    "square_8192": _PAIR_SRC,
+    "square_4096": _PAIR_SRC,
+    "ragged_batch16_3001x2047x1000": _PAIR_SRC,
+    "skinny_64x16384x8192": _ONE_SRC,
+    "tile_128x64x64": _ONE_SRC,
 }
 
 
-def kernel_source_sha(workload):
-    """sha256 prefix of the sources of the kernel that dominates `workload`."""
+def traffic_key(workload, ab="f16", out="f32", mx=False, path="AUTO"):
+    """TRAFFIC key of a run: the workload, then its element types when not
+    fp16 -> fp32 (with "mx-" for block scales), then an explicit path."""
+    key = workload
+    if mx:
+        key += "/mx-" + ab
+    elif ab != "f16" or out != "f32":
+        key += "/" + ab + ("" if out == "f32" else "->" + out)
+    if mx and out != "f32":
+        key += "->" + out
+    return key + ("" if path == "AUTO" else "/" + path)
+
+
+def kernel_source_sha(workload, path="AUTO"):
+    """sha256 prefix of the sources of the kernel that dominates `workload`
+    (on an explicit path of the other instruction shapes, that kernel's)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[workload]:
+    for name in (_SMALL_SRC if path in ("TC05_M64", "TC05_WS") else KERNEL_SOURCES[workload]):
         with open(os.path.join(ROOT, "dense_fp16_tensor_gemm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -201,7 +220,7 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     A, B = workloads.workload_inputs(w.name, args.ab_dtype)
-    scales = mx_scales(w) if args.mx else None
+    scales = workloads.workload_mx_scales(w.name) if args.mx else None
     per_step = max(1.0, args.cpu_seconds / 5)
     vals = []
     rows_used = None
@@ -225,19 +244,6 @@ def run_reference(args, w):
     }
     print(json.dumps(line), flush=True)
     return 0
-
-
-def mx_scales(w):
-    """Seeded block scales of the workload: (batch, rows, ceil(K/32)) E8M0
-    bytes uniform in 120..134 (2^-7..2^7), A's then B's."""
-    import numpy as np
-    rng = np.random.default_rng(w.seed + 7)
-    kb = (w.K + 31) // 32
-    sa = rng.integers(120, 135, size=(w.batch, w.M, kb)).astype(np.uint8)
-    sb = rng.integers(120, 135, size=(w.batch, w.N, kb)).astype(np.uint8)
-    if w.batch == 1:
-        sa, sb = sa[0], sb[0]
-    return sa, sb
 
 
 def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K", mx=False):
@@ -278,16 +284,19 @@ def main():
                     help="MN: A handed to the library as its transpose, (K, M) row-major")
     ap.add_argument("--b-major", default="K", choices=["K", "MN"],
                     help="MN: B handed to the library as its transpose, (K, N) row-major (the NN product)")
-    ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16", "e4m3", "e5m2"],
-                    help="element type of A and B (bf16, e4m3, e5m2: the same draws rounded to that type)")
+    ap.add_argument("--ab-dtype", default="f16", choices=["f16", "bf16", "e4m3", "e5m2", "e2m3", "e3m2", "e2m1"],
+                    help="element type of A and B (bf16, e4m3, e5m2: the same draws rounded to that type; "
+                         "e2m3, e3m2, e2m1: rounded to that grid and stored packed along K)")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of Out (16-bit: fp32 accumulator rounded to nearest even)")
     ap.add_argument("--mx", action="store_true",
                     help="block-scaled 8-bit product (needs --ab-dtype e4m3 or e5m2): one E8M0 scale per 32 K "
                          "elements of each row, drawn uniformly from 2^-7..2^7 and packed once before timing")
     args = ap.parse_args()
-    if args.mx and args.ab_dtype not in ("e4m3", "e5m2"):
-        ap.error("--mx needs --ab-dtype e4m3 or e5m2")
+    if args.mx and args.ab_dtype not in ("e4m3", "e5m2", "e2m3", "e3m2", "e2m1"):
+        ap.error("--mx needs an 8-, 6- or 4-bit --ab-dtype")
+    if args.ab_dtype in PACKED_BITS and (args.a_major != "K" or args.b_major != "K"):
+        ap.error("packed 6- and 4-bit operands are K-major")
     if args.mx and (args.a_major != "K" or args.b_major != "K"):
         ap.error("--mx takes K-major operands only")
     if args.warmup < 3:
@@ -319,18 +328,26 @@ def main():
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
     codes = {"f16": gnt.DType.F16, "bf16": gnt.DType.BF16, "f32": gnt.DType.F32,
-             "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2}
-    f8 = args.ab_dtype in ("e4m3", "e5m2")
-    ab_es = 1 if f8 else 2
+             "e4m3": gnt.DType.E4M3, "e5m2": gnt.DType.E5M2, "e2m3": gnt.DType.E2M3,
+             "e3m2": gnt.DType.E3M2, "e2m1": gnt.DType.E2M1}
+    packed = args.ab_dtype in PACKED_BITS
+    # the 8-bit MMA kind (8-, 6- and 4-bit elements)
+    f8 = args.ab_dtype in ("e4m3", "e5m2") or packed
+    ab_es = PACKED_BITS[args.ab_dtype] / 8 if packed else (1 if f8 else 2)
     raw = np.uint8 if f8 else np.int16
     A, B = workloads.workload_inputs(w.name, args.ab_dtype)
     batched = A.ndim == 3
-    # stored operands: an MN-major one is its transpose, row-major
+    # stored operands: an MN-major one is its transpose, row-major; 6- and
+    # 4-bit ones packed along K
     As = np.ascontiguousarray(np.swapaxes(A, -1, -2)) if a_mn else A
     Bs = np.ascontiguousarray(np.swapaxes(B, -1, -2)) if b_mn else B
     lda, ldb = As.shape[-1], Bs.shape[-1]
-    a = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).cuda()
-    b = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).cuda()
+    if packed:
+        As, Bs = workloads.pack_subbyte(As, args.ab_dtype), workloads.pack_subbyte(Bs, args.ab_dtype)
+        a, b = torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda()
+    else:
+        a = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).cuda()
+        b = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).cuda()
     out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=tdt[args.out_dtype],
                       device="cuda")
     stream = torch.cuda.current_stream()
@@ -339,7 +356,7 @@ def main():
     sA, sB, sO = (w.M * w.K, w.N * w.K, w.M * w.N) if batched else (0, 0, 0)
     majors = {"K": gnt.Major.K, "MN": gnt.Major.MN}
 
-    scales = mx_scales(w) if args.mx else None
+    scales = workloads.workload_mx_scales(w.name) if args.mx else None
     if args.mx:
         sa_plain = torch.from_numpy(scales[0]).cuda()
         sb_plain = torch.from_numpy(scales[1]).cuda()
@@ -460,9 +477,16 @@ def main():
         # the logical operands: A (M, K) and B^T (K, N), views of the stored ones
         al = a.transpose(-1, -2) if a_mn else a
         bt = b if b_mn else b.transpose(-1, -2)
+        if packed:
+            # cuBLAS's 4-bit floats: two per byte, its float4_e2m1fn_x2 type (no 6-bit type)
+            fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+            ok4 = fp4 is not None and args.ab_dtype == "e2m1"
+            al, bt = (al.view(fp4), bt.view(fp4)) if ok4 else (None, None)
         mm = torch.bmm if batched else torch.mm
         cub_fn = None
-        if args.mx:
+        if packed and not (args.mx and al is not None):
+            cub_fn = None  # no unscaled 6- or 4-bit product in cuBLAS
+        elif args.mx:
             # cuBLAS's block-scaled path: its 128 x 4 blocked scale layout is
             # the library's atom layout
             if not batched:
@@ -495,7 +519,8 @@ def main():
         if cub_fn is not None:
             cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
             cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
-                      "call": ("torch._scaled_mm(A, B^T, E8M0 block scales) -> f32 Out" if args.mx else
+                      "call": ("torch._scaled_mm(A, B^T, E8M0 block scales) -> f32 Out" +
+                               (" (A, B float4_e2m1fn_x2)" if packed else "") if args.mx else
                                "torch._scaled_mm(A, B^T, unit scales) -> f32 Out" if f8 else
                                "torch.%s(A, B^T%s) -> %s Out" % ("bmm" if batched else "mm",
                                                                 ", out_dtype=float32" if cub_out == "f32" else "",
@@ -504,8 +529,11 @@ def main():
 
     # ---- end to end through the host-buffer entry point
     e2e_steps = args.e2e_steps or max(3, args.steps // 4)
-    ha = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
-    hb = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
+    if packed:
+        ha, hb = torch.from_numpy(As).pin_memory(), torch.from_numpy(Bs).pin_memory()
+    else:
+        ha = torch.from_numpy(As.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
+        hb = torch.from_numpy(Bs.view(raw)).view(tdt[args.ab_dtype]).pin_memory()
     ho = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
 
     if args.mx:
@@ -519,7 +547,11 @@ def main():
             b.copy_(hb, non_blocking=True)
             sa_plain.copy_(hsa, non_blocking=True)
             sb_plain.copy_(hsb, non_blocking=True)
-            gnt.gemm_nt_mx_tensors(a, sa_plain, b, sb_plain, out=out, path=path, stream=stream)
+            if packed:
+                gnt.gemm_nt_packed(a, b, w.K, codes[args.ab_dtype], sa_plain, sb_plain, out=out, path=path,
+                                   stream=stream)
+            else:
+                gnt.gemm_nt_mx_tensors(a, sa_plain, b, sb_plain, out=out, path=path, stream=stream)
             ho.copy_(out, non_blocking=True)
         elif default_types and default_layout:
             gnt.gemm_nt_f16_f32_from_host(ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), a.data_ptr(),
@@ -557,14 +589,16 @@ def main():
     # bf16 one times that nominal ratio (4.5 / 2.25 PFLOP/s dense)
     tpeak = peaks["tflops"] * (2.0 if f8 else 1.0)
     tensor_bound = ai * peaks["hbm_gbs"] * 1e9 > tpeak * 1e12
-    tr = TRAFFIC.get(w.name + ("/mx-" + args.ab_dtype if args.mx else ""))
-    traffic = (tr[0] if (default_types or args.mx) and default_layout and tr and tr[1] == kernel_source_sha(w.name)
+    tr = TRAFFIC.get(traffic_key(w.name, args.ab_dtype, args.out_dtype, args.mx, args.path))
+    traffic = (tr[0] if default_layout and tr and tr[1] == kernel_source_sha(w.name, args.path)
                else None)
     if tensor_bound:
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": achieved / tpeak, "traffic": traffic,
-                "peak_source": ("%s bf16 dense burst x 2 (the nominal fp8 / bf16 ratio)" % peaks["source"]
+                "peak_source": ("%s bf16 dense burst x 2 (the nominal fp8 / bf16 ratio%s)" % (
+                                    peaks["source"], "; kind::f8f6f4 runs 6- and 4-bit elements at the "
+                                    "8-bit rate" if packed else "")
                                 if f8 else
                                 "%s bf16 dense burst (kind::f16 runs fp16 at the bf16 rate)" % peaks["source"])}
     else:
@@ -589,7 +623,7 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(A.nbytes + B.nbytes + (scales[0].nbytes + scales[1].nbytes
+                "h2d_bytes_per_step": int(As.nbytes + Bs.nbytes + (scales[0].nbytes + scales[1].nbytes
                                                                   if args.mx else 0)),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
         "clocks": clocks,

@@ -32,7 +32,7 @@ class DType(enum.IntEnum):
     F32 = 2
     E4M3 = 3  # 8-bit floats (A and B only)
     E5M2 = 4
-    E2M3 = 5  # 6- and 4-bit floats, one per byte in its low bits (A and B only)
+    E2M3 = 5  # 6- and 4-bit floats, packed along K, little-endian bits (A and B only)
     E3M2 = 6
     E2M1 = 7
 
@@ -48,6 +48,8 @@ class Path(enum.IntEnum):
     SKINNY = 2
     MMASYNC = 3
     TC05_PAIR = 4
+    TC05_M64 = 5   # 64-row tiles, plain M = 64 MMA
+    TC05_WS = 6    # 32- or 64-row tiles, weight-stationary MMA
 
 
 class GemmError(RuntimeError):
@@ -278,6 +280,51 @@ def gemm_nt_mx_tensors(A, SA, B, SB, out=None, path=Path.AUTO, stream=None, out_
     gemm_nt_mx(A.data_ptr(), pa.data_ptr(), B.data_ptr(), pb.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
                _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"), 1, 0, 0, 0, path,
                _stream_handle(stream))
+    return out
+
+
+PACKED_BITS = {DType.E2M3: 6, DType.E3M2: 6, DType.E2M1: 4}
+
+
+def gemm_nt_packed(A, B, K, ab_dtype, SA=None, SB=None, out=None, path=Path.AUTO, stream=None, out_dtype=None):
+    """Out = A @ B.T for 6- or 4-bit float inputs stored packed: A (M, K*w/8)
+    and B (N, K*w/8) uint8 CUDA tensors (w = 6 for E2M3 / E3M2, 4 for E2M1),
+    element k of a row at bits [w*k, w*k+w) of the row, little-endian.  K is a
+    multiple of 128, rows start on 32-byte boundaries.  With SA (M, K/32) and
+    SB (N, K/32) uint8 E8M0 scales (plain layout) the product is block-scaled
+    as in :func:`gemm_nt_mx_tensors`.  ``out``/``out_dtype`` as in :func:`gemm_nt`."""
+    import torch
+    ab = DType(ab_dtype)
+    if ab not in PACKED_BITS:
+        raise TypeError("ab_dtype must be E2M3, E3M2 or E2M1")
+    bits = PACKED_BITS[ab]
+    if A.dim() != 2 or B.dim() != 2 or A.dtype != torch.uint8 or B.dtype != torch.uint8:
+        raise TypeError("A and B are 2-D uint8 tensors of packed elements")
+    if K * bits % 8 or A.shape[1] != K * bits // 8 or B.shape[1] != K * bits // 8:
+        raise ValueError("A and B must hold K packed elements per row")
+    if (SA is None) != (SB is None):
+        raise ValueError("give both SA and SB, or neither")
+    dt = out.dtype if out is not None else (out_dtype or torch.float32)
+    ocodes = {torch.float32: DType.F32, torch.float16: DType.F16, torch.bfloat16: DType.BF16}
+    if dt not in ocodes:
+        raise TypeError("out must be float32, float16 or bfloat16")
+    M, N = A.shape[0], B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must have shape (M,N)")
+    # pitches in elements: the byte pitch of a row times 8 / w
+    pa_bytes, pb_bytes = _matrix_ld(A, "A"), _matrix_ld(B, "B")
+    if pa_bytes * 8 % bits or pb_bytes * 8 % bits:
+        raise ValueError("row pitches must hold whole packing groups")
+    lda, ldb = pa_bytes * 8 // bits, pb_bytes * 8 // bits
+    if SA is None:
+        gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ocodes[dt], M, N, K, lda, ldb,
+                           _matrix_ld(out, "out"), 1, 0, 0, 0, path, _stream_handle(stream))
+    else:
+        pa, pb = pack_mx_scales(SA, K, stream), pack_mx_scales(SB, K, stream)
+        gemm_nt_mx(A.data_ptr(), pa.data_ptr(), B.data_ptr(), pb.data_ptr(), out.data_ptr(), ab, ocodes[dt], M, N,
+                   K, lda, ldb, _matrix_ld(out, "out"), 1, 0, 0, 0, path, _stream_handle(stream))
     return out
 
 

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_nt.so")
 
-SOURCES = ["gemm_nt_api.cu", "tc05_gemm.cu", "tc05_pair.cu", "mmasync_gemm.cu", "gemm_nt_no_alloc.cu", "mx_scales.cu"]
+SOURCES = ["gemm_nt_api.cu", "tc05_gemm.cu", "tc05_small.cu", "tc05_pair.cu", "mmasync_gemm.cu", "gemm_nt_no_alloc.cu", "mx_scales.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

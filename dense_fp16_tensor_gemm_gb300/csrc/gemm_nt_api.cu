@@ -94,6 +94,7 @@ gemm_status_t device_state(DeviceState** out)
         if (e == cudaSuccess) e = tc05_configure(128, false);
         if (e == cudaSuccess) e = tc05_configure(256, false);
         if (e == cudaSuccess) e = tc05_configure(64, true);
+        if (e == cudaSuccess) e = tc05_small_configure();
         if (e == cudaSuccess) e = tc05_pair_configure(&d.max_pairs);
         d.status = static_cast<uint32_t*>(sym);
         d.init_err = e;
@@ -489,7 +490,10 @@ unsigned long long wait_limit()
     return v ? v : kDefaultWaitLimit;
 }
 
-gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaStream_t stream)
+// tm < 128: tiles of tm rows of A on the plain M = 64 MMA or (ws) on the
+// weight-stationary one; not swapped, unscaled, A K-major.
+gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaStream_t stream, int tm = 128,
+                       bool ws = false)
 {
     // X: the operand on the MMA's M side (128-row tiles); Y: the N side.
     const void* xp = swap ? q.B : q.A;
@@ -499,7 +503,14 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     const int64_t xs = swap ? q.sB : q.sA, ys = swap ? q.sA : q.sB;
     const bool x_mn = swap ? q.b_mn() : q.a_mn(), y_mn = swap ? q.a_mn() : q.b_mn();
     int bn;
-    if (swap) {
+    if (tm < 128) {
+        if (swap || q.mx() || x_mn)
+            return GEMM_ERR_NOT_SUPPORTED;
+        if (ws)
+            bn = tm == 32 ? 256 : (yrows <= 128 ? 128 : 256);
+        else
+            bn = yrows <= 64 ? 64 : (yrows <= 128 ? 128 : 256);
+    } else if (swap) {
         if (yrows > 64)
             return GEMM_ERR_NOT_SUPPORTED;
         bn = 64;
@@ -516,7 +527,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     // (K-major X only: an MN-major box is whole 64-row chunks.)
     const bool rowsplit = swap && !x_mn && !q.mx() && q.batch == 1 && yrows <= bn &&
                           xrows >= 64 * static_cast<int64_t>(d.num_sms) && xrows <= 128 * static_cast<int64_t>(d.num_sms);
-    int xbox = 128;
+    int xbox = tm;
     if (rowsplit) {
         const int64_t share = (xrows + d.num_sms - 1) / d.num_sms;
         xbox = static_cast<int>(std::min<int64_t>(128, (share + 7) / 8 * 8));
@@ -536,7 +547,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     p.rows_x = static_cast<int>(xrows);
     p.rows_y = static_cast<int>(yrows);
     p.batch = static_cast<int>(q.batch);
-    p.tiles_x = static_cast<int>((xrows + 127) / 128);
+    p.tiles_x = static_cast<int>((xrows + tm - 1) / tm);
     p.tiles_y = static_cast<int>((yrows + bn - 1) / bn);
     p.num_kb = static_cast<int>(q.kblocks());
     const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
@@ -559,7 +570,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         // no partial sums, nothing to zero
         p.mode = kModeRowSplit;
         grid = d.num_sms;
-    } else if (swap && q.out_type == GEMM_DTYPE_F32 && ntiles < d.num_sms &&
+    } else if ((swap || tm < 128) && q.out_type == GEMM_DTYPE_F32 && ntiles < d.num_sms &&
                p.total_iters >= 2 * static_cast<long long>(d.num_sms)) {
         // Stream-K when there are too few tiles to fill the GPU: each CTA takes
         // an even share of the (tile, k-block) iterations; tiles cut between
@@ -582,7 +593,9 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
         p.sf_x_bstride = xs == 0 ? 0 : mx_scale_bytes(xrows, q.K);
         p.sf_y_bstride = ys == 0 ? 0 : mx_scale_bytes(yrows, q.K);
     }
-    if (tc05_launch(tmx, tmy, p, bn, swap, grid, q.kind(), stream) != cudaSuccess)
+    const cudaError_t le = tm < 128 ? tc05_small_launch(tmx, tmy, p, bn, tm, ws, grid, q.kind(), stream)
+                                    : tc05_launch(tmx, tmy, p, bn, swap, grid, q.kind(), stream);
+    if (le != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -775,8 +788,7 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         return st;
     if (q.M == 0 || q.N == 0 || q.batch == 0)
         return GEMM_OK;
-    if (path != GEMM_PATH_AUTO && path != GEMM_PATH_TC05 && path != GEMM_PATH_SKINNY &&
-        path != GEMM_PATH_MMASYNC && path != GEMM_PATH_TC05_PAIR)
+    if (path < GEMM_PATH_AUTO || path > GEMM_PATH_TC05_WS)
         return GEMM_ERR_INVALID_VALUE;
     DeviceState* d = nullptr;
     st = device_state(&d);
@@ -803,6 +815,12 @@ gemm_status_t run(const Problem& q, gemm_path_t path, cudaStream_t stream)
         if (!tma_ok(q))
             return GEMM_ERR_NOT_SUPPORTED;
         return run_tc05_pair(q, *d, stream);
+    case GEMM_PATH_TC05_M64:
+    case GEMM_PATH_TC05_WS:
+        if (!tma_ok(q) || q.mx())
+            return GEMM_ERR_NOT_SUPPORTED;
+        return run_tc05(q, *d, false, stream, path == GEMM_PATH_TC05_WS && q.M <= 32 ? 32 : 64,
+                        path == GEMM_PATH_TC05_WS);
     default:
         return GEMM_ERR_NOT_SUPPORTED;
     }

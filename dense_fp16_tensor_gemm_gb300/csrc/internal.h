@@ -90,6 +90,12 @@ struct MmaParams {
 // epilogue; kind 0: 16-bit inputs, 1: 8-bit inputs, 2: 8-bit inputs with block
 // scales (bn 64 or 128, 128-row X tiles).  Returns the launch status.
 cudaError_t tc05_configure(int bn, bool swap);  // one-time per device
+// The same kernel with other instruction shapes: tm = 64 rows on the plain
+// M = 64 MMA (bn 64, 128, 256), or ws: the weight-stationary MMA with tm = 64
+// (bn 128, 256) or 32 (bn 256).  Kinds 0 and 1 (no block scales); X = A.
+cudaError_t tc05_small_configure();  // one-time per device
+cudaError_t tc05_small_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn, int tm,
+                              bool ws, int grid, int kind, cudaStream_t stream);
 cudaError_t tc05_launch(const CUtensorMap& tmx, const CUtensorMap& tmy, const TcParams& p, int bn,
                         bool swap, int grid, int kind, cudaStream_t stream);
 

@@ -167,6 +167,35 @@ __device__ __forceinline__ void tc_mma_w(uint32_t d_tmem, uint32_t alo, uint32_t
     }
 }
 
+// The weight-stationary form (tcgen05.mma.ws, one CTA): M = 32, 64 or 128,
+// N = 64, 128 or 256; no collector buffer reuse (B is read for every
+// instruction).  Operands and descriptors as in tc_mma_w; the accumulator
+// layout differs for M < 128 (see the kernel's configuration).
+template <bool F8>
+__device__ __forceinline__ void tc_mma_ws(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (F8) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "mov.b64 da, {%1, %2};\n\t"
+            "mov.b64 db, {%3, %4};\n\t"
+            "tcgen05.mma.ws.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+            "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "mov.b64 da, {%1, %2};\n\t"
+            "mov.b64 db, {%3, %4};\n\t"
+            "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+            "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 async ops of this
 // thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)

@@ -84,7 +84,7 @@ struct Seg {
 //                  most 128) over all of K; the 128-row operand box starts at
 //                  the first row, so neighbouring boxes overlap and only the
 //                  CTA's own rows are stored
-template <int BN>
+template <int BN, int TM = BM>
 struct WorkIter {
     long long it, end;
     int tile, step, mode;
@@ -138,8 +138,8 @@ struct WorkIter {
             tile += step;
         }
         decode_tile(p, t, s.b, tx, ty);
-        s.x0 = tx * BM;
-        s.xend = s.x0 + BM < p.rows_x ? s.x0 + BM : p.rows_x;
+        s.x0 = tx * TM;
+        s.xend = s.x0 + TM < p.rows_x ? s.x0 + TM : p.rows_x;
         s.y0 = ty * BN;
         s.partial = s.kb0 != 0 || s.kb1 != p.num_kb;
         return true;
@@ -241,21 +241,27 @@ __device__ __forceinline__ void store_rows_chunk(const TcParams& p, typename Out
 
 // One epilogue warp's share of a finished accumulator: TMEM lane quadrant q
 // (tile rows s.x0 + 32q .. +31) and accumulator columns [c_begin, c_end),
-// where `tacc` is the TMEM address of the accumulator's first column.
+// where `tacc` is the TMEM address of the accumulator's first column.  Other
+// accumulator layouts (64-row and weight-stationary MMAs) give the quadrant's
+// first tile row (row_off >= 0), its number of rows (row_cap) and the tile
+// column of its TMEM column 0 (col_off).
 // Rows >= s.xend and columns >= rows_y are not stored; `stage_buf` is this
 // warp's 32x32 fp32 staging area (unused when SWAP).  Partial segments (a
 // k range short of all of K) add into (fp32) Out with atomics.
 template <bool SWAP, int OT>
 __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, uint32_t tacc, int q,
-                                               int c_begin, int c_end, int lane, float* stage_buf)
+                                               int c_begin, int c_end, int lane, float* stage_buf,
+                                               int row_off = -1, int row_cap = 32, int col_off = 0)
 {
     using S = OutStore<OT>;
     const bool partial = s.partial;
     const uint32_t tbase = tacc + (static_cast<uint32_t>(q * 32) << 16);
     typename S::T* obase = static_cast<typename S::T*>(p.out) + static_cast<int64_t>(s.b) * p.stride_o;
-    const int x_row0 = s.x0 + q * 32;
-    const int nx = s.xend - x_row0;  // valid rows of this quadrant (may exceed 32)
-    const int y0 = s.y0;
+    const int x_row0 = s.x0 + (row_off < 0 ? q * 32 : row_off);
+    int nx = s.xend - x_row0;  // valid rows of this quadrant
+    if (nx > row_cap)
+        nx = row_cap;
+    const int y0 = s.y0 + col_off;
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 32) {
         if (nx <= 0 || y0 + c >= p.rows_y)

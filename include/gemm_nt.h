@@ -83,7 +83,10 @@ typedef enum gemm_path {
     GEMM_PATH_TC05 = 1,     /* persistent tcgen05 kernel, TMEM accumulator, one CTA per tile */
     GEMM_PATH_SKINNY = 2,   /* tcgen05 with swapped operands and split K, for small M */
     GEMM_PATH_MMASYNC = 3,  /* ldmatrix + mma.sync m16n8k16 warp kernel, any layout */
-    GEMM_PATH_TC05_PAIR = 4 /* tcgen05 on a CTA pair (cta_group::2), 256-row tiles */
+    GEMM_PATH_TC05_PAIR = 4, /* tcgen05 on a CTA pair (cta_group::2), 256-row tiles */
+    GEMM_PATH_TC05_M64 = 5,  /* one CTA per 64-row tile, plain M = 64 tcgen05.mma (few rows of A) */
+    GEMM_PATH_TC05_WS = 6    /* one CTA per 32- or 64-row tile, weight-stationary tcgen05.mma.ws
+                                (M = 32 when M <= 32, else 64) */
 } gemm_path_t;
 
 /*

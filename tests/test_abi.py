@@ -81,8 +81,11 @@ def test_batched_validation(lib):
     # negative stride
     assert f(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 2, -64, 64, 64, None) == gnt.Status.INVALID_VALUE
     # bad explicit path
-    assert lib.gemm_nt_f16_f32_batched_path(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 1, 0, 0, 0, 99,
-                                            None) == gnt.Status.INVALID_VALUE
+    for bad in (99, 7, -1):
+        assert lib.gemm_nt_f16_f32_batched_path(FAKE_A, FAKE_B, FAKE_O, 8, 8, 8, 8, 8, 8, 1, 0, 0, 0, bad,
+                                                None) == gnt.Status.INVALID_VALUE
+    # the path numbers of the header
+    assert [int(x) for x in gnt.Path] == list(range(7))
 
 
 def test_from_host_validation(lib):

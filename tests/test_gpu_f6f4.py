@@ -100,3 +100,54 @@ def test_block_scaled_integers_exact(ab):
     A, SA, B, SB = draw(1, 256, 640, 1024, ab, dist="int4", seed=607, lo=124, hi=131)
     ref, _ = oracle.gemm_nt_mx(A, SA, B, SB, dtype=ab)
     check_exact(run_mx(A, SA, B, SB, ab, "f32", P.AUTO), ref, "f32", "mx integers %s" % ab)
+
+
+@pytest.mark.parametrize("ab,mx", [("e2m1", False), ("e2m3", False), ("e2m1", True), ("e3m2", True)])
+def test_square_8192_sampled(ab, mx):
+    """The 8192^3 workload's draws rounded to the type, as the benchmark runs
+    it (its block scales for the block-scaled product), on the path it takes;
+    sampled rows and columns across tile edges and random elements."""
+    import gpu_util
+    A, B = workloads.workload_inputs("square_8192", ab)
+    A3, B3 = A[None], B[None]
+    if mx:
+        SA, SB = workloads.workload_mx_scales("square_8192")
+        got = run_mx(A3, SA[None], B3, SB[None], ab, "f32", P.AUTO)
+    else:
+        got = run_general(A3, B3, ab, "f32", P.AUTO)
+    bb, ii, jj = gpu_util.sample_indices(1, 8192, 8192, 4096, rows=(0, 127, 128, 4095, -1), cols=(0, 255, 256, -1))
+    if mx:
+        ref, absdot = oracle.gemm_nt_sampled_mx(A3, SA[None], B3, SB[None], bb, ii, jj, dtype=ab)
+    else:
+        ref, absdot = oracle.gemm_nt_sampled(A3, B3, bb, ii, jj, dtype=ab)
+    check_tol(got[bb, ii, jj], ref, absdot, "f32", "square_8192 %s%s" % (ab, " mx" if mx else ""))
+
+
+@pytest.mark.parametrize("ab", F6F4)
+def test_torch_binding(ab):
+    """gemm_nt_packed on uint8 tensors of packed rows, plain and block-scaled,
+    and its argument checks."""
+    import torch
+    code = getattr(gnt.DType, ab.upper())
+    A, B = _inputs(1, 130, 250, 256, ab, seed=608)
+    a = torch.from_numpy(workloads.pack_subbyte(A[0], ab)).cuda()
+    b = torch.from_numpy(workloads.pack_subbyte(B[0], ab)).cuda()
+    ref, absdot = oracle.gemm_nt(A, B, dtype=ab)
+    out = gnt.gemm_nt_packed(a, b, 256, code)
+    check_tol(out.double().cpu().numpy()[None], ref, absdot, "f32", "gemm_nt_packed %s" % ab)
+    rng = np.random.default_rng(609)
+    SA = rng.integers(122, 133, size=(130, 8)).astype(np.uint8)
+    SB = rng.integers(122, 133, size=(250, 8)).astype(np.uint8)
+    ref, absdot = oracle.gemm_nt_mx(A, SA[None], B, SB[None], dtype=ab)
+    out = gnt.gemm_nt_packed(a, b, 256, code, torch.from_numpy(SA).cuda(), torch.from_numpy(SB).cuda(),
+                             out_dtype=torch.bfloat16)
+    check_tol(out.double().cpu().numpy()[None], ref, absdot, "bf16", "gemm_nt_packed mx %s" % ab)
+    with pytest.raises(ValueError):
+        gnt.gemm_nt_packed(a, b, 128, code)  # rows hold 256 elements
+    with pytest.raises(TypeError):
+        gnt.gemm_nt_packed(a.view(torch.int8), b, 256, code)
+    with pytest.raises(TypeError):
+        gnt.gemm_nt_packed(a, b, 256, gnt.DType.E4M3)
+    with pytest.raises(ValueError):
+        gnt.gemm_nt_packed(a, b, 256, code, torch.from_numpy(SA).cuda())
+    torch.cuda.synchronize()

@@ -231,3 +231,18 @@ def workload_inputs(name, dtype="f16"):
     """Inputs of a named workload: 2-D for batch 1, 3-D otherwise."""
     w = WORKLOADS[name]
     return make_inputs(0 if w.batch == 1 else w.batch, w.M, w.N, w.K, w.dist, w.sigma, w.seed, dtype)
+
+
+def workload_mx_scales(name):
+    """Seeded block scales of a named workload for the block-scaled product:
+    E8M0 bytes uniform in 120..134 (2^-7..2^7), one per 32 K elements of each
+    row, (rows, ceil(K/32)) for batch 1 else (batch, rows, ceil(K/32)); A's,
+    then B's."""
+    w = WORKLOADS[name]
+    rng = np.random.default_rng(w.seed + 7)
+    kb = (w.K + 31) // 32
+    sa = rng.integers(120, 135, size=(w.batch, w.M, kb)).astype(np.uint8)
+    sb = rng.integers(120, 135, size=(w.batch, w.N, kb)).astype(np.uint8)
+    if w.batch == 1:
+        sa, sb = sa[0], sb[0]
+    return sa, sb
