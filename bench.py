@@ -50,12 +50,16 @@ PACKED_BITS = {"e2m3": 6, "e3m2": 6, "e2m1": 4}
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1084634368 + 248275456, "31005f3dea441fb4"),
-    "square_4096": (91346688 + 35053568, "31005f3dea441fb4"),
-    "ragged_batch16_3001x2047x1000": (171426816 + 342086400, "31005f3dea441fb4"),
-    "skinny_64x16384x8192": (269561856 + 3363072, "6b8cc54f64f26f7a"),
-    # block-scaled E4M3 inputs (--ab-dtype e4m3 --mx)
-    "square_8192/mx-e4m3": (347736320 + 238664960, "31005f3dea441fb4"),
+    "square_8192": (1081261056 + 249404160, "8a330fdcc73ab27a"),
+    "square_4096": (91230720 + 35089408, "8a330fdcc73ab27a"),
+    "ragged_batch16_3001x2047x1000": (171572736 + 342032640, "8a330fdcc73ab27a"),
+    "skinny_64x16384x8192": (269560832 + 3345408, "21f72969d813343d"),
+    # block-scaled E4M3 and E2M1 inputs (--ab-dtype e4m3 / e2m1 --mx), packed E2M1 (--ab-dtype e2m1)
+    "square_8192/mx-e4m3": (347773440 + 238179584, "8a330fdcc73ab27a"),
+    "square_8192/mx-e2m1": (172656128 + 218741760, "8a330fdcc73ab27a"),
+    "square_8192/e2m1": (156268800 + 216002816, "8a330fdcc73ab27a"),
+    # the weight-stationary shape on the skinny product (--path TC05_WS)
+    "skinny_64x16384x8192/TC05_WS": (278229504 + 5609472, "ebb199268b42ed4b"),
 }
 
 
