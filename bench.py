@@ -20,8 +20,11 @@ JSON line.
   --impl reference  times that oracle alone (the reference arm of this bench)
 
 Inputs of the default workload (512 MiB touched per step) exceed the 129 MB L2,
-so no L2 flush is needed between steps; smaller workloads flush L2 by writing a
-256 MiB buffer between timed steps.
+so no L2 flush is needed between steps.  Workloads of 16 MiB to 2x L2 rotate
+over enough copies of their operands and Out (more than 3x L2 in all) that each
+copy has left L2 before it is used again, and run back to back; smaller ones
+flush L2 by writing a 256 MiB buffer between timed steps (the flush's dirty
+lines then drain to DRAM during the next step, which the rotation avoids).
 """
 import argparse
 import hashlib
@@ -50,16 +53,16 @@ PACKED_BITS = {"e2m3": 6, "e3m2": 6, "e2m1": 4}
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1081261056 + 249404160, "8a330fdcc73ab27a"),
-    "square_4096": (91230720 + 35089408, "8a330fdcc73ab27a"),
-    "ragged_batch16_3001x2047x1000": (171572736 + 342032640, "8a330fdcc73ab27a"),
-    "skinny_64x16384x8192": (269560832 + 3345408, "21f72969d813343d"),
+    "square_8192": (1075527168 + 247324416, "5eeefbcb8d5dcc0c"),
+    "square_4096": (90972672 + 34517248, "5eeefbcb8d5dcc0c"),
+    "ragged_batch16_3001x2047x1000": (171270144 + 342383104, "5eeefbcb8d5dcc0c"),
+    "skinny_64x16384x8192": (269564416 + 3291648, "e9c104892387d81b"),
     # block-scaled E4M3 and E2M1 inputs (--ab-dtype e4m3 / e2m1 --mx), packed E2M1 (--ab-dtype e2m1)
-    "square_8192/mx-e4m3": (347773440 + 238179584, "8a330fdcc73ab27a"),
-    "square_8192/mx-e2m1": (172656128 + 218741760, "8a330fdcc73ab27a"),
-    "square_8192/e2m1": (156268800 + 216002816, "8a330fdcc73ab27a"),
+    "square_8192/mx-e4m3": (353830912 + 238180096, "5eeefbcb8d5dcc0c"),
+    "square_8192/mx-e2m1": (172762368 + 218801664, "5eeefbcb8d5dcc0c"),
+    "square_8192/e2m1": (156846848 + 215832064, "5eeefbcb8d5dcc0c"),
     # the weight-stationary shape on the skinny product (--path TC05_WS)
-    "skinny_64x16384x8192/TC05_WS": (278229504 + 5609472, "ebb199268b42ed4b"),
+    "skinny_64x16384x8192/TC05_WS": (278258432 + 5642752, "6f06c65923268fb5"),
 }
 
 
@@ -250,7 +253,7 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K", mx=False):
+def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K", mx=False, n_sets=1):
     cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) %s row-major, "
                        "fp32 accumulate, %s Out" % (
                            w.name, w.description, "%d," % w.batch if w.batch > 1 else "", w.M, w.K,
@@ -264,8 +267,13 @@ def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", 
             "(K,N) row-major" if b_major == "MN" else "(N,K) row-major")
     alg_bytes = alg_bytes or w.bytes
     if flush is not None:
-        cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (alg_bytes / 2 ** 20)
-                     if not flush else "L2 flushed between timed steps (256 MiB write)")
+        if n_sets > 1:
+            cfg["l2"] = ("operands and Out rotate over %d copies (%.0f MiB each, %.0f MiB in all > 3 x 129 MB L2): "
+                         "each copy has left L2 before its next use; steps back to back, no flush"
+                         % (n_sets, alg_bytes / 2 ** 20, n_sets * alg_bytes / 2 ** 20))
+        else:
+            cfg["l2"] = ("inputs larger than L2 (%.0f MiB per step > 129 MB L2), no flush" % (alg_bytes / 2 ** 20)
+                         if not flush else "L2 flushed between timed steps (256 MiB write)")
     if mx:
         cfg["block_scales"] = ("one E8M0 scale per 32 K elements of each row of A and B, uniform 2^-7..2^7 "
                                "(seed + 7), packed into the atom layout once before timing")
@@ -367,7 +375,25 @@ def main():
         sa_packed = gnt.pack_mx_scales(sa_plain, w.K)
         sb_packed = gnt.pack_mx_scales(sb_plain, w.K)
 
-    def step():
+    # algorithmic bytes: A and B (and their block scales) read once, Out written once
+    alg_bytes = float(w.batch) * (ab_es * w.M * w.K + ab_es * w.N * w.K + out.element_size() * w.M * w.N)
+    if args.mx:
+        alg_bytes += float(w.batch) * (w.M + w.N) * ((w.K + 31) // 32)
+    # cold-L2 timing: rotate over copies, or flush (see the module docstring)
+    rotate = 16 * 2 ** 20 <= alg_bytes <= 2 * L2_BYTES
+    flush = alg_bytes <= 2 * L2_BYTES and not rotate
+    n_sets = 1 + int(np.ceil(3 * L2_BYTES / alg_bytes)) if rotate else 1
+    sets = [(a, b, out, sa_packed if args.mx else None, sb_packed if args.mx else None)]
+    for _ in range(n_sets - 1):
+        sets.append((a.clone(), b.clone(), torch.empty_like(out), sa_packed.clone() if args.mx else None,
+                     sb_packed.clone() if args.mx else None))
+    cur = [0]
+
+    def step(fixed=False):
+        i = 0 if fixed else cur[0]
+        if not fixed:
+            cur[0] = (cur[0] + 1) % n_sets
+        a, b, out, sa_packed, sb_packed = sets[i]
         if args.mx:
             gnt.gemm_nt_mx(a.data_ptr(), sa_packed.data_ptr(), b.data_ptr(), sb_packed.data_ptr(), out.data_ptr(),
                            codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB,
@@ -384,11 +410,6 @@ def main():
                                    codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB, sO,
                                    path, sh)
 
-    # algorithmic bytes: A and B (and their block scales) read once, Out written once
-    alg_bytes = float(w.batch) * (ab_es * w.M * w.K + ab_es * w.N * w.K + out.element_size() * w.M * w.N)
-    if args.mx:
-        alg_bytes += float(w.batch) * (w.M + w.N) * ((w.K + 31) // 32)
-    flush = alg_bytes <= 2 * L2_BYTES
     scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
 
     for _ in range(args.warmup):
@@ -461,14 +482,14 @@ def main():
         torch.cuda.synchronize()
         return sum(x.elapsed_time(y) for x, y in ts) / n
 
-    # ---- hot-L2 figure for workloads that fit in L2 (steps back to back, no flush)
+    # ---- hot-L2 figure for workloads that fit in L2 (one set of operands back to back)
     hot = None
-    if flush:
+    if flush or rotate:
         h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         h0.record(stream)
         for _ in range(args.steps):
-            step()
+            step(fixed=True)
         h1.record(stream)
         torch.cuda.synchronize()
         hot_ms = h0.elapsed_time(h1) / args.steps
@@ -478,14 +499,25 @@ def main():
     # ---- context: cuBLAS on the same operands, timed the same way
     cublas = None
     if not args.no_cublas:
-        # the logical operands: A (M, K) and B^T (K, N), views of the stored ones
-        al = a.transpose(-1, -2) if a_mn else a
-        bt = b if b_mn else b.transpose(-1, -2)
-        if packed:
-            # cuBLAS's 4-bit floats: two per byte, its float4_e2m1fn_x2 type (no 6-bit type)
-            fp4 = getattr(torch, "float4_e2m1fn_x2", None)
-            ok4 = fp4 is not None and args.ab_dtype == "e2m1"
-            al, bt = (al.view(fp4), bt.view(fp4)) if ok4 else (None, None)
+        # the logical operands of each set: A (M, K) and B^T (K, N), views of the stored ones
+        def operands(i):
+            sa_, sb_ = sets[i][0], sets[i][1]
+            al_ = sa_.transpose(-1, -2) if a_mn else sa_
+            bt_ = sb_ if b_mn else sb_.transpose(-1, -2)
+            if packed:
+                # cuBLAS's 4-bit floats: two per byte, its float4_e2m1fn_x2 type (no 6-bit type)
+                fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+                ok4 = fp4 is not None and args.ab_dtype == "e2m1"
+                al_, bt_ = (al_.view(fp4), bt_.view(fp4)) if ok4 else (None, None)
+            return al_, bt_
+        ops = [operands(i) for i in range(n_sets)]
+        al, bt = ops[0]
+        ccur = [0]
+
+        def nxt():
+            i = ccur[0]
+            ccur[0] = (i + 1) % n_sets
+            return i
         mm = torch.bmm if batched else torch.mm
         cub_fn = None
         if packed and not (args.mx and al is not None):
@@ -496,10 +528,14 @@ def main():
             if not batched:
                 try:
                     e8 = torch.float8_e8m0fnu
-                    csa, csb = sa_packed.view(e8), sb_packed.view(e8)
-                    torch._scaled_mm(al, bt, scale_a=csa, scale_b=csb, out_dtype=torch.float32)
-                    cub_fn, cub_out = (lambda: torch._scaled_mm(al, bt, scale_a=csa, scale_b=csb,
-                                                                out_dtype=torch.float32)), "f32"
+                    scs = [(st[3].view(e8), st[4].view(e8)) for st in sets]
+                    torch._scaled_mm(al, bt, scale_a=scs[0][0], scale_b=scs[0][1], out_dtype=torch.float32)
+
+                    def cub_mx():
+                        i = nxt()
+                        return torch._scaled_mm(ops[i][0], ops[i][1], scale_a=scs[i][0], scale_b=scs[i][1],
+                                                out_dtype=torch.float32)
+                    cub_fn, cub_out = cub_mx, "f32"
                 except (TypeError, RuntimeError, NotImplementedError, AttributeError):
                     cub_fn = None
         elif f8:
@@ -510,18 +546,29 @@ def main():
             if not batched and not a_mn and not b_mn:
                 try:
                     torch._scaled_mm(al, bt, scale_a=one, scale_b=one, out_dtype=torch.float32)
-                    cub_fn, cub_out = (lambda: torch._scaled_mm(al, bt, scale_a=one, scale_b=one,
-                                                                out_dtype=torch.float32)), "f32"
+
+                    def cub_f8():
+                        i = nxt()
+                        return torch._scaled_mm(ops[i][0], ops[i][1], scale_a=one, scale_b=one,
+                                                out_dtype=torch.float32)
+                    cub_fn, cub_out = cub_f8, "f32"
                 except (TypeError, RuntimeError, NotImplementedError):
                     cub_fn = None
         else:
+            def cub_mm32():
+                i = nxt()
+                return mm(ops[i][0], ops[i][1], out_dtype=torch.float32)
+
+            def cub_mm():
+                i = nxt()
+                return mm(ops[i][0], ops[i][1])
             try:
                 mm(al, bt, out_dtype=torch.float32)
-                cub_fn, cub_out = (lambda: mm(al, bt, out_dtype=torch.float32)), "f32"
+                cub_fn, cub_out = cub_mm32, "f32"
             except (TypeError, RuntimeError, NotImplementedError):
-                cub_fn, cub_out = (lambda: mm(al, bt)), args.ab_dtype
+                cub_fn, cub_out = cub_mm, args.ab_dtype
         if cub_fn is not None:
-            cub_ms = timed(cub_fn, max(3, min(args.steps, 100)))
+            cub_ms = timed(cub_fn, max(3, args.steps))
             cublas = {"value": w.flops / (cub_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": cub_ms,
                       "call": ("torch._scaled_mm(A, B^T, E8M0 block scales) -> f32 Out" +
                                (" (A, B float4_e2m1fn_x2)" if packed else "") if args.mx else
@@ -623,7 +670,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.ab_dtype, "data": "synthetic",
         "config": workload_config(w, flush, args.ab_dtype, args.out_dtype, alg_bytes, args.a_major, args.b_major,
-                                  args.mx),
+                                  args.mx, n_sets),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s",

@@ -41,10 +41,17 @@ constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // 9.  The MMA still reads 128 rows: rows XR..127 come from the next slot and
 // only feed accumulator rows that are never stored.
 // KIND: 0 16-bit inputs (kind::f16), 1 8-bit inputs (kind::f8f6f4), 2 8-bit
-// inputs with block scales (kind::mxf8f6f4): each stage then also holds one
-// 512-byte scale atom for X and one for Y, and TMEM holds, after the two
-// accumulators, 8 columns of scales per stage (X atom, then Y atom).
+// inputs with block scales (kind::mxf8f6f4).  Block-scaled, the scale atoms
+// (512 bytes per 128 rows and 128 elements of K) come through a ring of two
+// scale stages of their own, each holding the atoms of kScaleKb consecutive
+// k-blocks of X and of Y -- contiguous in the packed layout, so one bulk copy
+// each; one 512-byte copy per operand and k-block beside the data loads held
+// the stream to half its rate.  TMEM holds, after the two accumulators, 8
+// columns of scales per data stage (X atom, then Y atom), which the MMA thread
+// fills with tcgen05.cp before the stage's MMAs.
 constexpr int kKind16 = 0, kKind8 = 1, kKindMx = 2;
+constexpr int kScaleKb = 8;      // k-blocks of scale atoms per scale stage
+constexpr int kScaleStages = 2;
 
 constexpr int pow2_at_least(int v)
 {
@@ -66,25 +73,27 @@ template <int BN, bool SWAP, int XR = 128, int KIND = kKind16, int TM = 128, boo
 struct Cfg {
     static constexpr int X_BYTES = XR * BK * 2;
     static constexpr int Y_BYTES = BN * BK * 2;
-    static constexpr int SF_BYTES = KIND == kKindMx ? 1024 : 0;
-    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES + SF_BYTES;
+    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
+    // block-scaled: scale stage t holds X's atoms [t][j], then Y's, j < kScaleKb
+    static constexpr int SC_STAGE_BYTES = 2 * kScaleKb * 512;
+    static constexpr int SC_BYTES = KIND == kKindMx ? kScaleStages * SC_STAGE_BYTES : 0;
     static constexpr int EPI_BYTES = SWAP ? 0 : 8 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
     static constexpr int BAR_BYTES = 256;
     static constexpr int BASE_STAGES =
         TM < 128 ? 8 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? (XR <= 112 ? 10 : 9) : 8)));
-    static constexpr int FIT_STAGES = (232448 - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int FIT_STAGES = (232448 - 1024 - SC_BYTES - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = BASE_STAGES < FIT_STAGES ? BASE_STAGES : FIT_STAGES;
     static constexpr int ACC_COLS = WS ? BN * TM / 128 : BN;  // TMEM columns of one accumulator
     static constexpr int SF_COL = 2 * ACC_COLS;               // first TMEM column of the scale slots
     static constexpr int TMEM_COLS = pow2_at_least(2 * ACC_COLS + (KIND == kKindMx ? 8 * STAGES : 0));
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SC_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(TM, BN);
     static_assert(TM == 128 || (!SWAP && KIND != kKindMx && XR == TM), "small tiles: plain operands, X = A");
     static_assert(WS ? (TM == 32 || TM == 64 || TM == 128) && (BN == 64 || BN == 128 || BN == 256)
                      : (TM == 64 || TM == 128), "instruction shapes");
     static_assert(ACC_COLS % 64 == 0, "each epilogue warp takes whole 32-column chunks");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert((2 * STAGES + 5 + 2 * kScaleStages) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(X_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
     static_assert(TMEM_COLS <= 512, "Tensor Memory columns");
 };
@@ -106,9 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xs = smem;
     uint8_t* ys = smem + STAGES * C::X_BYTES;
-    uint8_t* sfs = ys + STAGES * C::Y_BYTES;  // MX: per stage the X atom, then the Y atom
-    float* epi = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES);
+    uint8_t* sfs = ys + STAGES * C::Y_BYTES;  // MX: the scale stages
+    float* epi = reinterpret_cast<float*>(sfs + C::SC_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sfs + C::SC_BYTES + C::EPI_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -116,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* sc_full = drain + 2;                 // MX: scale stage t has landed
+    uint64_t* sc_empty = sc_full + kScaleStages;   // MX: the copies that read scale stage t are done
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -130,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&tempty[b]), 256);
         }
         mbar_init(smem_u32(drain), 1);
+        for (int t = 0; t < kScaleStages; ++t) {
+            mbar_init(smem_u32(&sc_full[t]), 1);
+            mbar_init(smem_u32(&sc_empty[t]), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmx);
@@ -170,11 +185,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bytes the two data loads credit: packed 6- and 4-bit elements count
             // their global bytes, width / 8 of the shared ones
             const uint32_t data_tx = (p.x_box_bytes + C::Y_BYTES) * (p.ab_packed_bits ? p.ab_packed_bits : 8) / 8;
+            int sst = 0;  // MX: scale stage ring
+            uint32_t sphase = 0, sc_filled = 0, sc_parity = 0;
+            // Swapped operands (few rows of A): X = B is streamed once, every CTA
+            // re-reads all of Y = A.  Marking B evict_first and A evict_last keeps
+            // A in L2 under the stream (8-bit skinny products 8 % faster, 16-bit 2 %).
+            const bool hints = SWAP && !p.x_mn && !p.y_mn;
+            const uint64_t pol_x = l2_policy_evict_first(), pol_y = l2_policy_evict_last();
             bool first = true, ok = true;
             WorkIter<BN, TM> w(p);
             Seg s;
             while (ok && w.next(s)) {
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (MX && (kb == s.kb0 || kb % kScaleKb == 0)) {
+                        // the next scale stage: atoms of k-blocks [kb, kg0 + 8) of the
+                        // row blocks of x0 and y0, contiguous in the packed layout
+                        if (!wait_bounded(smem_u32(&sc_empty[sst]), sphase ^ 1, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        const int kg0 = kb - kb % kScaleKb;
+                        const int n = p.num_kb - kg0 < kScaleKb ? p.num_kb - kg0 : kScaleKb;
+                        const uint32_t sb = smem_u32(&sc_full[sst]);
+                        const uint32_t sd = smem_u32(sfs + sst * C::SC_STAGE_BYTES);
+                        mbar_arrive_expect_tx(sb, static_cast<uint32_t>(2 * 512 * n));
+                        bulk_load(sd, p.sf_x + s.b * p.sf_x_bstride + (static_cast<int64_t>(s.x0 / BM) * p.num_kb + kg0) * 512,
+                                  static_cast<uint32_t>(512 * n), sb);
+                        bulk_load(sd + kScaleKb * 512,
+                                  p.sf_y + s.b * p.sf_y_bstride + (static_cast<int64_t>(s.y0 / BM) * p.num_kb + kg0) * 512,
+                                  static_cast<uint32_t>(512 * n), sb);
+                        sc_filled |= 1u << sst;
+                        sc_parity = (sc_parity & ~(1u << sst)) | (sphase << sst);
+                        if (++sst == kScaleStages) {
+                            sst = 0;
+                            sphase ^= 1;
+                        }
+                    }
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.wait_limit)) {
                         raise_timeout(p, abort_flag);
                         ok = false;
@@ -184,20 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     first = false;
                     if (!drop) {
                         const uint32_t fb = smem_u32(&full[stage]);
-                        mbar_arrive_expect_tx(fb, data_tx + C::SF_BYTES);
-                        load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * KE, s.x0,
-                                         s.b * p.x_bmul);
-                        load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * KE, s.y0,
-                                         s.b * p.y_bmul);
-                        if constexpr (MX) {
-                            // the stage's scale atoms: rows [128*(x0/128), +128) of X and
-                            // [128*(y0/128), +128) of Y, K blocks 4*kb .. 4*kb+3
-                            const uint32_t sfd = smem_u32(sfs + stage * C::SF_BYTES);
-                            bulk_load(sfd, p.sf_x + s.b * p.sf_x_bstride + (static_cast<int64_t>(s.x0 / BM) * p.num_kb + kb) * 512,
-                                      512, fb);
-                            bulk_load(sfd + 512,
-                                      p.sf_y + s.b * p.sf_y_bstride + (static_cast<int64_t>(s.y0 / BM) * p.num_kb + kb) * 512,
-                                      512, fb);
+                        mbar_arrive_expect_tx(fb, data_tx);
+                        if (hints) {
+                            tma_load_3d_hint(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, kb * KE, s.x0,
+                                             s.b * p.x_bmul, pol_x);
+                            tma_load_3d_hint(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, kb * KE, s.y0,
+                                             s.b * p.y_bmul, pol_y);
+                        } else {
+                            load_operand<XR>(smem_u32(xs + stage * C::X_BYTES), &tmx, fb, p.x_mn, kb * KE, s.x0,
+                                             s.b * p.x_bmul);
+                            load_operand<BN>(smem_u32(ys + stage * C::Y_BYTES), &tmy, fb, p.y_mn, kb * KE, s.y0,
+                                             s.b * p.y_bmul);
                         }
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -209,6 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Let every load this thread issued land before the CTA can exit.
+            for (int st = 0; st < kScaleStages; ++st) {
+                if (sc_filled & (1u << st)) {
+                    const uint32_t par = (sc_parity >> st) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(smem_u32(&sc_full[st]), par) &&
+                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                    }
+                }
+            }
             for (int st = 0; st < STAGES; ++st) {
                 if (filled & (1u << st)) {
                     const uint32_t par = (fill_parity >> st) & 1u;
@@ -233,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t fa = full0, ea = empty0, xlo = dx.lo, ylo = dy.lo;
             int stage = 0;
             uint32_t phase = 0;
+            int sst = 0;  // MX: scale stage ring
+            uint32_t sphase = 0, sc_cur = 0;
             int local = 0;
             bool skip_release = p.fault == 2 && blockIdx.x == 0;  // test hook: lose one stage release
             bool ok = true;
@@ -258,18 +313,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     if constexpr (MX) {
-                        // The scale slot of a stage is refilled only after the
+                        if (kb == s.kb0 || kb % kScaleKb == 0) {
+                            if (!wait_bounded(smem_u32(&sc_full[sst]), sphase, abort_flag, p.wait_limit)) {
+                                raise_timeout(p, abort_flag);
+                                ok = false;
+                                break;
+                            }
+                            sc_cur = sf_smem0 + static_cast<uint32_t>(sst * C::SC_STAGE_BYTES);
+                        }
+                        // The scale slot of a data stage is refilled only after the
                         // stage's previous MMAs completed (its release), and the
                         // copy is ordered before the MMAs that follow it.
                         const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + 8 * stage);
-                        const uint32_t sfd = sf_smem0 + static_cast<uint32_t>(stage * C::SF_BYTES);
-                        tc_cp_atom(sft, atom_desc(sfd));
-                        tc_cp_atom(sft + 4, atom_desc(sfd + 512));
+                        const uint32_t j = static_cast<uint32_t>(kb % kScaleKb);
+                        tc_cp_atom(sft, atom_desc(sc_cur + j * 512));
+                        tc_cp_atom(sft + 4, atom_desc(sc_cur + (kScaleKb + j) * 512));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             tc_mma_mx(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi,
                                       idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4), sft,
                                       sft + 4 + y_sf_off, (k > 0 || kb != s.kb0) ? 1u : 0u);
+                        if (kb % kScaleKb == kScaleKb - 1 || kb == s.kb1 - 1) {
+                            // the scale stage's last copies: free it once they are done
+                            tc_commit(smem_u32(&sc_empty[sst]));
+                            if (++sst == kScaleStages) {
+                                sst = 0;
+                                sphase ^= 1;
+                            }
+                        }
                     } else if constexpr (WS) {
                         tc_mma_ws<F8>(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
 #pragma unroll
