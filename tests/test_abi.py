@@ -134,6 +134,37 @@ def test_dtype_validation(lib):
     assert f(FAKE_A, FAKE_B, FAKE_O, D.BF16, D.F16, 0, 8, 8, 8, 8, 8, 1, 64, 64, 64, 0, None) == 0
 
 
+def test_packed_validation(lib):
+    """6- and 4-bit inputs: K-major only, whole-byte pitches and batch strides
+    (fp4: even; fp6: multiples of 4 elements), and the overlap check counts
+    their packed extent; all decided on the host."""
+    f = lib.gemm_nt_batched_major
+    D, Mj = gnt.DType, gnt.Major
+    M, N, K = 8, 8, 256
+    for ab, g in ((D.E2M1, 2), (D.E2M3, 4), (D.E3M2, 4)):
+        ok = (FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_O, ab, D.F32, M, N, K, K, K, N, 1, 0, 0, 0, 0, None)
+        assert f(*ok) not in (gnt.Status.INVALID_VALUE, gnt.Status.OVERLAP)
+        # MN-major packed operands
+        assert f(FAKE_A, Mj.MN, FAKE_B, Mj.K, FAKE_O, ab, D.F32, M, N, K, M + 8, K, N, 1, 0, 0, 0, 0,
+                 None) == gnt.Status.INVALID_VALUE
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.MN, FAKE_O, ab, D.F32, M, N, K, K, N + 8, N, 1, 0, 0, 0, 0,
+                 None) == gnt.Status.INVALID_VALUE
+        # a pitch that starts rows inside a byte (or a packing group)
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_O, ab, D.F32, M, N, K, K + g - 1, K, N, 1, 0, 0, 0, 0,
+                 None) == gnt.Status.INVALID_VALUE
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_O, ab, D.F32, M, N, K, K, K + g - 1, N, 1, 0, 0, 0, 0,
+                 None) == gnt.Status.INVALID_VALUE
+        # a batch stride that does
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_O, ab, D.F32, M, N, K, K, K, N, 2, M * K + g - 1, N * K,
+                 M * N, 0, None) == gnt.Status.INVALID_VALUE
+        # A holds M*K*w/8 bytes: Out starting there does not overlap, 8 bytes before it does
+        a_bytes = M * K * (4 if ab == D.E2M1 else 6) // 8
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_A + a_bytes, ab, D.F32, M, N, K, K, K, N, 1, 0, 0, 0, 0,
+                 None) != gnt.Status.OVERLAP
+        assert f(FAKE_A, Mj.K, FAKE_B, Mj.K, FAKE_A + a_bytes - 8, ab, D.F32, M, N, K, K, K, N, 1, 0, 0, 0, 0,
+                 None) == gnt.Status.OVERLAP
+
+
 def test_major_validation(lib):
     """gemm_nt_batched_major: an MN-major operand's pitch counts its stored rows'
     length (M or N), unknown majors are rejected, and the overlap check uses the
