@@ -116,7 +116,13 @@ gemm_status_t gemm_nt_f16_f32_batched(const void *A, const void *B, float *Out,
 /*
  * As gemm_nt_f16_f32_batched, on an explicitly chosen kernel.  Returns
  * GEMM_ERR_NOT_SUPPORTED (and launches nothing) if that kernel cannot take the
- * arguments, e.g. a tensor-core path with unaligned A.
+ * arguments, e.g. a tensor-core path with unaligned A.  GEMM_PATH_TC05_M64 and
+ * GEMM_PATH_TC05_WS ("Blackwell Tensor Cores" names the M = 64 and the
+ * weight-stationary tcgen05.mma forms beside its 128-row example) put 64 rows
+ * of A (32 on the weight-stationary form when M <= 32) on each tile's MMA
+ * side; they take the same inputs as GEMM_PATH_TC05 except block scales and
+ * an MN-major A (GEMM_ERR_NOT_SUPPORTED).  GEMM_PATH_AUTO never picks them.
+ * A path value outside gemm_path_t: GEMM_ERR_INVALID_VALUE.
  */
 gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *Out,
                                            int64_t M, int64_t N, int64_t K,
