@@ -1,5 +1,6 @@
 // tc05_kernel.cuh -- persistent, warp-specialised tcgen05 kernel for Out = A @ B.T
-// (fp16 inputs, fp32 accumulation in Tensor Memory, fp32 output).
+// (16-, 8-, 6- or 4-bit inputs, fp32 accumulation in Tensor Memory, fp32, fp16
+// or bf16 output).
 //
 // The single-CTA example of "Blackwell Tensor Cores" ("The Accumulator's
 // Lifetime") allocates TMEM with warp 0, stages A/B in 128-byte-swizzled shared
@@ -44,11 +45,10 @@ constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // inputs with block scales (kind::mxf8f6f4).  Block-scaled, the scale atoms
 // (512 bytes per 128 rows and 128 elements of K) come through a ring of two
 // scale stages of their own, each holding the atoms of kScaleKb consecutive
-// k-blocks of X and of Y -- contiguous in the packed layout, so one bulk copy
-// each; one 512-byte copy per operand and k-block beside the data loads held
-// the stream to half its rate.  TMEM holds, after the two accumulators, 8
-// columns of scales per data stage (X atom, then Y atom), which the MMA thread
-// fills with tcgen05.cp before the stage's MMAs.
+// k-blocks of X and of Y -- contiguous in the packed layout, so two bulk
+// copies per 8 k-blocks instead of two per k-block.  TMEM holds, after the two
+// accumulators, 8 columns of scales per data stage (X atom, then Y atom), which
+// the MMA thread fills with tcgen05.cp before the stage's MMAs.
 constexpr int kKind16 = 0, kKind8 = 1, kKindMx = 2;
 constexpr int kScaleKb = 8;      // k-blocks of scale atoms per scale stage
 constexpr int kScaleStages = 2;
