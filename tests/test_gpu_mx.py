@@ -179,3 +179,16 @@ def test_torch_wrapper_and_unsupported_paths():
     with pytest.raises(gnt.GemmError) as e:
         run_mx(A, SA, B, SB, "e4m3", "f32", P.AUTO)
     assert e.value.status == gnt.Status.NOT_SUPPORTED
+
+
+@pytest.mark.parametrize("ab", ["e4m3", "e2m1"])
+def test_skinny_workload_sampled(ab):
+    """The skinny workload (64 x 16384 x 8192) block-scaled, with its scales, as
+    the benchmark runs it (whole 128-row tiles of B on the swapped kernel);
+    sampled rows, columns and random elements."""
+    A, B = workloads.workload_inputs("skinny_64x16384x8192", ab)
+    SA, SB = workloads.workload_mx_scales("skinny_64x16384x8192")
+    got = run_mx(A[None], SA[None], B[None], SB[None], ab, "f32", P.AUTO)
+    bb, ii, jj = gpu_util.sample_indices(1, 64, 16384, 4096, rows=(0, 31, 32, -1), cols=(0, 127, 128, 8191, -1))
+    ref, absdot = oracle.gemm_nt_sampled_mx(A[None], SA[None], B[None], SB[None], bb, ii, jj, dtype=ab)
+    check_tol(got[bb, ii, jj], ref, absdot, "f32", "skinny workload mx %s" % ab)
