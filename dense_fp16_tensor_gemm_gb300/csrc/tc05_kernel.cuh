@@ -36,6 +36,8 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
+// block-scaled kernels add warp 10, which copies the scale atoms into TMEM
+constexpr int threads_of(int kind) { return kind == 2 ? kThreads + 32 : kThreads; }
 
 // XR: rows of X staged per stage.  128 normally; 112 for the row split of the
 // swapped path (shares of at most 112 rows), which packs 10 stages instead of
@@ -48,7 +50,9 @@ constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // k-blocks of X and of Y -- contiguous in the packed layout, so two bulk
 // copies per 8 k-blocks instead of two per k-block.  TMEM holds, after the two
 // accumulators, 8 columns of scales per data stage (X atom, then Y atom), which
-// the MMA thread fills with tcgen05.cp before the stage's MMAs.
+// warp 10 fills with tcgen05.cp once the stage's data has landed (which follows
+// the release of the stage's previous MMAs) and signals per data stage, so
+// the MMA thread issues nothing but MMAs.
 constexpr int kKind16 = 0, kKind8 = 1, kKindMx = 2;
 constexpr int kScaleKb = 8;      // k-blocks of scale atoms per scale stage
 constexpr int kScaleStages = 2;
@@ -78,7 +82,7 @@ struct Cfg {
     static constexpr int SC_STAGE_BYTES = 2 * kScaleKb * 512;
     static constexpr int SC_BYTES = KIND == kKindMx ? kScaleStages * SC_STAGE_BYTES : 0;
     static constexpr int EPI_BYTES = SWAP ? 0 : 8 * 32 * 32 * 4;  // per-warp 32x32 fp32 staging
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 384;
     static constexpr int BASE_STAGES =
         TM < 128 ? 8 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : (SWAP ? (XR <= 112 ? 10 : 9) : 8)));
     static constexpr int FIT_STAGES = (232448 - 1024 - SC_BYTES - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
@@ -93,7 +97,7 @@ struct Cfg {
                      : (TM == 64 || TM == 128), "instruction shapes");
     static_assert(ACC_COLS % 64 == 0, "each epilogue warp takes whole 32-column chunks");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert((2 * STAGES + 5 + 2 * kScaleStages) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert((3 * STAGES + 5 + 2 * kScaleStages + 1) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(X_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
     static_assert(TMEM_COLS <= 512, "Tensor Memory columns");
 };
@@ -101,7 +105,7 @@ struct Cfg {
 // 8-bit A and B (KIND 1, 2): a stage slot holds 128 elements of K in the same
 // 128 bytes per row.
 template <int BN, bool SWAP, int XR, int KIND, int TM = 128, bool WS = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(KIND), 1)
     tc05_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                      const TcParams p)
 {
@@ -127,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint64_t* sc_full = drain + 2;                 // MX: scale stage t has landed
     uint64_t* sc_empty = sc_full + kScaleStages;   // MX: the copies that read scale stage t are done
+    uint64_t* sf_ready = sc_empty + kScaleStages;  // MX: data stage s's scales are in TMEM
+    uint64_t* cdrain = sf_ready + STAGES;          // MX: the copier's last copies are done
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -144,6 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kScaleStages; ++t) {
             mbar_init(smem_u32(&sc_full[t]), 1);
             mbar_init(smem_u32(&sc_empty[t]), 1);
+        }
+        if (MX) {
+            for (int st = 0; st < STAGES; ++st)
+                mbar_init(smem_u32(&sf_ready[st]), 1);
+            mbar_init(smem_u32(cdrain), 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -279,15 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // additions (stage addresses, descriptor words) and the waits' fast path.
         if (lane == 0) {
             const uint32_t idesc = (MX ? idesc_mx(BM, BN) : C::IDESC) | p.idesc_bits;
-            const uint32_t sf_smem0 = smem_u32(sfs);
             const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
             const DescWords dx = desc_words(smem_u32(xs), p.x_mn != 0);
             const DescWords dy = desc_words(smem_u32(ys), p.y_mn != 0);
             uint32_t fa = full0, ea = empty0, xlo = dx.lo, ylo = dy.lo;
             int stage = 0;
             uint32_t phase = 0;
-            int sst = 0;  // MX: scale stage ring
-            uint32_t sphase = 0, sc_cur = 0;
             int local = 0;
             bool skip_release = p.fault == 2 && blockIdx.x == 0;  // test hook: lose one stage release
             bool ok = true;
@@ -313,34 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     if constexpr (MX) {
-                        if (kb == s.kb0 || kb % kScaleKb == 0) {
-                            if (!wait_bounded(smem_u32(&sc_full[sst]), sphase, abort_flag, p.wait_limit)) {
-                                raise_timeout(p, abort_flag);
-                                ok = false;
-                                break;
-                            }
-                            sc_cur = sf_smem0 + static_cast<uint32_t>(sst * C::SC_STAGE_BYTES);
+                        // the copier has put this stage's scales into its TMEM slot
+                        if (!wait_bounded(smem_u32(&sf_ready[stage]), phase, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
                         }
-                        // The scale slot of a data stage is refilled only after the
-                        // stage's previous MMAs completed (its release), and the
-                        // copy is ordered before the MMAs that follow it.
+                        tc_fence_after();
                         const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + 8 * stage);
-                        const uint32_t j = static_cast<uint32_t>(kb % kScaleKb);
-                        tc_cp_atom(sft, atom_desc(sc_cur + j * 512));
-                        tc_cp_atom(sft + 4, atom_desc(sc_cur + (kScaleKb + j) * 512));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             tc_mma_mx(d_tmem, xlo + k * dx.kstep, dx.hi, ylo + k * dy.kstep, dy.hi,
                                       idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4), sft,
                                       sft + 4 + y_sf_off, (k > 0 || kb != s.kb0) ? 1u : 0u);
-                        if (kb % kScaleKb == kScaleKb - 1 || kb == s.kb1 - 1) {
-                            // the scale stage's last copies: free it once they are done
-                            tc_commit(smem_u32(&sc_empty[sst]));
-                            if (++sst == kScaleStages) {
-                                sst = 0;
-                                sphase ^= 1;
-                            }
-                        }
                     } else if constexpr (WS) {
                         tc_mma_ws<F8>(d_tmem, xlo, dx.hi, ylo, dy.hi, idesc, kb != s.kb0);
 #pragma unroll
@@ -379,6 +372,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long t0 = clock64();
             while (!mbar_try_wait(smem_u32(drain), 0) &&
                    static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+            }
+        }
+    } else if (warp >= 10) {
+        // ------------------------------------------------------------ scale copier (block-scaled)
+        // Copies each data stage's two scale atoms from the scale ring into the
+        // stage's TMEM slot and signals sf_ready[stage] when the copies are done.
+        // A stage's data lands only after its previous MMAs released it, so
+        // waiting for the data also frees the slot.
+        if (MX && lane == 0) {
+            const uint32_t sf_smem0 = smem_u32(sfs);
+            int stage = 0, sst = 0;
+            uint32_t phase = 0, sphase = 0, sc_cur = 0;
+            bool issued = false, ok = true;
+            WorkIter<BN, TM> w(p);
+            Seg s;
+            while (ok && w.next(s)) {
+                for (int kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, p.wait_limit)) {
+                        raise_timeout(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    if (kb == s.kb0 || kb % kScaleKb == 0) {
+                        if (!wait_bounded(smem_u32(&sc_full[sst]), sphase, abort_flag, p.wait_limit)) {
+                            raise_timeout(p, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        sc_cur = sf_smem0 + static_cast<uint32_t>(sst * C::SC_STAGE_BYTES);
+                    }
+                    tc_fence_after();
+                    const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + 8 * stage);
+                    const uint32_t j = static_cast<uint32_t>(kb % kScaleKb);
+                    tc_cp_atom(sft, atom_desc(sc_cur + j * 512));
+                    tc_cp_atom(sft + 4, atom_desc(sc_cur + (kScaleKb + j) * 512));
+                    tc_commit(smem_u32(&sf_ready[stage]));
+                    issued = true;
+                    if (kb % kScaleKb == kScaleKb - 1 || kb == s.kb1 - 1) {
+                        // the scale stage's last copies: free it once they are done
+                        tc_commit(smem_u32(&sc_empty[sst]));
+                        if (++sst == kScaleStages) {
+                            sst = 0;
+                            sphase ^= 1;
+                        }
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (issued) {
+                // no copy may still be running when TMEM is released
+                tc_commit(smem_u32(cdrain));
+                const long long t0 = clock64();
+                while (!mbar_try_wait(smem_u32(cdrain), 0) &&
+                       static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                }
             }
         }
     } else {
@@ -443,7 +494,7 @@ cudaError_t launch_kind(const CUtensorMap& tmx, const CUtensorMap& tmy, const Tc
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_of(KIND), 1, 1);
     cfg.dynamicSmemBytes = Cfg<BN, SWAP, XR, KIND, TM, WS>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
