@@ -60,3 +60,50 @@ def test_bounded_wait_reports_timeout(path, M, N, K, fault):
     gnt.gemm_nt_check()
     ref, absdot = oracle.gemm_nt(A, B)
     assert_parity(out.cpu().numpy(), ref, absdot, what="after timeout " + path.name)
+
+
+@pytest.mark.parametrize("fault", [1, 2])
+@pytest.mark.parametrize("path,M,N,K", [(P.TC05, 256, 384, 2048), (P.TC05_PAIR, 512, 512, 2048),
+                                        (P.SKINNY, 64, 16384, 4096)])
+def test_bounded_wait_reports_timeout_block_scaled(path, M, N, K, fault):
+    """The block-scaled kernels, whose scale copies come from a copier warp
+    with waits of its own (on the stage data and the scale ring).  K is long
+    enough that every CTA reuses its stages, so a skipped release is waited on."""
+    from test_gpu_mx import draw, run_mx
+    A, SA, B, SB = draw(1, M, N, K, "e4m3", seed=7)
+    gnt.gemm_nt_check()
+    gnt.gemm_nt_debug_set_wait_limit(LIMIT)
+    gnt.gemm_nt_debug_set_fault(fault)
+    try:
+        with pytest.raises(gnt.GemmError) as e:
+            run_mx(A, SA, B, SB, "e4m3", "f32", path)  # run_mx checks the status
+        assert e.value.status == gnt.Status.DEVICE_TIMEOUT
+    finally:
+        gnt.gemm_nt_debug_set_fault(0)
+        gnt.gemm_nt_debug_set_wait_limit(0)
+    gnt.gemm_nt_check()
+    ref, absdot = oracle.gemm_nt_mx(A, SA, B, SB, dtype="e4m3")
+    from gpu_util import check_tol
+    check_tol(run_mx(A, SA, B, SB, "e4m3", "f32", path), ref, absdot, "f32", "after timeout mx " + path.name)
+
+
+@pytest.mark.parametrize("fault", [1, 2])
+@pytest.mark.parametrize("path", [P.TC05_M64, P.TC05_WS])
+def test_bounded_wait_reports_timeout_other_shapes(path, fault):
+    A, B = workloads.make_inputs(0, 64, 1024, 2048, "uniform", seed=5)
+    gnt.gemm_nt_check()
+    gnt.gemm_nt_debug_set_wait_limit(LIMIT)
+    gnt.gemm_nt_debug_set_fault(fault)
+    try:
+        _run(A, B, path)
+        with pytest.raises(gnt.GemmError) as e:
+            gnt.gemm_nt_check()
+        assert e.value.status == gnt.Status.DEVICE_TIMEOUT
+    finally:
+        gnt.gemm_nt_debug_set_fault(0)
+        gnt.gemm_nt_debug_set_wait_limit(0)
+    gnt.gemm_nt_check()
+    out = _run(A, B, path)
+    gnt.gemm_nt_check()
+    ref, absdot = oracle.gemm_nt(A, B)
+    assert_parity(out.cpu().numpy(), ref, absdot, what="after timeout " + path.name)
