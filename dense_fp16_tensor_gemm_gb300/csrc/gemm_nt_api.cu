@@ -635,8 +635,15 @@ bool pair_split(int64_t ntiles, int num_kb, int pairs, int out_type)
 
 int pair_plan_width(const Problem& q, const DeviceState& d)
 {
-    if (q.mx())
-        return 192;  // two 192-column accumulators leave TMEM room for the scale slots
+    if (q.mx()) {
+        // block-scaled: one 256-column accumulator with the direct epilogue
+        // (Out rows 32-byte aligned, no split), else two 192-column ones;
+        // either leaves TMEM room for the scale slots
+        const bool direct = aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) && q.ldo % 8 == 0 &&
+                            (q.batch == 1 || q.sO % 8 == 0);
+        const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);
+        return direct && !pair_split(tiles256, static_cast<int>(q.kblocks()), d.max_pairs, q.out_type) ? 256 : 192;
+    }
     if (q.b_mn())
         return 256;  // each CTA's half of B must be whole 64-row chunks
     const int64_t tiles256 = q.batch * ((q.M + 255) / 256) * ((q.N + 255) / 256);

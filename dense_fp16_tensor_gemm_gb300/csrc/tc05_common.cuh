@@ -345,5 +345,60 @@ __device__ __forceinline__ void epilogue_store_direct(const TcParams& p, const S
     }
 }
 
+// The direct epilogue in two halves, for a kernel with a single accumulator:
+// the warp first loads its whole share (NCH 32-column chunks from c_begin of
+// its lane quadrant, 16x256b as above) into registers, so the caller can free
+// the accumulator for the next tile's MMAs before any store is issued, then
+// stores from those registers with the same coverage and masking.
+template <int NCH>
+__device__ __forceinline__ void epilogue_load_direct(uint32_t tacc, int q, int c_begin, uint32_t (&v)[2 * NCH][16])
+{
+#pragma unroll
+    for (int ci = 0; ci < NCH; ++ci)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            tmem_ld16x256_x4_wait(tacc + (static_cast<uint32_t>(q * 32 + h * 16) << 16) +
+                                      static_cast<uint32_t>(c_begin + 32 * ci),
+                                  v[2 * ci + h]);
+}
+
+template <int OT, int NCH>
+__device__ __forceinline__ void epilogue_store_direct_regs(const TcParams& p, const Seg& s, int q, int c_begin,
+                                                           int lane, const uint32_t (&v)[2 * NCH][16])
+{
+    using S = OutStore<OT>;
+    typename S::T* obase = static_cast<typename S::T*>(p.out) + static_cast<int64_t>(s.b) * p.stride_o;
+    const int x_row0 = s.x0 + q * 32;
+    const int nx = s.xend - x_row0;
+    const int rsub = lane >> 2;
+    const int csub = 2 * (lane & 3);
+#pragma unroll
+    for (int ci = 0; ci < NCH; ++ci) {
+        const int c = c_begin + 32 * ci;
+        if (nx > 0 && s.y0 + c < p.rows_y) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int row = h * 16 + half * 8 + rsub;  // within the quadrant
+                    if (row < nx) {
+                        typename S::T* dst = obase + static_cast<int64_t>(x_row0 + row) * p.ldo + s.y0 + c + csub;
+                        const int ncol = p.rows_y - (s.y0 + c + csub);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float v0 = __uint_as_float(v[2 * ci + h][4 * j + 2 * half]);
+                            const float v1 = __uint_as_float(v[2 * ci + h][4 * j + 2 * half + 1]);
+                            if (ncol - 8 * j >= 2)
+                                S::st2(dst + 8 * j, v0, v1);
+                            else if (ncol - 8 * j == 1)
+                                S::st1(dst + 8 * j, v0);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 }  // namespace tc
 }  // namespace gnt

@@ -54,17 +54,22 @@ constexpr int kSfAtomsB = 2;
 constexpr int kScaleKb = 8;
 constexpr int kScaleStages = 2;
 
+// Block-scaled 256-wide tiles (SINGLE) keep one accumulator: two 256-column
+// ones would leave TMEM no room for the scale slots.  Their epilogue warps
+// load their whole share of it into registers and free it at once, then
+// store, so the next tile's MMAs wait only for the TMEM reads.
 template <int PBN, bool DIRECT, int KIND = 0>
 struct PairCfg {
     static constexpr bool MX = KIND == 2;
-    static constexpr int STAGES = DIRECT ? 7 : 6;
+    static constexpr bool SINGLE = MX && PBN == 256;
+    static constexpr int STAGES = SINGLE ? 6 : (DIRECT ? 7 : 6);
     static constexpr int B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
     static constexpr int DATA_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SC_STAGE_BYTES = (1 + kSfAtomsB) * kScaleKb * 512;  // one scale stage
     static constexpr int SC_BYTES = MX ? kScaleStages * SC_STAGE_BYTES : 0;
     static constexpr int ACC_STRIDE = MX ? PBN : 256;
-    static constexpr int SF_COL = 2 * PBN;
+    static constexpr int SF_COL = SINGLE ? PBN : 2 * PBN;
     static constexpr int SF_COLS = 16;
     static constexpr int EPI_BYTES = DIRECT ? 0 : 8 * 32 * 32 * 4;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SC_BYTES + EPI_BYTES + BAR_BYTES;
@@ -76,7 +81,8 @@ struct PairCfg {
     static_assert((3 * STAGES + 6 + 2 * kScaleStages) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(B_BYTES % 1024 == 0, "stage slots keep the 1024-byte swizzle alignment");
     static_assert(!MX || SF_COL + SF_COLS * STAGES <= TMEM_COLS, "scale slots fit in TMEM");
-    static_assert(!MX || PBN == 192, "block-scaled tiles are 192 wide (two B atoms per stage)");
+    static_assert(!MX || PBN == 192 || (PBN == 256 && DIRECT),
+                  "block-scaled tiles: 192 wide, or 256 wide with the direct epilogue (two B atoms per stage)");
 };
 
 // Pair tiles (256 rows x PBN columns): tiles [0, sk_first) whole and round-robin
@@ -439,8 +445,8 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
             PairIter<PBN> w(p, 0);
             Seg s;
             while (ok && w.next(s)) {
-                const int buf = local & 1;
-                const uint32_t use = static_cast<uint32_t>(local >> 1);
+                const int buf = C::SINGLE ? 0 : (local & 1);
+                const uint32_t use = static_cast<uint32_t>(C::SINGLE ? local : (local >> 1));
                 if (!wait_bounded(smem_u32(&tempty[buf]), (use & 1) ^ 1, abort_flag, p.wait_limit)) {
                     raise_timeout(p, abort_flag);
                     break;
@@ -580,8 +586,8 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
         PairIter<PBN> w(p, static_cast<int>(rank));
         Seg s;
         while (w.next(s)) {
-            const int buf = local & 1;
-            const uint32_t use = static_cast<uint32_t>(local >> 1);
+            const int buf = C::SINGLE ? 0 : (local & 1);
+            const uint32_t use = static_cast<uint32_t>(C::SINGLE ? local : (local >> 1));
             if (!wait_bounded(smem_u32(&tfull[buf]), use & 1, abort_flag, p.wait_limit)) {
                 raise_timeout(p, abort_flag);
                 break;
@@ -589,7 +595,21 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
             tc_fence_after();
             const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[buf]), 0);
             const uint32_t tacc = tmem_base + static_cast<uint32_t>(buf * kAccStride);
-            if (!DIRECT && s.partial) {
+            if constexpr (C::SINGLE) {
+                // the warp's 128 columns into registers, the accumulator freed, then the stores
+                uint32_t v[2 * (PBN / 2 / 32)][16];
+                epilogue_load_direct<PBN / 2 / 32>(tacc, q, c_begin, v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(tempty_leader);
+                if (p.out_type == kOutF16)
+                    epilogue_store_direct_regs<kOutF16, PBN / 2 / 32>(p, s, q, c_begin, lane, v);
+                else if (p.out_type == kOutBF16)
+                    epilogue_store_direct_regs<kOutBF16, PBN / 2 / 32>(p, s, q, c_begin, lane, v);
+                else
+                    epilogue_store_direct_regs<kOutF32, PBN / 2 / 32>(p, s, q, c_begin, lane, v);
+            } else if (!DIRECT && s.partial) {
                 // the host splits only products with fp32 Out
                 sk_epilogue<kOutF32>(p, s, tacc, q, ew, c_begin, c_end, lane, static_cast<int>(rank), stage_buf,
                                      tempty_leader);
@@ -702,6 +722,7 @@ cudaError_t tc05_pair_configure(int* max_pairs)
     if (e == cudaSuccess) e = configure_one<224, true>(&n);
     if (e == cudaSuccess) e = configure_one<192, true>(&n);
     if (e == cudaSuccess) e = configure_kind<192, true, 2>(&n);
+    if (e == cudaSuccess) e = configure_kind<256, true, 2>(&n);
     if (e == cudaSuccess) e = configure_kind<192, false, 2>(&n);
     if (e != cudaSuccess)
         return e;
@@ -714,9 +735,12 @@ cudaError_t tc05_pair_launch(const CUtensorMap& tma, const CUtensorMap& tmb, con
                              const CUtensorMap* tmsb)
 {
     if (kind == 2) {
-        // block-scaled: 192-wide tiles leave TMEM room for the scale slots
-        if (pbn != 192 || !tmsa || !tmsb)
+        // block-scaled: two 192-wide accumulators, or one 256-wide (direct
+        // epilogue only), leave TMEM room for the scale slots
+        if ((pbn != 192 && pbn != 256) || (pbn == 256 && !direct) || !tmsa || !tmsb)
             return cudaErrorInvalidValue;
+        if (pbn == 256)
+            return launch_kind<256, true, 2>(tma, tmb, *tmsa, *tmsb, p, pairs, stream);
         if (direct)
             return launch_kind<192, true, 2>(tma, tmb, *tmsa, *tmsb, p, pairs, stream);
         return launch_kind<192, false, 2>(tma, tmb, *tmsa, *tmsb, p, pairs, stream);
