@@ -235,8 +235,9 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
  * the plain one.
  *
  * path: GEMM_PATH_AUTO, GEMM_PATH_TC05 (128 x 64 or 128 x 128 tiles),
- * GEMM_PATH_SKINNY (M <= 64) or GEMM_PATH_TC05_PAIR (256 x 192 tiles on CTA
- * pairs); AUTO takes SKINNY for M <= 64 and N >= 1024, the pairs for M and N
+ * GEMM_PATH_SKINNY (M <= 64) or GEMM_PATH_TC05_PAIR (256 x 256 tiles on CTA
+ * pairs when Out rows are 32-byte aligned and K is not split, else 256 x 192);
+ * AUTO takes SKINNY for M <= 64 and N >= 1024, the pairs for M and N
  * above 128, else TC05.  The warp kernel takes no scales
  * (GEMM_ERR_NOT_SUPPORTED), nor does any kernel a layout the tensor-core
  * kernels cannot read (unaligned bases, pitches not multiples of 16 bytes).  Null SA / SB with K > 0, a 16-bit ab_type, or
