@@ -28,12 +28,6 @@ def _inputs(batch, M, N, K, ab, dist="normal", seed=0, sigma=1.0):
     return workloads.make_inputs(batch, M, N, K, dist, sigma, seed=seed, dtype=ab)
 
 
-def test_packing_rule():
-    """The packed storage of a few codes, worked out by hand from the bit order."""
-    assert workloads.pack_subbyte(np.array([[1, 2, 3, 4]], np.uint8), "e2m3").tolist() == [[0x81, 0x30, 0x10]]
-    assert workloads.pack_subbyte(np.array([[1, 2, 15, 7]], np.uint8), "e2m1").tolist() == [[0x21, 0x7F]]
-
-
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 @pytest.mark.parametrize("ab", F6F4)
 @pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR], ids=lambda p: p.name)

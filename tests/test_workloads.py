@@ -1,4 +1,5 @@
 """Seeded input generators (no GPU)."""
+import pytest
 import numpy as np
 
 import workloads
@@ -76,3 +77,53 @@ def test_f8_inputs_follow_the_same_draws():
         x, _ = workloads.make_inputs(0, 64, 8, 256, "normal", 1.0, seed=5, dtype=dtype)
         v = torch.from_numpy(x.copy()).view(tt).to(torch.float64).numpy()
         assert np.isfinite(v).all() and abs(float(v.std()) - 1.0) < 0.1
+
+
+def _unpack_bits(packed, bits, K):
+    """Independent reading of the packed rows: the row as one little-endian
+    bit string (numpy's unpackbits, bit order little), element k = bits
+    [bits*k, bits*k + bits)."""
+    flat = np.unpackbits(np.asarray(packed, dtype=np.uint8), axis=-1, bitorder="little")
+    flat = flat[..., : bits * K].reshape(packed.shape[:-1] + (K, bits))
+    return (flat * (1 << np.arange(bits))).sum(axis=-1).astype(np.uint8)
+
+
+def test_subbyte_packing_rule_and_round_trip():
+    """pack_subbyte: hand-worked bytes, and every code at every position read
+    back through an independent bit-string decoding."""
+    assert workloads.pack_subbyte(np.array([[1, 2, 3, 4]], np.uint8), "e2m3").tolist() == [[0x81, 0x30, 0x10]]
+    assert workloads.pack_subbyte(np.array([[1, 2, 15, 7]], np.uint8), "e2m1").tolist() == [[0x21, 0x7F]]
+    rng = np.random.default_rng(0)
+    for dtype, bits in (("e2m1", 4), ("e2m3", 6), ("e3m2", 6)):
+        codes = rng.integers(0, 1 << bits, size=(3, 5, 64)).astype(np.uint8)
+        packed = workloads.pack_subbyte(codes, dtype)
+        assert packed.shape == (3, 5, 64 * bits // 8)
+        assert np.array_equal(_unpack_bits(packed, bits, 64), codes)
+    with pytest.raises(ValueError):
+        workloads.pack_subbyte(np.zeros((2, 3), np.uint8), "e2m1")
+    with pytest.raises(ValueError):
+        workloads.pack_subbyte(np.zeros((2, 6), np.uint8), "e3m2")
+
+
+def test_subbyte_draws_are_codes_of_the_format():
+    """The 6- and 4-bit draws: codes within the format's width, the sign bit
+    set exactly for negative draws (a zero code may carry either sign), and
+    every magnitude code reachable for normal(0,1) over enough draws."""
+    for dtype, bits in (("e2m1", 4), ("e2m3", 6), ("e3m2", 6)):
+        A, B = workloads.make_inputs(0, 64, 64, 256, "normal", 1.0, seed=11, dtype=dtype)
+        assert A.dtype == np.uint8 and int(A.max()) < (1 << bits)
+        mags = np.unique(np.concatenate([A.ravel(), B.ravel()]) & ((1 << (bits - 1)) - 1))
+        assert len(mags) >= (1 << (bits - 1)) // 2
+    # integers 0..4 are exact in E2M1: magnitude codes 0, 2, 4, 5, 6 (0, 1, 2, 3, 4)
+    I, _ = workloads.make_inputs(0, 8, 8, 128, "int4", seed=1, dtype="e2m1")
+    assert set(np.unique(I & 7).tolist()) == {0, 2, 4, 5, 6}
+
+
+def test_mx_scale_recipe():
+    sa, sb = workloads.workload_mx_scales("square_4096")
+    assert sa.shape == (4096, 128) and sb.shape == (4096, 128)
+    assert sa.min() >= 120 and sa.max() <= 134
+    sa2, _ = workloads.workload_mx_scales("square_4096")
+    assert np.array_equal(sa, sa2)
+    sr, _ = workloads.workload_mx_scales("ragged_batch16_3001x2047x1000")
+    assert sr.shape == (16, 3001, 32)
