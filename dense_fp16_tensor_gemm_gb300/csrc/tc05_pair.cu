@@ -40,16 +40,17 @@ constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CT
 // number of rounds over the pairs.  DIRECT: the epilogue stores straight from
 // TMEM-loaded registers (Out rows 32-byte aligned), which frees the 32 KB of
 // staging for a seventh pipeline stage.
-// KIND: 0 16-bit inputs, 1 8-bit, 2 8-bit block-scaled (PBN = 192 only).
-// Block-scaled, each CTA needs the scale atoms of its 128 rows of A and those
-// of all of the tile's B rows (each half of the pair MMA reads B's scales from
-// its own CTA's TMEM; a 192-row window starts 0 or 64 rows into a 128-row block
-// and so spans exactly two atoms).  They come through a ring of two scale
-// stages, each holding the atoms of kScaleKb consecutive k-blocks (A: 4 KB in
-// one box, B: 8 KB in one box): small per-k-block scale loads beside the data
-// loads slowed the stream down by a third.  TMEM holds the accumulators PBN
-// columns apart and, from column 2*PBN, 16 scale columns per data stage (A
-// atom, then the B atoms), filled by tcgen05.cp before the stage's MMAs.
+// KIND: 0 16-bit inputs, 1 8-bit, 2 8-bit block-scaled (PBN = 192, or 256
+// with a single accumulator).  Block-scaled, each CTA needs the scale atoms of
+// its 128 rows of A and those of all of the tile's B rows (each half of the
+// pair MMA reads B's scales from its own CTA's TMEM; a 192-row window starts 0
+// or 64 rows into a 128-row block, a 256-row one on a block, and either spans
+// exactly two atoms).  They come through a ring of two scale stages, each
+// holding the atoms of kScaleKb consecutive k-blocks (A: 4 KB in one box, B:
+// 8 KB in one box): small per-k-block scale loads beside the data loads slowed
+// the stream down by a third.  TMEM holds the accumulators PBN columns apart
+// (one at 256 wide) and, after them, 16 scale columns per data stage (A atom,
+// then the B atoms), filled by tcgen05.cp before the stage's MMAs.
 constexpr int kSfAtomsB = 2;
 constexpr int kScaleKb = 8;
 constexpr int kScaleStages = 2;
