@@ -139,9 +139,9 @@ def test_long_k_few_tiles(path):
 
 @pytest.mark.parametrize("M,N,K", [(256, 192, 128), (640, 1000, 384), (1000, 576, 256), (130, 1300, 640)])
 def test_pair_tile_windows(M, N, K):
-    """256 x 192 pair tiles whose B rows start at every offset within a
-    128-row scale atom (0, 64; 192 = 64 mod 128) and span two or three atoms,
-    ragged M and N."""
+    """Pair tiles over ragged M and N: Out rows 32-byte aligned (N a multiple
+    of 8) run 256 x 256 tiles with one accumulator, N = 1300 the 256 x 192
+    tiles, whose B rows start 0 or 64 rows into a 128-row scale atom."""
     A, SA, B, SB = draw(1, M, N, K, "e5m2", seed=M + N + K)
     ref, absdot = oracle.gemm_nt_mx(A, SA, B, SB, dtype="e5m2")
     check_tol(run_mx(A, SA, B, SB, "e5m2", "f32", P.TC05_PAIR), ref, absdot, "f32", "pair %dx%dx%d" % (M, N, K))
@@ -192,3 +192,28 @@ def test_skinny_workload_sampled(ab):
     bb, ii, jj = gpu_util.sample_indices(1, 64, 16384, 4096, rows=(0, 31, 32, -1), cols=(0, 127, 128, 8191, -1))
     ref, absdot = oracle.gemm_nt_sampled_mx(A[None], SA[None], B[None], SB[None], bb, ii, jj, dtype=ab)
     check_tol(got[bb, ii, jj], ref, absdot, "f32", "skinny workload mx %s" % ab)
+
+
+@pytest.mark.parametrize("M,N,K", [(640, 1000, 384), (300, 2000, 1152)])
+@pytest.mark.parametrize("pad", [0, 1], ids=["aligned_out", "unaligned_out"])
+def test_pair_both_tile_widths(M, N, K, pad):
+    """The same product with an Out pitch of N (rows 32-byte aligned: 256-wide
+    tiles, one accumulator, epilogue from registers) and N + 1 (192-wide
+    tiles, two accumulators, staged epilogue); columns past N untouched."""
+    import torch
+    A, SA, B, SB = draw(1, M, N, K, "e4m3", seed=M + K)
+    ref, absdot = oracle.gemm_nt_mx(A, SA, B, SB, dtype="e4m3")
+    a, pa = gpu_util.to_device(A, "e4m3", K)
+    b, pb = gpu_util.to_device(B, "e4m3")
+    sa = gnt.pack_mx_scales(torch.from_numpy(SA).cuda(), K)
+    sb = gnt.pack_mx_scales(torch.from_numpy(SB).cuda(), K)
+    ldo = N + pad
+    o = torch.full((M, ldo), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    gnt.gemm_nt_mx(pa, sa.data_ptr(), pb, sb.data_ptr(), o.data_ptr(), gnt.DType.E4M3, gnt.DType.F32, M, N, K,
+                   K, K, ldo, 1, 0, 0, 0, P.TC05_PAIR, stream)
+    gnt.gemm_nt_check(stream)
+    got = o.double().cpu().numpy()
+    if pad:
+        assert np.isnan(got[:, N:]).all()
+    check_tol(got[None, :, :N], ref, absdot, "f32", "pair ldo=%d" % ldo)
