@@ -396,18 +396,18 @@ def main():
         a, b, out, sa_packed, sb_packed = sets[i]
         if args.mx:
             gnt.gemm_nt_mx(a.data_ptr(), sa_packed.data_ptr(), b.data_ptr(), sb_packed.data_ptr(), out.data_ptr(),
-                           codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB,
-                           sO, path, sh)
+                           codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, sA, sB,
+                           sO, nb, path, sh)
         elif not default_layout:
             gnt.gemm_nt_batched_major(a.data_ptr(), majors[args.a_major], b.data_ptr(), majors[args.b_major],
                                       out.data_ptr(), codes[args.ab_dtype], codes[args.out_dtype], w.M, w.N, w.K,
-                                      lda, ldb, w.N, nb, sA, sB, sO, path, sh)
+                                      lda, ldb, w.N, sA, sB, sO, nb, path, sh)
         elif default_types:
             gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M, w.N, w.K,
-                                             w.K, w.K, w.N, nb, sA, sB, sO, path, sh)
+                                             w.K, w.K, w.N, sA, sB, sO, nb, path, sh)
         else:
             gnt.gemm_nt_batched_ex(a.data_ptr(), b.data_ptr(), out.data_ptr(), codes[args.ab_dtype],
-                                   codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, nb, sA, sB, sO,
+                                   codes[args.out_dtype], w.M, w.N, w.K, w.K, w.K, w.N, sA, sB, sO, nb,
                                    path, sh)
 
     scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None

@@ -18,12 +18,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libgemm_nt.so")
 class Status(enum.IntEnum):
     OK = 0
     INVALID_VALUE = 1
-    OVERLAP = 2
-    UNSUPPORTED_DEVICE = 3
-    CUDA = 4
+    MISALIGNED = 2          # reserved: never returned
+    OVERLAP = 3
+    LAUNCH = 4
     DEVICE_TIMEOUT = 5
-    NOT_SUPPORTED = 6
-    SCRATCH_TOO_SMALL = 7
+    UNSUPPORTED_DEVICE = 6
+    NOT_SUPPORTED = 7
+    SCRATCH_TOO_SMALL = 8
 
 
 class DType(enum.IntEnum):
@@ -55,7 +56,7 @@ class Path(enum.IntEnum):
 class GemmError(RuntimeError):
     def __init__(self, status):
         self.status = Status(status)
-        super().__init__("libgemm_nt: %s (%s)" % (status_string(status), self.status.name))
+        super().__init__("libgemm_nt: %s (%s)" % (error_string(status), self.status.name))
 
 
 # name -> (restype, argtypes); mirrors include/gemm_nt.h
@@ -75,7 +76,7 @@ _SIGNATURES = {
     "gemm_nt_mx_pack_scales": (ctypes.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _i64, _vp]),
     "gemm_nt_select_path": (ctypes.c_int, [_vp, _vp, _vp] + [_i64] * 10),
     "gemm_nt_check": (ctypes.c_int, [_vp]),
-    "gemm_nt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_nt_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_nt_probe_m16n8k16": (ctypes.c_int, [_vp] * 6),
     "gemm_nt_debug_set_wait_limit": (None, [_u64]),
     "gemm_nt_debug_set_fault": (None, [ctypes.c_int]),
@@ -106,8 +107,8 @@ def _check(status):
         raise GemmError(status)
 
 
-def status_string(status):
-    return load().gemm_nt_status_string(int(status)).decode()
+def error_string(status):
+    return load().gemm_nt_error_string(int(status)).decode()
 
 
 # ---------------------------------------------------------------- C-ABI mirror
@@ -115,36 +116,36 @@ def gemm_nt_f16_f32(A, B, Out, M, N, K, lda, ldb, ldo, stream=0):
     _check(load().gemm_nt_f16_f32(A, B, Out, M, N, K, lda, ldb, ldo, stream))
 
 
-def gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO,
+def gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB, strideO, batch,
                             stream=0):
-    _check(load().gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
-                                          strideB, strideO, stream))
+    _check(load().gemm_nt_f16_f32_batched(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB,
+                                          strideO, batch, stream))
 
 
-def gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
-                                 strideO, path, stream=0):
-    _check(load().gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
-                                               strideB, strideO, int(path), stream))
+def gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB, strideO,
+                                 batch, path, stream=0):
+    _check(load().gemm_nt_f16_f32_batched_path(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB,
+                                               strideO, batch, int(path), stream))
 
 
-def gemm_nt_batched_ex(A, B, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
-                       strideO, path=0, stream=0):
+def gemm_nt_batched_ex(A, B, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, strideA, strideB, strideO,
+                       batch, path=0, stream=0):
     _check(load().gemm_nt_batched_ex(A, B, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo,
-                                     batch, strideA, strideB, strideO, int(path), stream))
+                                     strideA, strideB, strideO, batch, int(path), stream))
 
 
-def gemm_nt_batched_major(A, a_major, B, b_major, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch,
-                          strideA, strideB, strideO, path=0, stream=0):
+def gemm_nt_batched_major(A, a_major, B, b_major, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, strideA,
+                          strideB, strideO, batch, path=0, stream=0):
     _check(load().gemm_nt_batched_major(A, int(a_major), B, int(b_major), Out, int(ab_type), int(out_type), M, N,
-                                        K, lda, ldb, ldo, batch, strideA, strideB, strideO, int(path), stream))
+                                        K, lda, ldb, ldo, strideA, strideB, strideO, batch, int(path), stream))
 
 
-def gemm_nt_mx(A, SA, B, SB, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO,
+def gemm_nt_mx(A, SA, B, SB, Out, ab_type, out_type, M, N, K, lda, ldb, ldo, strideA, strideB, strideO, batch,
                path=0, stream=0):
     """Block-scaled 8-bit product; SA / SB in the packed atom layout (see
     include/gemm_nt.h)."""
-    _check(load().gemm_nt_mx(A, SA, B, SB, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo, batch,
-                             strideA, strideB, strideO, int(path), stream))
+    _check(load().gemm_nt_mx(A, SA, B, SB, Out, int(ab_type), int(out_type), M, N, K, lda, ldb, ldo, strideA,
+                             strideB, strideO, batch, int(path), stream))
 
 
 def gemm_nt_mx_scale_bytes(rows, K):
@@ -155,12 +156,12 @@ def gemm_nt_mx_pack_scales(plain, ld, stride, packed, rows, K, batch=1, stream=0
     _check(load().gemm_nt_mx_pack_scales(plain, ld, stride, packed, rows, K, batch, stream))
 
 
-def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB,
-                                     strideO, stream=0):
+def gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB, strideO,
+                                     batch, stream=0):
     """The batched product without any device allocation (fixed scratch array
     inside the library; see include/gemm_nt.h)."""
-    _check(load().gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
-                                                   strideB, strideO, stream))
+    _check(load().gemm_nt_f16_f32_batched_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB,
+                                                   strideO, batch, stream))
 
 
 def gemm_nt_f16_f32_from_host(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, batch, stream=0):
@@ -168,9 +169,9 @@ def gemm_nt_f16_f32_from_host(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, b
                                             stream))
 
 
-def gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, batch=1, strideA=0, strideB=0, strideO=0):
-    return Path(load().gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA,
-                                           strideB, strideO))
+def gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, strideA=0, strideB=0, strideO=0, batch=1):
+    return Path(load().gemm_nt_select_path(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB,
+                                           strideO, batch))
 
 
 def gemm_nt_check(stream=0):
@@ -237,7 +238,7 @@ def gemm_nt(A, B, out=None, path=Path.AUTO, stream=None, out_dtype=None):
         raise ValueError("out must have shape (M,N)")
     gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
                        _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
-                       1, 0, 0, 0, path, _stream_handle(stream))
+                       0, 0, 0, 1, path, _stream_handle(stream))
     return out
 
 
@@ -278,7 +279,7 @@ def gemm_nt_mx_tensors(A, SA, B, SB, out=None, path=Path.AUTO, stream=None, out_
     if tuple(out.shape) != (M, N):
         raise ValueError("out must have shape (M,N)")
     gemm_nt_mx(A.data_ptr(), pa.data_ptr(), B.data_ptr(), pb.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
-               _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"), 1, 0, 0, 0, path,
+               _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"), 0, 0, 0, 1, path,
                _stream_handle(stream))
     return out
 
@@ -320,11 +321,11 @@ def gemm_nt_packed(A, B, K, ab_dtype, SA=None, SB=None, out=None, path=Path.AUTO
     lda, ldb = pa_bytes * 8 // bits, pb_bytes * 8 // bits
     if SA is None:
         gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ocodes[dt], M, N, K, lda, ldb,
-                           _matrix_ld(out, "out"), 1, 0, 0, 0, path, _stream_handle(stream))
+                           _matrix_ld(out, "out"), 0, 0, 0, 1, path, _stream_handle(stream))
     else:
         pa, pb = pack_mx_scales(SA, K, stream), pack_mx_scales(SB, K, stream)
         gemm_nt_mx(A.data_ptr(), pa.data_ptr(), B.data_ptr(), pb.data_ptr(), out.data_ptr(), ab, ocodes[dt], M, N,
-                   K, lda, ldb, _matrix_ld(out, "out"), 1, 0, 0, 0, path, _stream_handle(stream))
+                   K, lda, ldb, _matrix_ld(out, "out"), 0, 0, 0, 1, path, _stream_handle(stream))
     return out
 
 
@@ -344,5 +345,5 @@ def gemm_nt_batched(A, B, out=None, path=Path.AUTO, stream=None, out_dtype=None)
         raise ValueError("out must have shape (batch,M,N)")
     gemm_nt_batched_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), ab, ot, M, N, K,
                        _matrix_ld(A, "A"), _matrix_ld(B, "B"), _matrix_ld(out, "out"),
-                       batch, A.stride(0), B.stride(0), out.stride(0), path, _stream_handle(stream))
+                       A.stride(0), B.stride(0), out.stride(0), batch, path, _stream_handle(stream))
     return out

@@ -73,7 +73,7 @@ gemm_status_t device_state(DeviceState** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     DeviceState& d = g_dev[dev];
     std::call_once(d.once, [&d, dev] {
         int major = 0, minor = 0;
@@ -100,7 +100,7 @@ gemm_status_t device_state(DeviceState** out)
         d.init_err = e;
     });
     if (d.init_err != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     if (!d.supported)
         return GEMM_ERR_UNSUPPORTED_DEVICE;
     *out = &d;
@@ -121,20 +121,20 @@ gemm_status_t stream_workspace(cudaStream_t stream, size_t bytes, void** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     std::lock_guard<std::mutex> lock(g_ws_mu);
     Workspace& w = g_ws[std::make_pair(dev, stream)];
     if (w.bytes < bytes) {
         if (w.ptr) {
             if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(w.ptr) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
             w.ptr = nullptr;
             w.bytes = 0;
         }
         if (cudaMalloc(&w.ptr, bytes) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         if (cudaMemset(w.ptr, 0, bytes) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         w.bytes = bytes;
     }
     *out = w.ptr;
@@ -474,13 +474,13 @@ gemm_status_t zero_out(const Problem& q, cudaStream_t stream)
     if (q.sO == q.M * q.ldo || q.batch == 1) {
         const int64_t rows = q.batch == 1 ? q.M : q.M * q.batch;
         if (cudaMemset2DAsync(q.Out, q.ldo * q.out_esize(), 0, q.N * q.out_esize(), rows, stream) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         return GEMM_OK;
     }
     for (int64_t b = 0; b < q.batch; ++b)
         if (cudaMemset2DAsync(static_cast<uint8_t*>(q.Out) + b * q.sO * q.out_esize(), q.ldo * q.out_esize(), 0,
                               q.N * q.out_esize(), q.M, stream) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
@@ -536,7 +536,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     CUtensorMap tmx, tmy;
     if (!make_map(&tmx, xp, xrows, q.K, xld, q.batch, xs, xbox, &p.x_bmul, q.ab_type, x_mn) ||
         !make_map(&tmy, yp, yrows, q.K, yld, q.batch, ys, bn, &p.y_bmul, q.ab_type, y_mn))
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     p.out = q.Out;
     p.out_type = q.kernel_out();
     p.x_mn = x_mn ? 1 : 0;
@@ -599,7 +599,7 @@ gemm_status_t run_tc05(const Problem& q, const DeviceState& d, bool swap, cudaSt
     const cudaError_t le = tm < 128 ? tc05_small_launch(tmx, tmy, p, bn, tm, ws, grid, q.kind(), stream)
                                     : tc05_launch(tmx, tmy, p, bn, swap, grid, q.kind(), stream);
     if (le != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
@@ -653,8 +653,11 @@ int pair_plan_width(const Problem& q, const DeviceState& d)
 }
 
 // CTA pairs: 256 x PBN tiles; each CTA loads its 128 rows of A and PBN/2 of
-// the tile's PBN rows of B.
-gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t stream)
+// the tile's PBN rows of B.  A split (stream-K) launch takes its scratch from
+// `fixed` when given (memory the caller owns; nothing is allocated), else from
+// the per-stream workspace.
+gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t stream,
+                            const PairScratch* fixed = nullptr)
 {
     if (d.max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
@@ -666,7 +669,7 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
                   q.a_mn()) ||
         !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type,
                   q.b_mn()))
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     p.out = q.Out;
     p.out_type = q.kernel_out();
     p.x_mn = q.a_mn() ? 1 : 0;
@@ -711,16 +714,29 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
     p.sk_iters = 0;
     p.sk_pairs = 0;
     if (rem != 0) {
-        void* ws = nullptr;
-        gemm_status_t st = stream_workspace(stream, pair_workspace_bytes(P), &ws);
-        if (st != GEMM_OK)
-            return st;
+        pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
+        if (fixed) {
+            // slices are indexed by the pair over every launched pair
+            if (pairs > fixed->slice_pairs || rem > fixed->counter_tiles)
+                return GEMM_ERR_SCRATCH_TOO_SMALL;
+            // the counters must start at zero; the slices are fully rewritten
+            if (cudaMemsetAsync(fixed->counters, 0, static_cast<size_t>(rem) * 2 * 8 * sizeof(uint32_t), stream) !=
+                cudaSuccess)
+                return GEMM_ERR_LAUNCH;
+            p.ws = fixed->slices;
+            p.ws_flags = fixed->counters;
+        } else {
+            void* ws = nullptr;
+            gemm_status_t st = stream_workspace(stream, pair_workspace_bytes(P), &ws);
+            if (st != GEMM_OK)
+                return st;
+            p.ws = static_cast<float*>(ws);
+            p.ws_flags =
+                reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(P) * 4 * kPairSliceBytes);
+        }
         p.sk_first = static_cast<int>(ntiles - rem);
         p.sk_iters = rem * p.num_kb;
         p.sk_pairs = static_cast<int>(sk_pairs);
-        p.ws = static_cast<float*>(ws);
-        p.ws_flags = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(P) * 4 * kPairSliceBytes);
-        pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
     }
     // Out rows 32-byte aligned: the epilogue stores without staging
     const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
@@ -736,15 +752,15 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
         p.sf_box_rb = static_cast<int>(std::min<int64_t>(2, (q.N + 127) / 128 * mats_b));
         if (!encode_scale_map(&tmsa, q.SA, q.M, q.K, q.sA == 0 ? 1 : q.batch, 1, p.sf_box_kg) ||
             !encode_scale_map(&tmsb, q.SB, q.N, q.K, mats_b, p.sf_box_rb, p.sf_box_kg))
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         p.sf_x_bstride = q.sA == 0 ? 0 : mx_scale_bytes(q.M, q.K);
         p.sf_y_bstride = q.sB == 0 ? 0 : mx_scale_bytes(q.N, q.K);
         if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream, &tmsa, &tmsb) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         return GEMM_OK;
     }
     if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
@@ -772,7 +788,7 @@ gemm_status_t run_mmasync(const Problem& q, cudaStream_t stream)
     p.vec_b = aligned(q.B, v8) && q.ldb % 8 == 0 && (q.batch == 1 || q.sB % 8 == 0);
     p.a_mn = q.a_mn() ? 1 : 0;
     p.b_mn = q.b_mn() ? 1 : 0;
-    return mmasync_launch(p, q.ab_type, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    return mmasync_launch(p, q.ab_type, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
 // The host link carries ~210 GB/s in and ~190 GB/s out (measured on GB300),
@@ -858,7 +874,7 @@ gemm_status_t from_host_blocks(const void* A_host, const void* B_host, float* Ou
     std::lock_guard<std::mutex> lock(d.pipe_mu);
     if (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(d.h2d, ev_start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(d.d2h, ev_start, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     const uint8_t* ha = static_cast<const uint8_t*>(A_host);
     const uint8_t* hb = static_cast<const uint8_t*>(B_host);
     const size_t row = static_cast<size_t>(K) * 2;
@@ -868,14 +884,14 @@ gemm_status_t from_host_blocks(const void* A_host, const void* B_host, float* Ou
             if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dA) + r0 * row, ha + r0 * row, rows * row,
                                 cudaMemcpyHostToDevice, d.h2d) != cudaSuccess ||
                 cudaEventRecord(ev_a[s], d.h2d) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
         }
         if (s < nb) {
             const int64_t r0 = s * pb, rows = std::min(pb, N - r0);
             if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dB) + r0 * row, hb + r0 * row, rows * row,
                                 cudaMemcpyHostToDevice, d.h2d) != cudaSuccess ||
                 cudaEventRecord(ev_b[s], d.h2d) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
         }
     }
     // blocks in the order their inputs complete: step s brings A_s and B_s
@@ -890,7 +906,7 @@ gemm_status_t from_host_blocks(const void* A_host, const void* B_host, float* Ou
             const int64_t r0 = i * pa, rows = std::min(pa, M - r0), c0 = j * pb, cols = std::min(pb, N - c0);
             if (cudaStreamWaitEvent(stream, ev_a[i], 0) != cudaSuccess ||
                 cudaStreamWaitEvent(stream, ev_b[j], 0) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
             const Problem q{dA + r0 * K, dB + c0 * K, dOut + r0 * N + c0, rows, cols, K, K, K, N, 1, 0, 0, 0};
             gemm_status_t st = run(q, GEMM_PATH_AUTO, stream);
             if (st != GEMM_OK)
@@ -898,12 +914,12 @@ gemm_status_t from_host_blocks(const void* A_host, const void* B_host, float* Ou
             if (cudaEventRecord(ev_o[k], stream) != cudaSuccess || cudaStreamWaitEvent(d.d2h, ev_o[k], 0) != cudaSuccess ||
                 cudaMemcpy2DAsync(Out_host + r0 * N + c0, N * sizeof(float), dOut + r0 * N + c0, N * sizeof(float),
                                   cols * sizeof(float), rows, cudaMemcpyDeviceToHost, d.d2h) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
             ++k;
         }
     }
     if (cudaEventRecord(ev_done, d.d2h) != cudaSuccess || cudaStreamWaitEvent(stream, ev_done, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
@@ -923,7 +939,7 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
         d->pipe_err = e;
     });
     if (d->pipe_err != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     if (batch == 1 && M >= 2048 && N >= 2048 && K > 0)
         return from_host_blocks(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, *d, stream);
     // chunks: [first, first + count) of batches, or of rows when batch == 1
@@ -945,29 +961,29 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
     cudaEvent_t* ev_out = d->ev + 2 + kPipeChunks;
     if (cudaEventRecord(ev_start, stream) != cudaSuccess || cudaStreamWaitEvent(d->h2d, ev_start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(d->d2h, ev_start, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     const size_t a_unit = static_cast<size_t>(by_rows ? K : M * K) * 2;  // bytes per row / per batch of A
     const size_t b_unit = static_cast<size_t>(N * K) * 2;                // bytes per batch of B
     const size_t o_unit = static_cast<size_t>(by_rows ? N : M * N) * 4;
     if (by_rows && K > 0 && cudaMemcpyAsync(dB, hb, b_unit, cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     for (int c = 0; c < nchunks; ++c) {
         const int64_t first = c * per, count = std::min(per, units - first);
         if (K > 0) {
             if (cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dA) + first * a_unit, ha + first * a_unit, count * a_unit,
                                 cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
             if (!by_rows && cudaMemcpyAsync(reinterpret_cast<uint8_t*>(dB) + first * b_unit, hb + first * b_unit,
                                             count * b_unit, cudaMemcpyHostToDevice, d->h2d) != cudaSuccess)
-                return GEMM_ERR_CUDA;
+                return GEMM_ERR_LAUNCH;
         }
         if (cudaEventRecord(ev_in[c], d->h2d) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
     }
     for (int c = 0; c < nchunks; ++c) {
         const int64_t first = c * per, count = std::min(per, units - first);
         if (cudaStreamWaitEvent(stream, ev_in[c], 0) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         Problem q = by_rows ? Problem{dA + first * K, dB, dOut + first * N, count, N, K, K, K, N, 1, 0, 0, 0}
                             : Problem{dA + first * M * K, dB + first * N * K, dOut + first * M * N, M, N, K, K, K, N,
                                       count, M * K, N * K, M * N};
@@ -977,20 +993,22 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
         if (cudaEventRecord(ev_out[c], stream) != cudaSuccess || cudaStreamWaitEvent(d->d2h, ev_out[c], 0) != cudaSuccess ||
             cudaMemcpyAsync(ho + first * o_unit, reinterpret_cast<uint8_t*>(dOut) + first * o_unit, count * o_unit,
                             cudaMemcpyDeviceToHost, d->d2h) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
     }
     if (cudaEventRecord(ev_done, d->d2h) != cudaSuccess || cudaStreamWaitEvent(stream, ev_done, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
 }  // namespace
 
-// The CTA-pair kernel with the split planned as in run_tc05_pair, but its
-// scratch taken from memory the caller of this function owns (no allocation).
+// The CTA-pair kernel with its split scratch taken from memory the caller of
+// this function owns (no allocation): arguments are checked before any CUDA
+// call, then `scratch` gives the current device's fixed scratch, and the work
+// is planned and launched by run_tc05_pair, as on the automatic path.
 int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
-                      float* slices, int slice_pairs, uint32_t* counters, int counter_tiles, cudaStream_t stream)
+                      int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB, int64_t strideO, int64_t batch,
+                      PairScratchFn scratch, cudaStream_t stream)
 {
     const Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
     gemm_status_t st = validate(q);
@@ -1002,73 +1020,15 @@ int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64
     st = device_state(&d);
     if (st != GEMM_OK)
         return st;
+    PairScratch fixed{};
+    st = static_cast<gemm_status_t>(scratch(&fixed));
+    if (st != GEMM_OK)
+        return st;
     if (q.K == 0)
         return zero_out(q, stream);
     if (!tma_ok(q) || d->max_pairs < 1)
         return GEMM_ERR_NOT_SUPPORTED;
-    TcParams p{};
-    p.ab_packed_bits = q.is_packed() ? q.ab_bits() : 0;
-    const int pbn = pair_plan_width(q, *d);
-    CUtensorMap tma, tmb;
-    if (!make_map(&tma, q.A, q.M, q.K, q.lda, q.batch, q.sA, 128, &p.x_bmul, q.ab_type) ||
-        !make_map(&tmb, q.B, q.N, q.K, q.ldb, q.batch, q.sB, pbn / 2, &p.y_bmul, q.ab_type))
-        return GEMM_ERR_CUDA;
-    p.out = q.Out;
-    p.out_type = q.kernel_out();
-    p.idesc_bits = q.ab_fmt();
-    p.ldo = q.ldo;
-    p.stride_o = q.sO;
-    p.rows_x = static_cast<int>(q.M);
-    p.rows_y = static_cast<int>(q.N);
-    p.batch = static_cast<int>(q.batch);
-    p.tiles_x = static_cast<int>((q.M + 255) / 256);
-    p.tiles_y = static_cast<int>((q.N + pbn - 1) / pbn);
-    p.num_kb = static_cast<int>(q.kblocks());
-    const int64_t tpb = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
-    const int64_t ntiles = tpb * q.batch;
-    if (ntiles > INT32_MAX)
-        return GEMM_ERR_NOT_SUPPORTED;
-    p.tiles_per_batch = static_cast<int>(tpb);
-    p.num_tiles = static_cast<int>(ntiles);
-    p.group_x = 8;
-    p.mode = kModeTiles;
-    p.total_iters = static_cast<long long>(ntiles) * p.num_kb;
-    p.vec4 = (aligned(q.Out, static_cast<uintptr_t>(4 * q.out_esize())) && q.ldo % 4 == 0 &&
-              (q.batch == 1 || q.sO % 4 == 0))
-                 ? 1
-                 : 0;
-    p.status = d->status;
-    p.wait_limit = wait_limit();
-    p.fault = g_fault.load();
-    // same split rule as run_tc05_pair
-    constexpr int64_t kMaxPieces = 4;
-    const int P = d->max_pairs;
-    const int64_t rem = pair_split(ntiles, p.num_kb, P, q.out_type) ? ntiles : 0;
-    const int64_t sk_pairs = std::min<int64_t>(P, rem * kMaxPieces);
-    int pairs = static_cast<int>(std::min<int64_t>(ntiles, P));
-    p.sk_first = p.num_tiles;
-    p.sk_iters = 0;
-    p.sk_pairs = 0;
-    if (rem != 0) {
-        if (sk_pairs > slice_pairs || rem > counter_tiles)
-            return GEMM_ERR_SCRATCH_TOO_SMALL;
-        // the counters must start at zero; the slices are fully rewritten
-        if (cudaMemsetAsync(counters, 0, static_cast<size_t>(rem) * 2 * 8 * sizeof(uint32_t), stream) !=
-            cudaSuccess)
-            return GEMM_ERR_CUDA;
-        p.sk_first = static_cast<int>(ntiles - rem);
-        p.sk_iters = rem * p.num_kb;
-        p.sk_pairs = static_cast<int>(sk_pairs);
-        p.ws = slices;
-        p.ws_flags = counters;
-        pairs = static_cast<int>(std::max<int64_t>(pairs, sk_pairs));
-    }
-    // Out rows 32-byte aligned: the epilogue stores without staging
-    const bool direct = p.sk_pairs == 0 && aligned(q.Out, static_cast<uintptr_t>(8 * q.out_esize())) &&
-                        q.ldo % 8 == 0 && (q.batch == 1 || q.sO % 8 == 0);
-    if (tc05_pair_launch(tma, tmb, p, pairs, pbn, direct, q.kind(), stream) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    return GEMM_OK;
+    return run_tc05_pair(q, *d, stream, &fixed);
 }
 
 }  // namespace gnt
@@ -1085,16 +1045,16 @@ gemm_status_t gemm_nt_f16_f32(const void* A, const void* B, float* Out, int64_t 
 }
 
 gemm_status_t gemm_nt_f16_f32_batched(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K,
-                                      int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
-                                      int64_t strideB, int64_t strideO, gemm_stream_t stream)
+                                      int64_t lda, int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB,
+                                      int64_t strideO, int64_t batch, gemm_stream_t stream)
 {
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
     return gnt::run(q, GEMM_PATH_AUTO, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_nt_f16_f32_batched_path(const void* A, const void* B, float* Out, int64_t M, int64_t N,
-                                           int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch,
-                                           int64_t strideA, int64_t strideB, int64_t strideO, gemm_path_t path,
+                                           int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t strideA,
+                                           int64_t strideB, int64_t strideO, int64_t batch, gemm_path_t path,
                                            gemm_stream_t stream)
 {
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
@@ -1102,8 +1062,8 @@ gemm_status_t gemm_nt_f16_f32_batched_path(const void* A, const void* B, float* 
 }
 
 gemm_status_t gemm_nt_batched_ex(const void* A, const void* B, void* Out, gemm_dtype_t ab_type, gemm_dtype_t out_type,
-                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch,
-                                 int64_t strideA, int64_t strideB, int64_t strideO, gemm_path_t path,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t strideA,
+                                 int64_t strideB, int64_t strideO, int64_t batch, gemm_path_t path,
                                  gemm_stream_t stream)
 {
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
@@ -1114,8 +1074,8 @@ gemm_status_t gemm_nt_batched_ex(const void* A, const void* B, void* Out, gemm_d
 
 gemm_status_t gemm_nt_batched_major(const void* A, gemm_major_t a_major, const void* B, gemm_major_t b_major,
                                     void* Out, gemm_dtype_t ab_type, gemm_dtype_t out_type, int64_t M, int64_t N,
-                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
-                                    int64_t strideB, int64_t strideO, gemm_path_t path, gemm_stream_t stream)
+                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB,
+                                    int64_t strideO, int64_t batch, gemm_path_t path, gemm_stream_t stream)
 {
     Problem q{A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
     q.ab_type = static_cast<int>(ab_type);
@@ -1127,7 +1087,7 @@ gemm_status_t gemm_nt_batched_major(const void* A, gemm_major_t a_major, const v
 
 gemm_status_t gemm_nt_mx(const void* A, const void* SA, const void* B, const void* SB, void* Out,
                          gemm_dtype_t ab_type, gemm_dtype_t out_type, int64_t M, int64_t N, int64_t K, int64_t lda,
-                         int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
+                         int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB, int64_t strideO, int64_t batch,
                          gemm_path_t path, gemm_stream_t stream)
 {
     if (K > 0 && M > 0 && N > 0 && batch > 0 && (!SA || !SB))
@@ -1168,7 +1128,7 @@ gemm_status_t gemm_nt_mx_pack_scales(const void* plain, int64_t ld, int64_t stri
     return gnt::mx_pack_launch(static_cast<const uint8_t*>(plain), ld, stride, static_cast<uint8_t*>(packed), rows, K,
                                batch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GEMM_OK
-               : GEMM_ERR_CUDA;
+               : GEMM_ERR_LAUNCH;
 }
 
 gemm_status_t gemm_nt_f16_f32_from_host(const void* A_host, const void* B_host, float* Out_host, void* dA,
@@ -1190,8 +1150,8 @@ gemm_status_t gemm_nt_f16_f32_from_host(const void* A_host, const void* B_host, 
 }
 
 gemm_path_t gemm_nt_select_path(const void* A, const void* B, const float* Out, int64_t M, int64_t N, int64_t K,
-                                int64_t lda, int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA,
-                                int64_t strideB, int64_t strideO)
+                                int64_t lda, int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB,
+                                int64_t strideO, int64_t batch)
 {
     Problem q{A, B, const_cast<float*>(Out), M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO};
     return gnt::select_path(q);
@@ -1204,29 +1164,30 @@ gemm_status_t gemm_nt_check(gemm_stream_t stream)
     if (st != GEMM_OK)
         return st;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     uint32_t word = 0;
     if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+        return GEMM_ERR_LAUNCH;
     if (word) {
         const uint32_t zero = 0;
         if (cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+            return GEMM_ERR_LAUNCH;
         gnt::reset_workspaces();
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
     return GEMM_OK;
 }
 
-const char* gemm_nt_status_string(gemm_status_t status)
+const char* gemm_nt_error_string(gemm_status_t status)
 {
     switch (status) {
     case GEMM_OK: return "success";
     case GEMM_ERR_INVALID_VALUE: return "invalid argument";
+    case GEMM_ERR_MISALIGNED: return "misaligned operand (reserved: never returned)";
     case GEMM_ERR_OVERLAP: return "output overlaps an input or itself";
-    case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
-    case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GEMM_ERR_LAUNCH: return "CUDA runtime or driver call failed";
     case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
     case GEMM_ERR_NOT_SUPPORTED: return "the requested kernel cannot take these arguments";
     case GEMM_ERR_SCRATCH_TOO_SMALL:
         return "the call needs more scratch than the no-allocation entry point's fixed array holds";
@@ -1249,7 +1210,7 @@ gemm_status_t gemm_nt_probe_m16n8k16(const void* A, const void* B, uint32_t* ar,
     return gnt::probe_launch(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), ar, br, dr,
                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? GEMM_OK
-               : GEMM_ERR_CUDA;
+               : GEMM_ERR_LAUNCH;
 }
 
 void gemm_nt_debug_set_wait_limit(uint64_t cycles) { gnt::g_wait_limit.store(cycles); }

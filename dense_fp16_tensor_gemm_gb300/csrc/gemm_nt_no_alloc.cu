@@ -24,34 +24,46 @@ static __device__ __align__(256) unsigned char g_no_alloc_scratch[kSliceBytes + 
 constexpr int kMaxDevices = 64;
 
 // Host code cannot use g_no_alloc_scratch's name as a device address: the
-// device address is looked up once per device, with that device current.
+// device address is looked up with the device current, once it has succeeded,
+// and again on the next call after a failed lookup.
 struct ScratchAddress {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
     unsigned char* ptr = nullptr;
 };
 ScratchAddress g_address[kMaxDevices];
+
+int current_scratch(gnt::PairScratch* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return GEMM_ERR_LAUNCH;
+    ScratchAddress& a = g_address[dev];
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(a.mu);
+        if (a.ptr == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr)
+                return GEMM_ERR_LAUNCH;
+            a.ptr = static_cast<unsigned char*>(p);
+        }
+        base = a.ptr;
+    }
+    out->slices = reinterpret_cast<float*>(base);
+    out->slice_pairs = kSlicePairs;
+    out->counters = reinterpret_cast<uint32_t*>(base + kSliceBytes);
+    out->counter_tiles = kCounterTiles;
+    return GEMM_OK;
+}
 
 }  // namespace
 
 extern "C" gemm_status_t gemm_nt_f16_f32_batched_no_alloc(const void* A, const void* B, float* Out, int64_t M,
                                                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                                                          int64_t ldo, int64_t batch, int64_t strideA,
-                                                          int64_t strideB, int64_t strideO, gemm_stream_t stream)
+                                                          int64_t ldo, int64_t strideA, int64_t strideB,
+                                                          int64_t strideO, int64_t batch, gemm_stream_t stream)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return GEMM_ERR_CUDA;
-    ScratchAddress& a = g_address[dev];
-    std::call_once(a.once, [&a] {
-        void* p = nullptr;
-        a.err = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
-        a.ptr = static_cast<unsigned char*>(p);
-    });
-    if (a.err != cudaSuccess || a.ptr == nullptr)
-        return GEMM_ERR_CUDA;
-    return static_cast<gemm_status_t>(gnt::run_pair_no_alloc(
-        A, B, Out, M, N, K, lda, ldb, ldo, batch, strideA, strideB, strideO, reinterpret_cast<float*>(a.ptr),
-        kSlicePairs, reinterpret_cast<uint32_t*>(a.ptr + kSliceBytes), kCounterTiles,
-        reinterpret_cast<cudaStream_t>(stream)));
+    return static_cast<gemm_status_t>(gnt::run_pair_no_alloc(A, B, Out, M, N, K, lda, ldb, ldo, strideA, strideB,
+                                                             strideO, batch, current_scratch,
+                                                             reinterpret_cast<cudaStream_t>(stream)));
 }

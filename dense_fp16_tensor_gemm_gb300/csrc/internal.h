@@ -126,13 +126,26 @@ cudaError_t mmasync_launch(const MmaParams& p, int in_type, cudaStream_t stream)
 cudaError_t probe_launch(const uint16_t* A, const uint16_t* B, uint32_t* ar, uint32_t* br, float* dr,
                          cudaStream_t stream);
 
-// The CTA-pair kernel on caller-independent scratch (no allocation): `slices`
-// holds the stream-K slices of up to `slice_pairs` pairs, `counters` the
-// counters of up to `counter_tiles` split tiles.  Plans the call exactly like
-// the automatic path would for the CTA-pair kernel; returns
-// GEMM_ERR_SCRATCH_TOO_SMALL if that plan needs more.
+// Scratch of the pair kernel's split (stream-K) path in memory that the caller
+// of run_pair_no_alloc owns: `slices` holds the slices of up to `slice_pairs`
+// launched pairs (4 * kPairSliceBytes each), `counters` the counters of up to
+// `counter_tiles` split tiles (16 words each).
+struct PairScratch {
+    float* slices;
+    int slice_pairs;
+    uint32_t* counters;
+    int counter_tiles;
+};
+// Fills in the current device's fixed scratch; returns a gemm_status_t value.
+typedef int (*PairScratchFn)(PairScratch* out);
+
+// The CTA-pair kernel without any allocation.  Host-side argument errors are
+// returned before any CUDA call; `scratch` is called only for valid, non-empty
+// arguments.  Plans the call exactly like the automatic path does for the
+// CTA-pair kernel (the same planner); returns GEMM_ERR_SCRATCH_TOO_SMALL if that
+// plan needs more than the scratch holds.
 int run_pair_no_alloc(const void* A, const void* B, float* Out, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldo, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideO,
-                      float* slices, int slice_pairs, uint32_t* counters, int counter_tiles, cudaStream_t stream);
+                      int64_t ldb, int64_t ldo, int64_t strideA, int64_t strideB, int64_t strideO, int64_t batch,
+                      PairScratchFn scratch, cudaStream_t stream);
 
 }  // namespace gnt

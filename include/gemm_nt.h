@@ -13,6 +13,15 @@
  * accumulator (C = 0, accum=False), so Out is overwritten: there is no alpha,
  * beta or C input.
  *
+ * The pages run each kernel as compiled(a, b, out) on torch CUDA tensors (the
+ * listings that compile the kernel and compare it with torch, in "Warp Matrix
+ * Instructions" and "Blackwell Tensor Cores") and define no C interface.  The
+ * entry points here take that call's three operands as device pointers, in the
+ * same order (A, B, Out), followed by the sizes, the leading dimensions, the
+ * batch strides and batch count where there are any, and the stream.  Status
+ * codes 0-6 are those of the plain and batched products; 7 and 8 belong to the
+ * entry points that choose a kernel or allocate nothing.
+ *
  * Conventions shared by every entry point
  *   - Pointers A, B, Out are DEVICE pointers owned by the caller.  A and B hold
  *     fp16 bit patterns (__half / uint16_t).  The library keeps no reference to
@@ -33,6 +42,10 @@
  *   - Thread safety: all entry points may be called concurrently from several
  *     host threads.  Calls whose Out ranges overlap must not run concurrently.
  *   - Only devices of compute capability 10.3 (GB300, sm_103a) are supported.
+ *   - Per-device set-up (kernel attributes, the status word's address) is done
+ *     once, by the first call on a device that passes the argument checks, and
+ *     kept for the life of the process: after cudaDeviceReset() on a device,
+ *     make no further call on that device.
  */
 #ifndef GEMM_NT_H
 #define GEMM_NT_H
@@ -50,12 +63,16 @@ typedef struct CUstream_st *gemm_stream_t;
 typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_VALUE = 1,      /* null pointer, negative size, ld < row length, ... */
-    GEMM_ERR_OVERLAP = 2,            /* Out overlaps A or B, or batches of Out overlap */
-    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
-    GEMM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (launch, tensor map) */
+    GEMM_ERR_MISALIGNED = 2,         /* reserved, never returned: layouts the tensor-core kernels
+                                        cannot read run on the warp-MMA kernel instead */
+    GEMM_ERR_OVERLAP = 3,            /* Out overlaps A or B, or batches of Out overlap */
+    GEMM_ERR_LAUNCH = 4,             /* a CUDA runtime/driver call failed (launch, tensor map,
+                                        synchronisation, per-device set-up) */
     GEMM_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait ran out; Out is undefined */
-    GEMM_ERR_NOT_SUPPORTED = 6,      /* the requested kernel cannot take these arguments */
-    GEMM_ERR_SCRATCH_TOO_SMALL = 7   /* gemm_nt_f16_f32_batched_no_alloc: the call needs more
+    GEMM_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
+    /* Codes 7 and 8 belong to entry points beyond the plain and batched products: */
+    GEMM_ERR_NOT_SUPPORTED = 7,      /* the requested kernel cannot take these arguments */
+    GEMM_ERR_SCRATCH_TOO_SMALL = 8   /* gemm_nt_f16_f32_batched_no_alloc: the call needs more
                                         scratch than the library's fixed array holds */
 } gemm_status_t;
 
@@ -110,8 +127,8 @@ gemm_status_t gemm_nt_f16_f32(const void *A, const void *B, float *Out,
 gemm_status_t gemm_nt_f16_f32_batched(const void *A, const void *B, float *Out,
                                       int64_t M, int64_t N, int64_t K,
                                       int64_t lda, int64_t ldb, int64_t ldo,
-                                      int64_t batch, int64_t strideA, int64_t strideB,
-                                      int64_t strideO, gemm_stream_t stream);
+                                      int64_t strideA, int64_t strideB, int64_t strideO,
+                                      int64_t batch, gemm_stream_t stream);
 
 /*
  * As gemm_nt_f16_f32_batched, on an explicitly chosen kernel.  Returns
@@ -127,8 +144,8 @@ gemm_status_t gemm_nt_f16_f32_batched(const void *A, const void *B, float *Out,
 gemm_status_t gemm_nt_f16_f32_batched_path(const void *A, const void *B, float *Out,
                                            int64_t M, int64_t N, int64_t K,
                                            int64_t lda, int64_t ldb, int64_t ldo,
-                                           int64_t batch, int64_t strideA, int64_t strideB,
-                                           int64_t strideO, gemm_path_t path,
+                                           int64_t strideA, int64_t strideB, int64_t strideO,
+                                           int64_t batch, gemm_path_t path,
                                            gemm_stream_t stream);
 
 /*
@@ -166,8 +183,8 @@ gemm_status_t gemm_nt_batched_ex(const void *A, const void *B, void *Out,
                                  gemm_dtype_t ab_type, gemm_dtype_t out_type,
                                  int64_t M, int64_t N, int64_t K,
                                  int64_t lda, int64_t ldb, int64_t ldo,
-                                 int64_t batch, int64_t strideA, int64_t strideB,
-                                 int64_t strideO, gemm_path_t path, gemm_stream_t stream);
+                                 int64_t strideA, int64_t strideB, int64_t strideO,
+                                 int64_t batch, gemm_path_t path, gemm_stream_t stream);
 
 /* Storage order of one operand of gemm_nt_batched_major.  The operand is the
  * logical (rows, K) matrix of the product (A: rows = M; B: rows = N).
@@ -208,8 +225,8 @@ gemm_status_t gemm_nt_batched_major(const void *A, gemm_major_t a_major, const v
                                     gemm_dtype_t ab_type, gemm_dtype_t out_type,
                                     int64_t M, int64_t N, int64_t K,
                                     int64_t lda, int64_t ldb, int64_t ldo,
-                                    int64_t batch, int64_t strideA, int64_t strideB,
-                                    int64_t strideO, gemm_path_t path, gemm_stream_t stream);
+                                    int64_t strideA, int64_t strideB, int64_t strideO,
+                                    int64_t batch, gemm_path_t path, gemm_stream_t stream);
 
 /*
  * Block-scaled 8-bit product ("Blackwell Tensor Cores", on the other TMEM
@@ -248,8 +265,8 @@ gemm_status_t gemm_nt_mx(const void *A, const void *SA, const void *B, const voi
                          gemm_dtype_t ab_type, gemm_dtype_t out_type,
                          int64_t M, int64_t N, int64_t K,
                          int64_t lda, int64_t ldb, int64_t ldo,
-                         int64_t batch, int64_t strideA, int64_t strideB,
-                         int64_t strideO, gemm_path_t path, gemm_stream_t stream);
+                         int64_t strideA, int64_t strideB, int64_t strideO,
+                         int64_t batch, gemm_path_t path, gemm_stream_t stream);
 
 /* Bytes of one packed scale matrix for `rows` rows and K elements of K:
  * ceil(rows/128) * ceil(K/128) * 512; -1 for negative arguments. */
@@ -307,19 +324,24 @@ gemm_status_t gemm_nt_f16_f32_from_host(const void *A_host, const void *B_host, 
  * with K >= 6144 on a 152-SM GB300) returns GEMM_ERR_SCRATCH_TOO_SMALL and
  * launches nothing; problems that are not split use no scratch at all.
  *
- * It calls no cudaMalloc, cudaFree or other allocating routine.  The first call
- * on each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
- * Before each split launch the counters are cleared on `stream`.  All calls
- * share the one array: calls that may overlap on the GPU (different streams,
- * or several host threads without ordering) race on it and give wrong results,
- * so order them on one stream.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Argument
+ * errors are returned before any CUDA call, as for every entry point.  The
+ * first call on a device whose arguments pass the checks (and are not empty)
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  A lookup that
+ * failed is tried again on the next call.  The address is kept for the life of
+ * the process, so after cudaDeviceReset() on a device make no further call on
+ * it.  Before each split launch the counters are cleared on `stream`
+ * (cudaMemsetAsync, which allocates nothing).  All calls share the one array:
+ * calls that may overlap on the GPU (different streams, or several host threads
+ * without ordering) race on it and give wrong results, so order them on one
+ * stream.
  */
 gemm_status_t gemm_nt_f16_f32_batched_no_alloc(const void *A, const void *B, float *Out,
                                                int64_t M, int64_t N, int64_t K,
                                                int64_t lda, int64_t ldb, int64_t ldo,
-                                               int64_t batch, int64_t strideA, int64_t strideB,
-                                               int64_t strideO, gemm_stream_t stream);
+                                               int64_t strideA, int64_t strideB, int64_t strideO,
+                                               int64_t batch, gemm_stream_t stream);
 
 /*
  * The kernel GEMM_PATH_AUTO would choose for these arguments (host-only: reads
@@ -329,18 +351,19 @@ gemm_status_t gemm_nt_f16_f32_batched_no_alloc(const void *A, const void *B, flo
 gemm_path_t gemm_nt_select_path(const void *A, const void *B, const float *Out,
                                 int64_t M, int64_t N, int64_t K,
                                 int64_t lda, int64_t ldb, int64_t ldo,
-                                int64_t batch, int64_t strideA, int64_t strideB,
-                                int64_t strideO);
+                                int64_t strideA, int64_t strideB, int64_t strideO,
+                                int64_t batch);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_ERR_DEVICE_TIMEOUT if any kernel launched since the last check hit
- * its bounded-wait limit, GEMM_ERR_CUDA if the synchronisation failed, else GEMM_OK.
+ * its bounded-wait limit, GEMM_ERR_LAUNCH if the synchronisation failed, else GEMM_OK.
  */
 gemm_status_t gemm_nt_check(gemm_stream_t stream);
 
-/* Static, human-readable text for a status code. */
-const char *gemm_nt_status_string(gemm_status_t status);
+/* Static, human-readable text for a status code ("unknown status" for a value
+ * outside gemm_status_t).  Never NULL. */
+const char *gemm_nt_error_string(gemm_status_t status);
 
 /*
  * Diagnostic: one warp executes the warp example of "Warp Matrix Instructions"

@@ -35,7 +35,7 @@ def run_path(A, B, path, lda=None, ldb=None, ldo=None, a_offset=0, b_offset=0):
     out = torch.full((batch, M, ldo), float("nan"), dtype=torch.float32, device="cuda")
     gnt.gemm_nt_f16_f32_batched_path(
         a.data_ptr() + 2 * a_offset, b.data_ptr() + 2 * b_offset, out.data_ptr(), M, N, K, lda,
-        ldb, ldo, batch, M * lda, N * ldb, M * ldo, path, torch.cuda.current_stream().cuda_stream)
+        ldb, ldo, M * lda, N * ldb, M * ldo, batch, path, torch.cuda.current_stream().cuda_stream)
     gnt.gemm_nt_check(torch.cuda.current_stream().cuda_stream)
     o = out.cpu().numpy()
     if ldo > N:
@@ -163,7 +163,7 @@ def run_general(A, B, ab, out, path, a_mn=False, b_mn=False, lda=None, ldb=None,
     stream = torch.cuda.current_stream().cuda_stream
     gnt.gemm_nt_batched_major(pa, gnt.Major.MN if a_mn else gnt.Major.K, pb, gnt.Major.MN if b_mn else gnt.Major.K,
                               o.data_ptr() + esize * out_offset, dtype_code(ab), dtype_code(out), M, N, K,
-                              lda, ldb, ldo, batch, As.shape[1] * lda, Bs.shape[1] * ldb, M * ldo, path, stream)
+                              lda, ldb, ldo, As.shape[1] * lda, Bs.shape[1] * ldb, M * ldo, batch, path, stream)
     gnt.gemm_nt_check(stream)
     host = o.double().cpu().numpy()
     assert np.all(np.isnan(host[:out_offset])), "kernel wrote before the Out base"

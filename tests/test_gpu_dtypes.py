@@ -49,7 +49,7 @@ def run_ex(A, B, ab, out, path, ldo=None, out_offset=0, lda=None, ldb=None):
     esize = o.element_size()
     stream = torch.cuda.current_stream().cuda_stream
     gnt.gemm_nt_batched_ex(pa, pb, o.data_ptr() + esize * out_offset, _code(ab), _code(out), M, N, K,
-                           lda, ldb, ldo, batch, M * lda, N * ldb, M * ldo, path, stream)
+                           lda, ldb, ldo, M * lda, N * ldb, M * ldo, batch, path, stream)
     gnt.gemm_nt_check(stream)
     host = o.double().cpu().numpy()
     assert np.all(np.isnan(host[:out_offset])), "kernel wrote before the Out base"
@@ -121,7 +121,7 @@ def test_padded_and_misaligned_inputs(ab):
     stream = torch.cuda.current_stream().cuda_stream
     assert gnt.gemm_nt_select_path(pa, pb, o.data_ptr(), 150, 140, 136, 136, 136, 140) == P.MMASYNC
     gnt.gemm_nt_batched_ex(pa, pb, o.data_ptr(), _code(ab), gnt.DType.F16, 150, 140, 136, 136, 136, 140,
-                           1, 0, 0, 0, P.AUTO, stream)
+                           0, 0, 0, 1, P.AUTO, stream)
     gnt.gemm_nt_check(stream)
     check(o.double().cpu().numpy()[None], ref, absdot, "f16", "misaligned")
 
@@ -173,7 +173,7 @@ def test_k_zero_writes_zeros(out):
     import torch
     o = torch.full((2, 70, 90), float("nan"), dtype=_torch_dtype(out), device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
-    gnt.gemm_nt_batched_ex(16, 16, o.data_ptr(), gnt.DType.BF16, _code(out), 70, 90, 0, 0, 0, 90, 2, 0, 0,
-                           70 * 90, P.AUTO, stream)
+    gnt.gemm_nt_batched_ex(16, 16, o.data_ptr(), gnt.DType.BF16, _code(out), 70, 90, 0, 0, 0, 90, 0, 0,
+                           70 * 90, 2, P.AUTO, stream)
     gnt.gemm_nt_check(stream)
     assert bool(torch.all(o == 0))

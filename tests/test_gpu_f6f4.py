@@ -76,7 +76,7 @@ def test_padded_pitch_and_refusals(ab):
     with pytest.raises(gnt.GemmError) as e:
         gnt.gemm_nt_batched_major(z.data_ptr(), gnt.Major.MN, z.data_ptr() + 65536, gnt.Major.K, o.data_ptr(),
                                   getattr(gnt.DType, ab.upper()), gnt.DType.F32, 260, 300, 256, 260, 256, 300,
-                                  1, 0, 0, 0, P.AUTO, torch.cuda.current_stream().cuda_stream)
+                                  0, 0, 0, 1, P.AUTO, torch.cuda.current_stream().cuda_stream)
     assert e.value.status == gnt.Status.INVALID_VALUE
 
 

@@ -33,7 +33,7 @@ def _run(A, B, path):
     a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     out = torch.zeros((A.shape[0], B.shape[0]), dtype=torch.float32, device="cuda")
     gnt.gemm_nt_f16_f32_batched_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), A.shape[0], B.shape[0],
-                                     A.shape[1], A.shape[1], B.shape[1], B.shape[0], 1, 0, 0, 0, path,
+                                     A.shape[1], A.shape[1], B.shape[1], B.shape[0], 0, 0, 0, 1, path,
                                      torch.cuda.current_stream().cuda_stream)
     return out
 

@@ -99,7 +99,7 @@ def test_misaligned_base_uses_warp_kernel():
     o = torch.zeros(150 * 140, dtype=torch.float32, device="cuda")
     with pytest.raises(gnt.GemmError) as e:
         gnt.gemm_nt_batched_major(a.data_ptr() + 2, gnt.Major.MN, b.data_ptr(), gnt.Major.MN, o.data_ptr(),
-                                  gnt.DType.F16, gnt.DType.F32, 150, 140, 136, 150, 140, 140, 1, 0, 0, 0,
+                                  gnt.DType.F16, gnt.DType.F32, 150, 140, 136, 150, 140, 140, 0, 0, 0, 1,
                                   P.TC05_PAIR, torch.cuda.current_stream().cuda_stream)
     assert e.value.status == gnt.Status.NOT_SUPPORTED
 
@@ -120,7 +120,7 @@ def test_shared_operand(a_mn, b_mn):
     stream = torch.cuda.current_stream().cuda_stream
     gnt.gemm_nt_batched_major(pa, gnt.Major.MN if a_mn else gnt.Major.K, pb, gnt.Major.MN if b_mn else gnt.Major.K,
                               o.data_ptr(), gnt.DType.F16, gnt.DType.F32, M, N, K, As.shape[2], Bs.shape[2], N,
-                              batch, As.shape[1] * As.shape[2], 0, M * N, P.AUTO, stream)
+                              As.shape[1] * As.shape[2], 0, M * N, batch, P.AUTO, stream)
     gnt.gemm_nt_check(stream)
     check_tol(o.double().cpu().numpy(), ref, absdot, "f32", "shared B")
 
@@ -147,7 +147,7 @@ def test_nn_product_of_row_major_matrices():
     x, y = gpu_util.to_device(X, "f16")[0], gpu_util.to_device(Y[None], "f16")[0]
     c = torch.empty((M, N), dtype=torch.float32, device="cuda")
     gnt.gemm_nt_batched_major(x.data_ptr(), gnt.Major.K, y.data_ptr(), gnt.Major.MN, c.data_ptr(), gnt.DType.F16,
-                              gnt.DType.F32, M, N, K, K, N, N, 1, 0, 0, 0, P.AUTO,
+                              gnt.DType.F32, M, N, K, K, N, N, 0, 0, 0, 1, P.AUTO,
                               torch.cuda.current_stream().cuda_stream)
     gnt.gemm_nt_check()
     check_tol(c.double().cpu().numpy(), ref, absdot, "f32", "NN")

@@ -62,7 +62,7 @@ def run_mx(A, SA, B, SB, ab, out, path, shared_b=False, lda=None, pack_on_host=F
     o = torch.full((batch, M, N), float("nan"), dtype=gpu_util.torch_dtype(out), device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     gnt.gemm_nt_mx(pa, sa.data_ptr(), pb, sb.data_ptr(), o.data_ptr(), gpu_util.dtype_code(ab),
-                   gpu_util.dtype_code(out), M, N, K, lda, K, N, batch, M * lda, 0 if shared_b else N * K, M * N,
+                   gpu_util.dtype_code(out), M, N, K, lda, K, N, M * lda, 0 if shared_b else N * K, M * N, batch,
                    path, stream)
     gnt.gemm_nt_check(stream)
     return o.double().cpu().numpy()
@@ -171,7 +171,7 @@ def test_torch_wrapper_and_unsupported_paths():
     for path in (P.MMASYNC,):
         with pytest.raises(gnt.GemmError) as e:
             gnt.gemm_nt_mx(a.data_ptr(), pa.data_ptr(), b.data_ptr(), pb.data_ptr(), o.data_ptr(), gnt.DType.E4M3,
-                           gnt.DType.F32, 192, 256, 320, 320, 320, 256, 1, 0, 0, 0, path,
+                           gnt.DType.F32, 192, 256, 320, 320, 320, 256, 0, 0, 0, 1, path,
                            torch.cuda.current_stream().cuda_stream)
         assert e.value.status == gnt.Status.NOT_SUPPORTED
     # a pitch that is not a multiple of 16 bytes: no block-scaled kernel reads it
@@ -211,7 +211,7 @@ def test_pair_both_tile_widths(M, N, K, pad):
     o = torch.full((M, ldo), float("nan"), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     gnt.gemm_nt_mx(pa, sa.data_ptr(), pb, sb.data_ptr(), o.data_ptr(), gnt.DType.E4M3, gnt.DType.F32, M, N, K,
-                   K, K, ldo, 1, 0, 0, 0, P.TC05_PAIR, stream)
+                   K, K, ldo, 0, 0, 0, 1, P.TC05_PAIR, stream)
     gnt.gemm_nt_check(stream)
     got = o.double().cpu().numpy()
     if pad:
