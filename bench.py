@@ -253,6 +253,115 @@ def run_reference(args, w):
     return 0
 
 
+def l2_policy(alg_bytes):
+    """(rotate, flush, n_sets) for a workload of alg_bytes per step: inputs larger
+    than 2 x L2 run back to back; 16 MiB to 2 x L2 rotate over copies that fill
+    more than 3 x L2; smaller ones flush L2 between timed steps."""
+    import math
+    rotate = 16 * 2 ** 20 <= alg_bytes <= 2 * L2_BYTES
+    flush = alg_bytes <= 2 * L2_BYTES and not rotate
+    n_sets = 1 + int(math.ceil(3 * L2_BYTES / alg_bytes)) if rotate else 1
+    return rotate, flush, n_sets
+
+
+def roofline_of(flops, alg_bytes, kernel_ms, peaks):
+    """The bound (tensor or HBM) by arithmetic intensity against the measured
+    peaks, and the achieved fraction of it."""
+    tensor_bound = flops / alg_bytes * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12
+    if tensor_bound:
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["tflops"]}
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"]}
+
+
+def time_workload(gnt, torch, w, steps, warmup, stream, bus, peaks):
+    """Device time of one fp16 -> fp32 workload on the automatic path, as the
+    headline line times its own (inputs resident in HBM, the same L2 policy,
+    CUDA events on the launching stream, clocks sampled meanwhile)."""
+    A, B = workloads.workload_inputs(w.name)
+    a = torch.from_numpy(A.view("int16")).view(torch.float16).cuda()
+    b = torch.from_numpy(B.view("int16")).view(torch.float16).cuda()
+    batched = A.ndim == 3
+    out = torch.empty((w.batch, w.M, w.N) if batched else (w.M, w.N), dtype=torch.float32, device="cuda")
+    nb = w.batch if batched else 1
+    sA, sB, sO = (w.M * w.K, w.N * w.K, w.M * w.N) if batched else (0, 0, 0)
+    rotate, flush, n_sets = l2_policy(w.bytes)
+    sets = [(a, b, out)] + [(a.clone(), b.clone(), torch.empty_like(out)) for _ in range(n_sets - 1)]
+    sh = stream.cuda_stream
+    cur = [0]
+
+    def step():
+        x, y, o = sets[cur[0]]
+        cur[0] = (cur[0] + 1) % n_sets
+        gnt.gemm_nt_f16_f32_batched_path(x.data_ptr(), y.data_ptr(), o.data_ptr(), w.M, w.N, w.K, w.K, w.K, w.N,
+                                         sA, sB, sO, nb, gnt.Path.AUTO, sh)
+
+    scratch = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda") if flush else None
+    for _ in range(warmup):
+        step()
+    gnt.gemm_nt_check(sh)
+    sampler = ClockSampler(bus)
+    sampler.start()
+    n_ev = steps if flush else 1
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    torch.cuda.synchronize()
+    if flush:
+        for i in range(steps):
+            scratch.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+    else:
+        ev[0][0].record(stream)
+        for _ in range(steps):
+            step()
+        ev[0][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    gnt.gemm_nt_check(sh)
+    ms = sum(s.elapsed_time(e) for s, e in ev) / steps
+    roof = roofline_of(w.flops, w.bytes, ms, peaks)
+    rec = {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+           "roofline": roof, "gbs_algorithmic": w.bytes / (ms * 1e-3) / 1e9, "clocks": clocks,
+           "gpu_launches": steps, "path": gnt.gemm_nt_select_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M,
+                                                                   w.N, w.K, w.K, w.K, w.N, sA, sB, sO, nb).name,
+           "l2": workload_config(w, flush, n_sets=n_sets)["l2"]}
+    if w.name == "skinny_64x16384x8192":
+        rec["hbm_frac_of_8tbs"] = rec["gbs_algorithmic"] / 8000.0
+    if w.name == "tile_128x64x64":
+        rec["note"] = "one 128x64x64 tile: launch-bound, time reported"
+    del sets, a, b, out, scratch
+    torch.cuda.empty_cache()
+    return rec
+
+
+def steady_state(gnt, torch, step, flops, seconds, ms_hint, stream, bus, peaks):
+    """The same step back to back for about `seconds` (long enough for the board
+    to reach its power cap): TFLOP/s over the whole run, against the measured
+    sustained peak."""
+    n = max(10, int(seconds * 1e3 / max(ms_hint, 1e-3)))
+    sampler = ClockSampler(bus)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    gnt.gemm_nt_check(stream.cuda_stream)
+    ms = e0.elapsed_time(e1) / n
+    value = flops / (ms * 1e-3) / 1e12
+    peak = peaks.get("tflops_sustained") or peaks["tflops"]
+    return {"value": value, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n, "seconds": ms * n * 1e-3,
+            "frac_of_sustained_peak": value / peak, "sustained_peak": peak, "frac_of_burst_peak": value / peaks["tflops"],
+            "clocks": clocks, "gpu_launches": n, "l2": "inputs larger than L2, steps back to back"}
+
+
 def workload_config(w, flush, ab="f16", out="f32", alg_bytes=None, a_major="K", b_major="K", mx=False, n_sets=1):
     cfg = {"workload": "%s: %s; Out = A @ B.T, A (%s%d,%d) and B (%s%d,%d) %s row-major, "
                        "fp32 accumulate, %s Out" % (
@@ -292,6 +401,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS context timing")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other four workloads (the default 8192^3 run times them too)")
+    ap.add_argument("--steady-seconds", type=float, default=3.0,
+                    help="back-to-back run of the default workload after the timed region, for the "
+                         "power-capped figure (0: skip)")
     ap.add_argument("--a-major", default="K", choices=["K", "MN"],
                     help="MN: A handed to the library as its transpose, (K, M) row-major")
     ap.add_argument("--b-major", default="K", choices=["K", "MN"],
@@ -635,6 +749,21 @@ def main():
         return 0
 
     peaks = measured_peaks()
+    headline = (w.name == "square_8192" and default_types and default_layout and not args.mx
+                and args.path == "AUTO")
+    bus_id = bus if isinstance(bus, str) else None
+    # ---- the other four workloads, each timed like the headline (1 GPU)
+    others = None
+    if headline and world == 1 and not args.no_workloads:
+        others = {}
+        n_other = min(200, max(20, args.steps))
+        for name in ("tile_128x64x64", "square_4096", "skinny_64x16384x8192", "ragged_batch16_3001x2047x1000"):
+            others[name] = time_workload(gnt, torch, workloads.WORKLOADS[name], n_other, args.warmup, stream,
+                                         bus_id, peaks)
+    # ---- the headline back to back for seconds: the power-capped figure
+    steady = None
+    if headline and args.steady_seconds > 0:
+        steady = steady_state(gnt, torch, step, w.flops, args.steady_seconds, kernel_ms, stream, bus_id, peaks)
     ai = w.flops / alg_bytes
     # the 8-bit MMA runs at twice the 16-bit rate: its peak is the measured
     # bf16 one times that nominal ratio (4.5 / 2.25 PFLOP/s dense)
@@ -685,6 +814,8 @@ def main():
         "ms_per_step_median": step_ms_median,
         "hot": hot,
         "context_cublas": cublas,
+        "workloads": others,
+        "steady_state": steady,
         "device": {"name": torch.cuda.get_device_name(local),
                    "sms": torch.cuda.get_device_properties(local).multi_processor_count},
     }
