@@ -202,3 +202,19 @@ def test_pair_stream_k_integer_exact_and_deterministic():
     A, B = workloads.make_inputs(0, 512, 512, 8192, "normal", 1.0, seed=5)
     o1, o2 = run_path(A, B, P.TC05_PAIR), run_path(A, B, P.TC05_PAIR)
     assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32)), "stream-K sum order is not fixed"
+
+
+@pytest.mark.parametrize("batch,M,N,K", [(2, 600, 1024, 1000), (1, 513, 768, 2000)])
+def test_epilogue_choice_keeps_every_bit(batch, M, N, K):
+    """The pair kernel stores Out straight from TMEM when A's and B's rows sit on
+    128-byte lines, and through shared memory otherwise (rows of K = 1000
+    elements are 2000 bytes apart).  Both epilogues store the same accumulator:
+    the products must agree bit for bit with each other, and with the oracle."""
+    A, B = workloads.make_inputs(batch, M, N, K, "normal", 1.0, seed=batch + M + K)
+    ref, absdot = oracle.gemm_nt(A, B)
+    pitch = (K + 63) // 64 * 64  # whole 128-byte lines
+    packed = run_path(A, B, P.TC05_PAIR)                                  # 2000- / 4000-byte rows
+    padded = run_path(A, B, P.TC05_PAIR, lda=pitch, ldb=pitch)           # rows on 128-byte lines
+    assert_parity(packed, ref, absdot, what="pair, rows off their lines")
+    assert_parity(padded, ref, absdot, what="pair, rows on lines")
+    assert np.array_equal(packed, padded)
