@@ -325,6 +325,9 @@ def time_workload(gnt, torch, w, steps, warmup, stream, bus, peaks):
     gnt.gemm_nt_check(sh)
     ms = sum(s.elapsed_time(e) for s, e in ev) / steps
     roof = roofline_of(w.flops, w.bytes, ms, peaks)
+    # DRAM bytes per launch from an ncu capture, while the kernel's sources match it
+    tr = TRAFFIC.get(traffic_key(w.name))
+    roof["traffic"] = tr[0] if tr and w.name in KERNEL_SOURCES and tr[1] == kernel_source_sha(w.name) else None
     rec = {"value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
            "roofline": roof, "gbs_algorithmic": w.bytes / (ms * 1e-3) / 1e9, "clocks": clocks,
            "gpu_launches": steps, "path": gnt.gemm_nt_select_path(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M,
