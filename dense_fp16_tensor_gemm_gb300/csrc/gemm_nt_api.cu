@@ -34,16 +34,18 @@ constexpr unsigned long long kDefaultWaitLimit = 4000000000ull;  // ~2 s of SM c
 std::atomic<unsigned long long> g_wait_limit{0};
 std::atomic<int> g_fault{0};
 
+// Set up once per device by the first call that succeeds in it: a set-up that
+// failed (a CUDA error) is tried again by the next call.
 struct DeviceState {
-    std::once_flag once;
-    cudaError_t init_err = cudaSuccess;
+    std::mutex init_mu;
+    std::atomic<bool> ready{false};  // set-up done (supported or not)
     bool supported = false;
     int num_sms = 0;
     int max_pairs = 0;  // CTA pairs of the pair kernel resident at once
     uint32_t* status = nullptr;
-    // host-buffer pipeline: copy streams and events, created on first use
-    std::once_flag pipe_once;
-    cudaError_t pipe_err = cudaSuccess;
+    // host-buffer pipeline: copy streams and events, created by the first call
+    // that succeeds in creating them
+    std::atomic<bool> pipe_ready{false};
     std::mutex pipe_mu;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t ev[2 + 2 * 16];  // start, done, per-chunk input and output events
@@ -75,32 +77,37 @@ gemm_status_t device_state(DeviceState** out)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return GEMM_ERR_LAUNCH;
     DeviceState& d = g_dev[dev];
-    std::call_once(d.once, [&d, dev] {
-        int major = 0, minor = 0;
-        cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            d.init_err = e;
-            return;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(d.init_mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess)
+                return GEMM_ERR_LAUNCH;
+            const bool supported = major == 10 && minor == 3;
+            if (supported) {
+                void* sym = nullptr;
+                int max_pairs = 0;
+                e = cudaGetSymbolAddress(&sym, g_status_word);
+                if (e == cudaSuccess) e = cudaMemset(sym, 0, sizeof(uint32_t));
+                if (e == cudaSuccess) e = tc05_configure(64, false);
+                if (e == cudaSuccess) e = tc05_configure(128, false);
+                if (e == cudaSuccess) e = tc05_configure(256, false);
+                if (e == cudaSuccess) e = tc05_configure(64, true);
+                if (e == cudaSuccess) e = tc05_small_configure();
+                if (e == cudaSuccess) e = tc05_pair_configure(&max_pairs);
+                if (e != cudaSuccess)
+                    return GEMM_ERR_LAUNCH;
+                d.status = static_cast<uint32_t*>(sym);
+                d.max_pairs = max_pairs;
+            }
+            d.num_sms = sms;
+            d.supported = supported;
+            d.ready.store(true, std::memory_order_release);
         }
-        d.supported = (major == 10 && minor == 3);
-        if (!d.supported)
-            return;
-        void* sym = nullptr;
-        e = cudaGetSymbolAddress(&sym, g_status_word);
-        if (e == cudaSuccess) e = cudaMemset(sym, 0, sizeof(uint32_t));
-        if (e == cudaSuccess) e = tc05_configure(64, false);
-        if (e == cudaSuccess) e = tc05_configure(128, false);
-        if (e == cudaSuccess) e = tc05_configure(256, false);
-        if (e == cudaSuccess) e = tc05_configure(64, true);
-        if (e == cudaSuccess) e = tc05_small_configure();
-        if (e == cudaSuccess) e = tc05_pair_configure(&d.max_pairs);
-        d.status = static_cast<uint32_t*>(sym);
-        d.init_err = e;
-    });
-    if (d.init_err != cudaSuccess)
-        return GEMM_ERR_LAUNCH;
+    }
     if (!d.supported)
         return GEMM_ERR_UNSUPPORTED_DEVICE;
     *out = &d;
@@ -940,15 +947,18 @@ gemm_status_t from_host_pipelined(const void* A_host, const void* B_host, float*
     gemm_status_t st = device_state(&d);
     if (st != GEMM_OK)
         return st;
-    std::call_once(d->pipe_once, [d] {
-        cudaError_t e = cudaStreamCreateWithFlags(&d->h2d, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d->d2h, cudaStreamNonBlocking);
-        for (auto& ev : d->ev)
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        d->pipe_err = e;
-    });
-    if (d->pipe_err != cudaSuccess)
-        return GEMM_ERR_LAUNCH;
+    if (!d->pipe_ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(d->pipe_mu);
+        if (!d->pipe_ready.load(std::memory_order_relaxed)) {
+            cudaError_t e = d->h2d ? cudaSuccess : cudaStreamCreateWithFlags(&d->h2d, cudaStreamNonBlocking);
+            if (e == cudaSuccess && !d->d2h) e = cudaStreamCreateWithFlags(&d->d2h, cudaStreamNonBlocking);
+            for (auto& ev : d->ev)
+                if (e == cudaSuccess && !ev) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess)
+                return GEMM_ERR_LAUNCH;
+            d->pipe_ready.store(true, std::memory_order_release);
+        }
+    }
     if (batch == 1 && M >= 2048 && N >= 2048 && K > 0)
         return from_host_blocks(A_host, B_host, Out_host, dA, dB, dOut, M, N, K, *d, stream);
     // chunks: [first, first + count) of batches, or of rows when batch == 1

@@ -43,9 +43,10 @@
  *     host threads.  Calls whose Out ranges overlap must not run concurrently.
  *   - Only devices of compute capability 10.3 (GB300, sm_103a) are supported.
  *   - Per-device set-up (kernel attributes, the status word's address) is done
- *     once, by the first call on a device that passes the argument checks, and
- *     kept for the life of the process: after cudaDeviceReset() on a device,
- *     make no further call on that device.
+ *     once, by the first call on a device that passes the argument checks (a
+ *     set-up that failed is tried again by the next call), and kept for the
+ *     life of the process: after cudaDeviceReset() on a device, make no further
+ *     call on that device.
  */
 #ifndef GEMM_NT_H
 #define GEMM_NT_H
