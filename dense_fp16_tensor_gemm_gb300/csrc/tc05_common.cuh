@@ -239,6 +239,83 @@ __device__ __forceinline__ void store_rows_chunk(const TcParams& p, typename Out
     __syncwarp();
 }
 
+// fp32 Out rows that are not 16-byte aligned.  A 32-column row segment
+// stored one float per lane would cover two 128-byte lines; here every store
+// instruction writes one aligned line of one row instead.  Row rr's columns
+// start sr floats into a line, and the staging area keeps the row rotated by
+// sr: chunk column i at word (i + sr) mod 32.  So word l holds the line's
+// column l, from this chunk (l >= sr) or, for l < sr, from the previous
+// chunk's last sr columns, which stay in words 0 .. sr-1 until this chunk's
+// line is stored: the chunk's first 32 - sr columns go in before the line
+// stores, its last sr columns after them.  The last chunk's tail is stored
+// after the loop.  No bank conflicts when ldo is odd (the rows' rotations then
+// differ).  Only columns in [y0 + c_begin, min(y0 + c_end, rows_y)) and rows
+// below nx are stored, so the result is that of epilogue_store.
+__device__ __forceinline__ void epilogue_store_lines(const TcParams& p, uint32_t tbase, float* obase, int x_row0,
+                                                     int nx, int y0, int c_begin, int c_end, int lane,
+                                                     float* stage_buf)
+{
+    const int cb = y0 + c_begin;
+    const int ce = min(y0 + c_end, p.rows_y);
+    float* const row0 = obase + static_cast<int64_t>(x_row0) * p.ldo + cb;  // element (x_row0, cb)
+    const uint32_t s0 = (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row0)) >> 2) & 31u;
+    const uint32_t sstep = static_cast<uint32_t>(p.ldo) & 31u;
+    const int s_own = static_cast<int>((s0 + static_cast<uint32_t>(lane) * sstep) & 31u);  // sr of this lane's row
+    float* const wrot = stage_buf + lane * 32 + s_own;  // chunk column i goes to wrot[i] or wrot[i - 32]
+    const float* const rcol = stage_buf + lane;
+    int c = c_begin;
+#pragma unroll 1
+    for (; c < c_end; c += 32) {
+        if (nx <= 0 || y0 + c >= p.rows_y)
+            break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32_wait(tbase + static_cast<uint32_t>(c), r);
+        // Opaque copies of the loop-invariant row pointer and rotation, so that
+        // the 32 row pointers and rotations are formed here in every chunk
+        // rather than hoisted out of the loop into registers.
+        uint32_t sr;
+        uint64_t dst_bits;
+        asm volatile("mov.b32 %0, %1;" : "=r"(sr) : "r"(s0));
+        asm volatile("mov.b64 %0, %1;" : "=l"(dst_bits) : "l"(reinterpret_cast<uint64_t>(row0)));
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < 32 - s_own)
+                wrot[i] = __uint_as_float(r[i]);
+        __syncwarp();
+        const int gl = (y0 + c) - cb + lane;  // this lane's column, from cb, if its row started on a line
+        float* dst = reinterpret_cast<float*>(dst_bits);
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            const int g = gl - static_cast<int>(sr);
+            if (rr < nx && g >= 0 && g < ce - cb)
+                __stcs(dst + g, rcol[rr * 32]);
+            dst += p.ldo;
+            sr = (sr + sstep) & 31u;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i >= 32 - s_own)
+                wrot[i - 32] = __uint_as_float(r[i]);
+    }
+    __syncwarp();
+    if (c > c_begin) {
+        // the last chunk's columns [y0 + c - sr, y0 + c), in words 0 .. sr-1
+        const int gl = (y0 + c) - cb + lane;
+        float* dst = row0;
+        uint32_t sr = s0;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            const int g = gl - static_cast<int>(sr);
+            if (rr < nx && static_cast<uint32_t>(lane) < sr && g < ce - cb)
+                __stcs(dst + g, rcol[rr * 32]);
+            dst += p.ldo;
+            sr = (sr + sstep) & 31u;
+        }
+    }
+    __syncwarp();  // the staging area is rewritten by the next call
+}
+
 // One epilogue warp's share of a finished accumulator: TMEM lane quadrant q
 // (tile rows s.x0 + 32q .. +31) and accumulator columns [c_begin, c_end),
 // where `tacc` is the TMEM address of the accumulator's first column.  Other
@@ -262,6 +339,12 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Seg& s, 
     if (nx > row_cap)
         nx = row_cap;
     const int y0 = s.y0 + col_off;
+    if constexpr (!SWAP && OT == kOutF32) {
+        if (!partial && !p.vec4) {
+            epilogue_store_lines(p, tbase, obase, x_row0, nx, y0, c_begin, c_end, lane, stage_buf);
+            return;
+        }
+    }
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 32) {
         if (nx <= 0 || y0 + c >= p.rows_y)

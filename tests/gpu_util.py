@@ -11,7 +11,7 @@ def dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def run_path(A, B, path, lda=None, ldb=None, ldo=None, a_offset=0, b_offset=0):
+def run_path(A, B, path, lda=None, ldb=None, ldo=None, a_offset=0, b_offset=0, o_offset=0):
     """Out = A @ B.T through gemm_nt_f16_f32_batched_path.
 
     A (M,K) or (batch,M,K), B likewise, numpy float16.  Optional padded leading
@@ -32,12 +32,15 @@ def run_path(A, B, path, lda=None, ldb=None, ldo=None, a_offset=0, b_offset=0):
     b = torch.full((b_offset + batch * N * ldb,), float("nan"), dtype=torch.float16)
     b[b_offset:].view(batch, N, ldb)[:, :, :K] = torch.from_numpy(B3)
     a, b = a.cuda(), b.cuda()
-    out = torch.full((batch, M, ldo), float("nan"), dtype=torch.float32, device="cuda")
+    # Out's elements before the (offset) base and past column N hold NaN and must stay so
+    flat = torch.full((o_offset + batch * M * ldo,), float("nan"), dtype=torch.float32, device="cuda")
     gnt.gemm_nt_f16_f32_batched_path(
-        a.data_ptr() + 2 * a_offset, b.data_ptr() + 2 * b_offset, out.data_ptr(), M, N, K, lda,
+        a.data_ptr() + 2 * a_offset, b.data_ptr() + 2 * b_offset, flat.data_ptr() + 4 * o_offset, M, N, K, lda,
         ldb, ldo, M * lda, N * ldb, M * ldo, batch, path, torch.cuda.current_stream().cuda_stream)
     gnt.gemm_nt_check(torch.cuda.current_stream().cuda_stream)
-    o = out.cpu().numpy()
+    f = flat.cpu().numpy()
+    assert np.all(np.isnan(f[:o_offset])), "kernel wrote before Out's base"
+    o = f[o_offset:].reshape(batch, M, ldo)
     if ldo > N:
         assert np.all(np.isnan(o[:, :, N:])), "kernel wrote past column N"
     o = o[:, :, :N]

@@ -72,6 +72,22 @@ def test_padded_leading_dimensions(path):
     assert_parity(out, ref, absdot, what=path.name)
 
 
+# fp32 Out rows off 16-byte boundaries: the epilogue stores whole 128-byte lines,
+# rotating each row by its offset into a line.  Odd ldo gives every row its own
+# rotation, ldo = 2 (mod 4) two rows per rotation, and ldo = 0 (mod 32) with a
+# base one float off the same rotation on every row.  Shapes end inside a warp's
+# 32 rows and inside a 32-column chunk; integer inputs make the result exact.
+@pytest.mark.parametrize("path", [P.AUTO, P.TC05, P.TC05_PAIR])
+@pytest.mark.parametrize("M,N,ldo,o_offset", [(300, 517, 517, 0), (300, 517, 519, 3), (133, 700, 702, 0),
+                                              (133, 700, 704, 1), (261, 290, 320, 1), (40, 1000, 1001, 2),
+                                              (513, 77, 77, 5)])
+def test_misaligned_out_rows(path, M, N, ldo, o_offset):
+    A, B = workloads.make_inputs(0, M, N, 264, "int4", seed=M + N)
+    ref, absdot = oracle.gemm_nt(A, B)
+    out = run_path(A, B, path, ldo=ldo, o_offset=o_offset)
+    assert_parity(out, ref, absdot, exact=True, what="%s %dx%d ldo %d offset %d" % (path.name, M, N, ldo, o_offset))
+
+
 def test_misaligned_inputs_use_warp_kernel():
     A, B = workloads.make_inputs(0, 100, 90, 77, "uniform", seed=6)
     ref, absdot = oracle.gemm_nt(A, B)
