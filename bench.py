@@ -53,14 +53,14 @@ PACKED_BITS = {"e2m3": 6, "e3m2": 6, "e2m1": 4}
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1068301312 + 247986944, "6bf4aaa74c564c83"),
-    "square_4096": (91150848 + 34589952, "6bf4aaa74c564c83"),
-    "ragged_batch16_3001x2047x1000": (163060224 + 335566336, "6bf4aaa74c564c83"),
+    "square_8192": (1071864320 + 249641216, "6da15f6dd9fa44ab"),
+    "square_4096": (91443968 + 35110656, "6da15f6dd9fa44ab"),
+    "ragged_batch16_3001x2047x1000": (163064576 + 335357952, "6da15f6dd9fa44ab"),
     "skinny_64x16384x8192": (269565696 + 3018752, "4fa381e58c0df18e"),
     # block-scaled E4M3 and E2M1 inputs (--ab-dtype e4m3 / e2m1 --mx), packed E2M1 (--ab-dtype e2m1)
-    "square_8192/mx-e4m3": (363069184 + 235615232, "6bf4aaa74c564c83"),
-    "square_8192/mx-e2m1": (171309568 + 217513472, "6bf4aaa74c564c83"),
-    "square_8192/e2m1": (156682240 + 215752192, "6bf4aaa74c564c83"),
+    "square_8192/mx-e4m3": (357480704 + 235872000, "6da15f6dd9fa44ab"),
+    "square_8192/mx-e2m1": (170795776 + 217559552, "6da15f6dd9fa44ab"),
+    "square_8192/e2m1": (155943680 + 215941632, "6da15f6dd9fa44ab"),
     # the weight-stationary shape on the skinny product (--path TC05_WS)
     "skinny_64x16384x8192/TC05_WS": (278233600 + 5644032, "52c340da27c3933d"),
 }

@@ -452,6 +452,26 @@ bool encode_scale_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same scales as a 5-D tensor {128 bytes, 4 rows, 4 copies, K block group,
+// row block} whose copy dimension has stride 0: a box {128, 4, 4, 1, box_rb}
+// lands each of box_rb consecutive atoms of one K block group four times over,
+// as [row block][copy][atom] (the source of one non-replicating TMEM copy).
+bool encode_scale_rep_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t mats, int box_rb)
+{
+    auto enc = encode_fn();
+    const int64_t kg = (K + 127) / 128, rb = (rows + 127) / 128 * mats;
+    if (!enc || kg <= 0 || rb <= 0 || kg > (int64_t(1) << 31) || rb > (int64_t(1) << 31) || box_rb < 1 ||
+        box_rb > rb)
+        return false;
+    cuuint64_t dims[5] = {128, 4, 4, static_cast<cuuint64_t>(kg), static_cast<cuuint64_t>(rb)};
+    cuuint64_t strides[4] = {128, 0, 512, static_cast<cuuint64_t>(kg * 512)};
+    cuuint32_t box[5] = {128, 4, 4, 1, static_cast<cuuint32_t>(box_rb)};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int64_t batch,
               int64_t stride, int box_rows, int* bmul, int dtype = GEMM_DTYPE_F16, bool mn = false)
 {
@@ -766,8 +786,11 @@ gemm_status_t run_tc05_pair(const Problem& q, const DeviceState& d, cudaStream_t
         const int64_t mats_b = q.sB == 0 ? 1 : q.batch;
         p.sf_box_kg = static_cast<int>(std::min<int64_t>(8, (q.K + 127) / 128));
         p.sf_box_rb = static_cast<int>(std::min<int64_t>(2, (q.N + 127) / 128 * mats_b));
+        // 256-wide tiles take B's scales per data stage, four times over
+        const bool rep_b = pbn == 256 && direct;
         if (!encode_scale_map(&tmsa, q.SA, q.M, q.K, q.sA == 0 ? 1 : q.batch, 1, p.sf_box_kg) ||
-            !encode_scale_map(&tmsb, q.SB, q.N, q.K, mats_b, p.sf_box_rb, p.sf_box_kg))
+            !(rep_b ? encode_scale_rep_map(&tmsb, q.SB, q.N, q.K, mats_b, p.sf_box_rb)
+                    : encode_scale_map(&tmsb, q.SB, q.N, q.K, mats_b, p.sf_box_rb, p.sf_box_kg)))
             return GEMM_ERR_LAUNCH;
         p.sf_x_bstride = q.sA == 0 ? 0 : mx_scale_bytes(q.M, q.K);
         p.sf_y_bstride = q.sB == 0 ? 0 : mx_scale_bytes(q.N, q.K);

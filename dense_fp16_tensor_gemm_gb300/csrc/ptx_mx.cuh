@@ -84,6 +84,32 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 5-D tiled load, completing on a barrier in either CTA of the pair: a scale
+// map whose third dimension has stride 0 lands each atom several times over.
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, int32_t c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
+// Shared-memory descriptor of a 128-row x 32-byte source for tcgen05.cp
+// .128x256b, no swizzle: row L's first 16 bytes at start + (L / 8) * 128 +
+// (L % 8) * 16 (8-row core matrices of 128 contiguous bytes), its second 16
+// bytes `lbo` bytes further on.
+__device__ __forceinline__ uint64_t rows32_desc(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(lbo >> 4) << 16;
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
 // The pair forms (cta_group::2), issued by the leader CTA of a pair: the copy
 // moves each CTA's atom at this shared offset into its own TMEM; each half of
 // the MMA reads the scales of its 128 rows of A, and of all N rows of B, from
@@ -91,6 +117,15 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
 __device__ __forceinline__ void tc_cp_atom_pair(uint32_t taddr, uint64_t sdesc)
 {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 128 rows of 32 bytes (shared) -> TMEM lane L, columns col..col+7, no
+// replication: with the source holding two atoms four times over (copy q of
+// atom h at h * lbo + 512 * q), every lane quadrant receives both atoms, as
+// two .32x128b.warpx4 copies would give it, in one instruction.
+__device__ __forceinline__ void tc_cp_rows32_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void tc_mma_pair_mx(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo,

@@ -47,8 +47,9 @@ constexpr int kTemptyArrivals = 2 * 8;         // one per epilogue warp, both CT
 // or 64 rows into a 128-row block, a 256-row one on a block, and either spans
 // exactly two atoms).  They come through a ring of two scale stages, each
 // holding the atoms of kScaleKb consecutive k-blocks (A: 4 KB in one box, B:
-// 8 KB in one box): small per-k-block scale loads beside the data loads slowed
-// the stream down by a third.  TMEM holds the accumulators PBN columns apart
+// 8 KB in one box): per-k-block 512-byte bulk copies of the atoms beside the
+// data loads slowed the stream down by a third.  (256-wide tiles take B's
+// atoms differently, see below.)  TMEM holds the accumulators PBN columns apart
 // (one at 256 wide) and, after them, 16 scale columns per data stage (A atom,
 // then the B atoms), filled by tcgen05.cp before the stage's MMAs.
 constexpr int kSfAtomsB = 2;
@@ -59,6 +60,13 @@ constexpr int kScaleStages = 2;
 // ones would leave TMEM no room for the scale slots.  Their epilogue warps
 // load their whole share of it into registers and free it at once, then
 // store, so the next tile's MMAs wait only for the TMEM reads.
+// Their B scales do not go through the scale ring: each data stage carries
+// the k-block's two B atoms four times over (4 KB, one TMA box of a map whose
+// copy dimension has stride 0), so that one non-replicating .128x256b copy
+// fills every lane quadrant.  Two replicating .32x128b.warpx4 copies per
+// k-block, beside A's, held the tensor pipe to about 80 % of its rate.  The
+// copier warp still issues the copies: issued by the MMA thread before each
+// k-block's MMAs, they made the 8192^3 product 28 % slower.
 template <int PBN, bool DIRECT, int KIND = 0>
 struct PairCfg {
     static constexpr bool MX = KIND == 2;
@@ -66,8 +74,10 @@ struct PairCfg {
     static constexpr int STAGES = SINGLE ? 6 : (DIRECT ? 7 : 6);
     static constexpr int B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
     static constexpr int DATA_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int SC_STAGE_BYTES = (1 + kSfAtomsB) * kScaleKb * 512;  // one scale stage
+    static constexpr int SFB_REP_BYTES = SINGLE ? kSfAtomsB * 4 * 512 : 0;  // per data stage
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFB_REP_BYTES;
+    // one scale stage: A's atoms, then (not SINGLE) B's
+    static constexpr int SC_STAGE_BYTES = (1 + (SINGLE ? 0 : kSfAtomsB)) * kScaleKb * 512;
     static constexpr int SC_BYTES = MX ? kScaleStages * SC_STAGE_BYTES : 0;
     static constexpr int ACC_STRIDE = MX ? PBN : 256;
     static constexpr int SF_COL = SINGLE ? PBN : 2 * PBN;
@@ -264,7 +274,10 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* as = smem;
     uint8_t* bs = smem + kStages * A_BYTES;
-    // block-scaled: scale stage t holds A's atoms [t][k] then B's [t][rb][k]
+    // block-scaled 256-wide: data stage s's B atoms, four times over, at
+    // sfb_rep + s * SFB_REP_BYTES as [row block h][copy q][512-byte atom]
+    uint8_t* sfb_rep = smem + kStages * C::DATA_BYTES;
+    // block-scaled: scale stage t holds A's atoms [t][k], then (192-wide) B's [t][rb][k]
     uint8_t* sfs = smem + kStages * STAGE_BYTES;
     float* epi = reinterpret_cast<float*>(sfs + C::SC_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sfs + C::SC_BYTES + EPI_BYTES);
@@ -341,8 +354,10 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;
-            // both CTAs' data loads of a stage, as credited (packed elements: global bytes)
-            const uint32_t data_tx = 2 * STAGE_BYTES * (p.ab_packed_bits ? p.ab_packed_bits : 8) / 8;
+            // both CTAs' loads of a stage, as credited (packed elements: global
+            // bytes), with (256-wide block-scaled) the replicated B atoms
+            const uint32_t data_tx = 2 * C::DATA_BYTES * (p.ab_packed_bits ? p.ab_packed_bits : 8) / 8 +
+                                     (C::SINGLE ? 2u * 4u * 512u * static_cast<uint32_t>(p.sf_box_rb) : 0u);
             int sst = 0;  // scale stage ring
             uint32_t sphase = 0, sc_filled = 0, sc_parity = 0;
             bool first = true, ok = true;
@@ -350,6 +365,9 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
             Seg s;
             while (ok && w.next(s)) {
                 const int yb = s.y0 + static_cast<int>(rank) * (PBN / 2);
+                // first scale row block of the tile's A rows and of its B rows
+                const int rbx = MX ? static_cast<int>((s.b * p.sf_x_bstride) / (512LL * p.num_kb)) + s.x0 / BM : 0;
+                const int rby = MX ? static_cast<int>((s.b * p.sf_y_bstride) / (512LL * p.num_kb)) + s.y0 / BM : 0;
                 for (int kb = s.kb0; kb < s.kb1; ++kb) {
                     if (MX && (kb == s.kb0 || kb % kScaleKb == 0)) {
                         // the next scale stage: atoms of k-blocks [kb - kb % 8, +8)
@@ -360,18 +378,17 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
                         }
                         const uint32_t sb_local = smem_u32(&sc_full[sst]);
                         if (leader) {
-                            // both CTAs' boxes: A's p.sf_box_kg atoms, B's p.sf_box_rb times as many
-                            mbar_arrive_expect_tx(sb_local, 2 * 512 * p.sf_box_kg * (1 + p.sf_box_rb));
+                            // both CTAs' boxes: A's p.sf_box_kg atoms, (192-wide) B's p.sf_box_rb times as many
+                            mbar_arrive_expect_tx(sb_local, 2 * 512 * p.sf_box_kg * (1 + (C::SINGLE ? 0 : p.sf_box_rb)));
                             sc_filled |= 1u << sst;
                             sc_parity = (sc_parity & ~(1u << sst)) | (sphase << sst);
                         }
                         const uint32_t sb_leader = mapa_shared(sb_local, 0);
                         const uint32_t sd = smem_u32(sfs + sst * C::SC_STAGE_BYTES);
                         const int kg0 = kb - kb % kScaleKb;
-                        const int rbx = static_cast<int>((s.b * p.sf_x_bstride) / (512LL * p.num_kb)) + s.x0 / BM;
-                        const int rby = static_cast<int>((s.b * p.sf_y_bstride) / (512LL * p.num_kb)) + s.y0 / BM;
                         tma_load_4d_pair(sd, &tmsa, sb_leader, 0, 0, kg0, rbx);
-                        tma_load_4d_pair(sd + kScaleKb * 512, &tmsb, sb_leader, 0, 0, kg0, rby);
+                        if (!C::SINGLE)
+                            tma_load_4d_pair(sd + kScaleKb * 512, &tmsb, sb_leader, 0, 0, kg0, rby);
                         if (++sst == kScaleStages) {
                             sst = 0;
                             sphase ^= 1;
@@ -396,6 +413,9 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
                                                s.x0, s.b * p.x_bmul);
                         load_operand<PBN / 2, true>(smem_u32(bs + stage * B_BYTES), &tmb, fb_leader, p.y_mn,
                                                     kb * KE, yb, s.b * p.y_bmul);
+                        if constexpr (C::SINGLE)
+                            tma_load_5d_pair(smem_u32(sfb_rep + stage * C::SFB_REP_BYTES), &tmsb, fb_leader, 0, 0, 0,
+                                             kb, rby);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -546,11 +566,17 @@ __global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 
                     const uint32_t sft = tmem_base + static_cast<uint32_t>(C::SF_COL + C::SF_COLS * stage);
                     const uint32_t j = static_cast<uint32_t>(kb % kScaleKb);
                     tc_cp_atom_pair(sft, atom_desc(sc_cur + j * 512));
-                    // B's box: row block a, K block group j at (a * box_kg + j); a B
-                    // row block past the tensor (box of one) holds only rows past N
+                    if constexpr (C::SINGLE) {
+                        // both B atoms from the data stage, each four times over: one copy
+                        tc_cp_rows32_pair(sft + 4, rows32_desc(smem_u32(sfb_rep + stage * C::SFB_REP_BYTES), 4 * 512));
+                    } else {
+                        // B's box: row block a, K block group j at (a * box_kg + j); a B
+                        // row block past the tensor (box of one) holds only rows past N
 #pragma unroll
-                    for (int a = 0; a < kSfAtomsB; ++a)
-                        tc_cp_atom_pair(sft + 4 + 4 * a, atom_desc(sc_cur + (kScaleKb + a * p.sf_box_kg + j) * 512));
+                        for (int a = 0; a < kSfAtomsB; ++a)
+                            tc_cp_atom_pair(sft + 4 + 4 * a,
+                                            atom_desc(sc_cur + (kScaleKb + a * p.sf_box_kg + j) * 512));
+                    }
                     tc_commit_pair(smem_u32(&sf_ready[stage]));
                     issued = true;
                     if (kb % kScaleKb == kScaleKb - 1 || kb == s.kb1 - 1) {
