@@ -147,6 +147,23 @@ def test_pair_tile_windows(M, N, K):
     check_tol(run_mx(A, SA, B, SB, "e5m2", "f32", P.TC05_PAIR), ref, absdot, "f32", "pair %dx%dx%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("batch,M,N,K,ab,shared", [(1, 300, 96, 384, "e4m3", False), (3, 200, 264, 512, "e4m3", False),
+                                                    (2, 260, 264, 256, "e5m2", True), (2, 257, 520, 640, "e2m1", False)])
+def test_single_accumulator_scale_boxes(batch, M, N, K, ab, shared):
+    """256 x 256 pair tiles (Out rows 32-byte aligned) take B's scale atoms in
+    each data stage, four times over: N = 96 (one row block, a box of one),
+    batches whose B row blocks follow one another in the packed scales, B and
+    its scales shared by every batch, and packed 4-bit elements.  Integer
+    inputs and scales 2^-3..2^3 make every result exact."""
+    A, SA, B, SB = draw(batch, M, N, K, ab, dist="int4", seed=507 + N, lo=124, hi=131)
+    if shared:
+        B = np.repeat(B[:1], batch, axis=0)
+        SB = np.repeat(SB[:1], batch, axis=0)
+    ref, _ = oracle.gemm_nt_mx(A, SA, B, SB, dtype=ab)
+    out = run_mx(A, SA, B, SB, ab, "f32", P.TC05_PAIR, shared_b=shared)
+    check_exact(out, ref, "f32", "pair %d x %dx%dx%d %s%s" % (batch, M, N, K, ab, " shared B" if shared else ""))
+
+
 def test_unit_scales_equal_the_unscaled_product():
     """Scales of 127 on the device give the unscaled 8-bit kernel's result
     (both fp32-accumulated, compared through the oracle)."""
