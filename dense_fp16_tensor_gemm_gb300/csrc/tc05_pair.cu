@@ -10,8 +10,12 @@
 // tile, each SM moves 32 KB per k-block from L2 instead of 48 KB for the same
 // MMA work.
 //
-// Roles per CTA (320 threads): warp 0 producer, warp 1 TMEM allocation (both
-// CTAs) and MMA issue (leader only), warps 2-9 epilogue.  Synchronisation:
+// Roles per CTA (352 threads): warp 0 producer, warp 1 TMEM allocation (both
+// CTAs) and MMA issue (leader only), warps 2-9 epilogue, warp 10 the scale
+// copier of block-scaled kernels (others launch it too and it exits at once:
+// under the 352-thread launch bound ptxas spills less in the staged-epilogue
+// kernels, whose 16 x 3001 x 2047 x 1000 product ran 185 against 190 us with
+// 320 threads).  Synchronisation:
 //   full[s]    in the leader: its producer posts the byte count of both CTAs'
 //              loads; both CTAs' TMA loads complete on it
 //   empty[s]   in each CTA: the leader's MMA commit arrives on both (multicast)
@@ -254,9 +258,9 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
 }
 
 // F8: 8-bit A and B (kind::f8f6f4, 128 elements of K per 128-byte stage row).
-// Block-scaled kernels add warp 10, which copies the scale atoms into TMEM.
+// Block-scaled kernels give warp 10 the copy of the scale atoms into TMEM.
 template <int PBN, bool DIRECT, int KIND>
-__global__ void __launch_bounds__(KIND == 2 ? kPairThreads + 32 : kPairThreads, 1)
+__global__ void __launch_bounds__(kPairThreads + 32, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const __grid_constant__ CUtensorMap tmsa, const __grid_constant__ CUtensorMap tmsb,
                      const TcParams p)
@@ -701,7 +705,7 @@ cudaError_t configure_kind(int* max_pairs)
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr, KIND == 2 ? kPairThreads + 32 : kPairThreads);
+    cudaLaunchConfig_t cfg = pair_config(2, C::SMEM, nullptr, attr, kPairThreads + 32);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, tc05_pair_kernel<PBN, DIRECT, KIND>, &cfg);
     if (e != cudaSuccess)
@@ -723,7 +727,7 @@ cudaError_t launch_kind(const CUtensorMap& tma, const CUtensorMap& tmb, const CU
 {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(2 * pairs, PairCfg<PBN, DIRECT, KIND>::SMEM, stream, attr,
-                                         KIND == 2 ? kPairThreads + 32 : kPairThreads);
+                                         kPairThreads + 32);
     return cudaLaunchKernelEx(&cfg, tc05_pair_kernel<PBN, DIRECT, KIND>, tma, tmb, tmsa, tmsb, p);
 }
 
