@@ -12,10 +12,11 @@
 //
 // Roles per CTA (352 threads): warp 0 producer, warp 1 TMEM allocation (both
 // CTAs) and MMA issue (leader only), warps 2-9 epilogue, warp 10 the scale
-// copier of block-scaled kernels (others launch it too and it exits at once:
-// under the 352-thread launch bound ptxas spills less in the staged-epilogue
-// kernels, whose 16 x 3001 x 2047 x 1000 product ran 185 against 190 us with
-// 320 threads).  Synchronisation:
+// copier of block-scaled kernels (others launch it too and it exits at once).
+// The kernels are compiled for up to 384 threads: under that bound ptxas
+// spills nothing (under 320 the staged-epilogue instances spilled, and their
+// 16 x 3001 x 2047 x 1000 product ran 190 us, against 183 us now).
+// Synchronisation:
 //   full[s]    in the leader: its producer posts the byte count of both CTAs'
 //              loads; both CTAs' TMA loads complete on it
 //   empty[s]   in each CTA: the leader's MMA commit arrives on both (multicast)
@@ -260,7 +261,7 @@ __device__ __forceinline__ void sk_epilogue(const TcParams& p, const Seg& s, uin
 // F8: 8-bit A and B (kind::f8f6f4, 128 elements of K per 128-byte stage row).
 // Block-scaled kernels give warp 10 the copy of the scale atoms into TMEM.
 template <int PBN, bool DIRECT, int KIND>
-__global__ void __launch_bounds__(kPairThreads + 32, 1)
+__global__ void __launch_bounds__(kPairThreads + 64, 1)
     tc05_pair_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
                      const __grid_constant__ CUtensorMap tmsa, const __grid_constant__ CUtensorMap tmsb,
                      const TcParams p)
