@@ -53,14 +53,14 @@ PACKED_BITS = {"e2m3": 6, "e3m2": 6, "e2m1": 4}
 # sha256 of the kernel source it was taken on; reported as null once the kernel
 # source no longer matches.
 TRAFFIC = {
-    "square_8192": (1071864320 + 249641216, "6da15f6dd9fa44ab"),
-    "square_4096": (91443968 + 35110656, "6da15f6dd9fa44ab"),
-    "ragged_batch16_3001x2047x1000": (163064576 + 335357952, "6da15f6dd9fa44ab"),
+    "square_8192": (1074521600 + 248043520, "dfb399817f9f0705"),
+    "square_4096": (91492352 + 34789888, "dfb399817f9f0705"),
+    "ragged_batch16_3001x2047x1000": (162286592 + 332889344, "dfb399817f9f0705"),
     "skinny_64x16384x8192": (269563136 + 2948352, "1c2d3c01ce774de5"),
     # block-scaled E4M3 and E2M1 inputs (--ab-dtype e4m3 / e2m1 --mx), packed E2M1 (--ab-dtype e2m1)
-    "square_8192/mx-e4m3": (357480704 + 235872000, "6da15f6dd9fa44ab"),
-    "square_8192/mx-e2m1": (170795776 + 217559552, "6da15f6dd9fa44ab"),
-    "square_8192/e2m1": (155943680 + 215941632, "6da15f6dd9fa44ab"),
+    "square_8192/mx-e4m3": (358762240 + 234705152, "dfb399817f9f0705"),
+    "square_8192/mx-e2m1": (171194624 + 217513216, "dfb399817f9f0705"),
+    "square_8192/e2m1": (156736768 + 216092416, "dfb399817f9f0705"),
     # the weight-stationary shape on the skinny product (--path TC05_WS)
     "skinny_64x16384x8192/TC05_WS": (278262528 + 5557504, "0de165ee5081595b"),
 }
